@@ -1,0 +1,219 @@
+"""Pins of the scheduler / K/V-pool oracle against what the pages print."""
+
+import json
+import os
+import random
+
+import pytest
+
+from oracle import sched
+from oracle.kv import KVPool
+from iteration_level_scheduling_gb300 import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def load(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def specs_from_lengths(lengths, prompt_len=1):
+    return [synth.RequestSpec(i, 0.0, [1] * prompt_len, L) for i, L in enumerate(lengths)]
+
+
+# --------------------------------------------------------------------------- #
+# [ultralytics] worked simulation: 90 / 50 steps, 43% / 78% busy
+# --------------------------------------------------------------------------- #
+def test_worked_example_closed_forms():
+    g = load("ultralytics_slot_simulation.json")
+    outs, S = g["output_lengths"], g["slots"]
+    assert sched.static_steps(outs, S) == g["static_steps"]
+    assert sched.continuous_steps(outs, S) == g["continuous_steps"]
+    assert f"{sched.slots_busy(sum(outs), g['static_steps'], S):.0%}" == g["static_slots_busy"]
+    assert f"{sched.slots_busy(sum(outs), g['continuous_steps'], S):.0%}" == g["continuous_slots_busy"]
+
+
+@pytest.mark.parametrize("mode,key", [("iteration", "continuous"), ("request", "static")])
+def test_worked_example_schedulers(mode, key):
+    g = load("ultralytics_slot_simulation.json")
+    outs, S = g["output_lengths"], g["slots"]
+    s, recs = sched.run(specs_from_lengths(outs), max_batch=S, max_tokens=4096, kv_slots=10 ** 6, mode=mode)
+    assert len(recs) == g[f"{key}_steps"]
+    assert s.generated_total == sum(outs)
+    assert f"{sched.slots_busy(s.generated_total, len(recs), S):.0%}" == g[f"{key}_slots_busy"]
+    assert all(len(r.rids) <= S for r in recs)
+
+
+def test_worked_example_with_prompts():
+    """Prompt lengths do not change the step counts (one token per iteration)."""
+    g = load("ultralytics_slot_simulation.json")
+    reqs = synth.tiny_requests(0)
+    assert [r.out_len for r in reqs] == g["output_lengths"]
+    s, recs = sched.run(reqs, max_batch=4, max_tokens=4096, kv_slots=4 * 128)
+    assert len(recs) == 50
+    s, recs = sched.run(reqs, max_batch=4, max_tokens=4096, kv_slots=4 * 128, mode="request")
+    assert len(recs) == 90
+
+
+def test_closed_form_equals_scheduler_random():
+    """With every request present at time 0 the iteration-level scheduler is the
+    slot model of the closed form; the request-level one is the group model."""
+    rnd = random.Random(5)
+    for _ in range(200):
+        n = rnd.randint(1, 14)
+        S = rnd.randint(1, 5)
+        outs = [rnd.randint(1, 30) for _ in range(n)]
+        _, recs = sched.run(specs_from_lengths(outs), S, 4096, 10 ** 6)
+        assert len(recs) == sched.continuous_steps(outs, S)
+        _, recs = sched.run(specs_from_lengths(outs), S, 4096, 10 ** 6, mode="request")
+        assert len(recs) == sched.static_steps(outs, S)
+
+
+# --------------------------------------------------------------------------- #
+# [estelledc] case 1: D joins at step 11, E at 51, F at 101
+# --------------------------------------------------------------------------- #
+def test_case1_join_steps():
+    g = load("estelledc_case1.json")
+    first = g["first_requests"]
+    names = list(first) + list(g["continuous_join_step_1_indexed"])
+    outs = [first["A"], first["B"], first["C"], 500, 500, 500]
+    s, recs = sched.run(specs_from_lengths(outs), g["slots"], 4096, 10 ** 6, token_fn=lambda it: [0] * len(it.rids))
+    by_id = {r.rid: r for r in s.reqs}
+    for j, name in enumerate(names[3:]):
+        assert by_id[3 + j].admitted_at + 1 == g["continuous_join_step_1_indexed"][name]
+    for rec in recs[:100]:
+        assert len(rec.rids) == 3  # the batch never has an idle slot
+
+
+def test_case1_static_phases():
+    g = load("estelledc_case1.json")
+    first = g["first_requests"]
+    _, recs = sched.run(specs_from_lengths([first["A"], first["B"], first["C"]]), 3, 4096, 10 ** 6, mode="request")
+    names = {0: "A", 1: "B", 2: "C"}
+    for lo, hi, members in g["static_phases_1_indexed"]:
+        for step in range(lo, hi + 1):
+            assert sorted(names[r] for r in recs[step - 1].rids) == sorted(members)
+    assert len(recs) == 100
+
+
+# --------------------------------------------------------------------------- #
+# [houmin] the (x1, x2, x3, x4) batch: 7 flattened rows
+# --------------------------------------------------------------------------- #
+def test_houmin_batch_descriptor():
+    g = load("houmin_selective_batch.json")
+    specs = [synth.RequestSpec(1, 0.0, [11, 12], 10), synth.RequestSpec(2, 1.0, [21], 10),
+             synth.RequestSpec(3, 2.0, [31, 32], 10), synth.RequestSpec(4, 2.0, [41, 42, 43], 10)]
+    s, recs = sched.run(specs, 4, 4096, 10 ** 6, token_fn=lambda it: [0] * len(it.rids), max_iters=3)
+    it = recs[2]
+    assert it.rids == [1, 2, 3, 4]
+    assert it.phase == [1, 1, 0, 0]
+    assert it.n_input == [1, 1, 2, 3]
+    assert it.offsets[-1] == g["rows_batch"]
+    assert it.offsets[4] - it.offsets[2] == g["rows_x3_x4"]
+    by = {r.rid: r for r in s.reqs}
+    # token index of the token each request returns at this iteration
+    for name, idx in g["returned_token_index"].items():
+        r = by[int(name[1])]
+        assert len(r.prompt) + len(r.generated) == idx
+
+
+# --------------------------------------------------------------------------- #
+# [0h-n0] admission pseudocode: reservation, stall when full, no overtaking
+# --------------------------------------------------------------------------- #
+def test_kv_full_stall_and_fcfs():
+    # pool of 100 tokens; each request reserves prompt + output
+    specs = [synth.RequestSpec(0, 0.0, [1] * 10, 50),  # 60
+             synth.RequestSpec(1, 0.0, [1] * 10, 40),  # 50 -> does not fit beside 60
+             synth.RequestSpec(2, 0.0, [1] * 5, 5)]    # 10 -> would fit, but must not overtake
+    s, recs = sched.run(specs, 8, 4096, 100)
+    assert recs[0].rids == [0]
+    by = {r.rid: r for r in s.reqs}
+    assert by[1].admitted_at == by[0].finished_at + 1
+    assert by[2].admitted_at == by[1].admitted_at
+    assert by[1].kv_off == 0 and by[2].kv_off == 50
+
+
+def test_token_budget():
+    specs = [synth.RequestSpec(i, 0.0, [1] * 30, 3) for i in range(5)]
+    s, recs = sched.run(specs, 8, 64, 10 ** 6)
+    assert recs[0].rids == [0, 1] and sum(recs[0].n_input) == 60
+    for r in recs:
+        assert sum(r.n_input) <= 64
+
+
+def test_invariants_random_traces():
+    for seed in range(6):
+        rnd = random.Random(seed)
+        trace = synth.poisson_trace(seed, n=60, rate=rnd.choice([0.2, 0.5, 2.0]), prompt_range=(1, 40),
+                                    out_range=(1, 30), vocab=100)
+        max_batch, max_tokens, slots = rnd.randint(1, 8), rnd.randint(40, 200), rnd.randint(80, 400)
+        s, recs = sched.run(trace, max_batch, max_tokens, slots)
+        admitted = sorted((r for r in s.reqs), key=lambda r: (r.admitted_at, r.arrival, r.rid))
+        order = sorted(s.reqs, key=lambda r: (r.arrival, r.rid))
+        assert [r.rid for r in admitted] == [r.rid for r in order]  # FCFS, never overtaken
+        live = {}
+        for rec in recs:
+            assert 1 <= len(rec.rids) <= max_batch
+            assert sum(rec.n_input) <= max_tokens
+            for rid, ph, n, c in zip(rec.rids, rec.phase, rec.n_input, rec.ctx):
+                assert (ph == 0) == (c == 0)
+        # reservations never overlap and stay inside the pool
+        for r in s.reqs:
+            assert r.state == "finished" and len(r.generated) == r.out_len
+        assert s.pool.used() == 0 and s.pool.free_list == [(0, slots)]
+        # replay the reservation intervals per iteration
+        for rec in recs:
+            iv = sorted(zip(rec.kv_off, [s.reserve_size(r) for r in (next(q for q in s.reqs if q.rid == x) for x in rec.rids)]))
+            for (o1, l1), (o2, _) in zip(iv, iv[1:]):
+                assert o1 + l1 <= o2
+            assert all(o + l <= slots for o, l in iv)
+
+
+# --------------------------------------------------------------------------- #
+# K/V pool: first fit at the lowest address, coalescing frees
+# --------------------------------------------------------------------------- #
+def test_kv_pool_script():
+    p = KVPool(100)
+    assert p.alloc(1, 30) == 0
+    assert p.alloc(2, 30) == 30
+    assert p.alloc(3, 30) == 60
+    assert p.alloc(4, 20) is None
+    p.free(2)
+    assert p.alloc(5, 10) == 30  # first fit in the hole
+    assert p.alloc(6, 25) is None  # hole left is 20, tail is 10
+    assert p.alloc(7, 20) == 40
+    assert p.alloc(8, 10) == 90
+    p.free(1)
+    p.free(5)
+    assert p.free_list == [(0, 40)]  # merged across the freed neighbours
+    p.free(7)
+    p.free(3)
+    p.free(8)
+    assert p.free_list == [(0, 100)] and p.used() == 0
+
+
+def test_kv_pool_random_no_overlap():
+    rnd = random.Random(1)
+    p = KVPool(500)
+    live = {}
+    for step in range(3000):
+        if live and rnd.random() < 0.45:
+            rid = rnd.choice(sorted(live))
+            p.free(rid)
+            del live[rid]
+        else:
+            rid = step
+            n = rnd.randint(1, 80)
+            off = p.alloc(rid, n)
+            # brute force: the lowest offset where n slots are free
+            busy = [False] * 500
+            for o, l in live.values():
+                for t in range(o, o + l):
+                    busy[t] = True
+            expect = next((o for o in range(500 - n + 1) if not any(busy[o:o + n])), None)
+            assert off == expect
+            if off is not None:
+                live[rid] = (off, n)
+        assert p.used() == sum(l for _, l in live.values())
+        assert sum(l for _, l in p.free_list) == 500 - p.used()
