@@ -1,0 +1,291 @@
+// Attention of one layer, split per request and merged back by indexing.
+//
+// Selective batching ("論文解説: Orca", Selective Batching; garden.houmin.site
+// Orca notes, 3.1.2 "方案"): the [sum L, 3H] projection is split by request,
+// attention runs per request over that request's own K/V, and the outputs are
+// merged back into [sum L, H].  Here the split and the merge are the prefix-sum
+// row offsets: each CTA reads its request's q rows straight out of the qkv
+// matrix and writes its output rows straight into the attention matrix, so no
+// copy is made.  The page notes that attention has no weights to share across
+// requests, so not batching it costs little; what it costs is the K/V read,
+// which is what these kernels stream.
+//
+// K/V pool layout per layer: [K|V][head][slot][head_dim], so the keys of one
+// head of one request are contiguous (head_dim * elem bytes per token).
+//
+// decode  : requests with one input row (increment phase).  Work item =
+//           (request, chunk of `chunk` keys) x head; a request whose keys span
+//           several chunks is merged by the last CTA to finish (per-(request,
+//           head) arrival counter; no CTA ever waits on another).
+// prefill : requests with several input rows (initiation phase, or any
+//           multi-row request).  Work item = (request, 16 query rows) x head;
+//           each warp owns one query row and attends causally over keys
+//           0..pos of its request.
+// Scores use exp2 with log2(e)/sqrt(head_dim) folded into q; the softmax is
+// the online (running max / running sum) form, exact up to rounding.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace orca {
+
+namespace {
+
+constexpr int kAttnThreads = 128;
+constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr float kNegBig = -1e30f;
+
+template <typename T>
+struct AttnArgs {
+    const T *qkv;
+    const T *kpool;  // layer's K block: [head][slot][D]
+    const T *vpool;
+    int64_t kv_slots;
+    T *out;
+    int H, n_heads;
+    float scale_log2;
+    AttnPlan p;
+    float *part;
+    int *counters;
+};
+
+// One warp attends its query (q, already scaled, VEC values of its lane's
+// slice) to keys t in [t_begin, t_end) of one head, the lane group g of the
+// warp taking tokens t_begin + g + j*step for j = 0, 1, ...  Updates the lane's
+// running (m, l, o).  The loop trip count is uniform across the warp.
+template <typename T, int D, int U>
+__device__ __forceinline__ void attend_range(const float *q, const T *kb, const T *vb, int t_begin, int t_end,
+                                             int step, float &m, float &l, float *o) {
+    constexpr int VEC = Elem<T>::kPer16;
+    constexpr int LPT = D / VEC;
+    const int g = (threadIdx.x & 31) / LPT;
+    for (int base = t_begin; base < t_end; base += step * U) {
+        float kk[U][VEC], vv[U][VEC];
+        bool valid[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int t = base + g + u * step;
+            valid[u] = t < t_end;
+            if (valid[u]) {
+                load16_stream(kb + (size_t)t * D, kk[u]);
+                load16_stream(vb + (size_t)t * D, vv[u]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) kk[u][e] = 0.f, vv[u][e] = 0.f;
+            }
+        }
+        float s[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc = fmaf(q[e], kk[u][e], acc);
+#pragma unroll
+            for (int off = LPT / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            s[u] = valid[u] ? acc : kNegBig;
+        }
+        float mx = m;
+#pragma unroll
+        for (int u = 0; u < U; ++u) mx = fmaxf(mx, s[u]);
+        const float corr = exp2f(m - mx);
+        l *= corr;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[e] *= corr;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float pr = valid[u] ? exp2f(s[u] - mx) : 0.f;
+            l += pr;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[e] = fmaf(pr, vv[u][e], o[e]);
+        }
+        m = mx;
+    }
+}
+
+// Merge the running states of the lane groups of a warp (lanes with the same
+// slice of head_dim); afterwards every lane holds the warp's total for its slice.
+template <int LPT, int VEC>
+__device__ __forceinline__ void merge_groups(float &m, float &l, float *o) {
+#pragma unroll
+    for (int off = LPT; off < 32; off <<= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+        const float mx = fmaxf(m, m2);
+        const float c1 = exp2f(m - mx), c2 = exp2f(m2 - mx);
+        l = l * c1 + l2 * c2;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const float o2 = __shfl_xor_sync(0xffffffffu, o[e], off);
+            o[e] = o[e] * c1 + o2 * c2;
+        }
+        m = mx;
+    }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArgs<T> a) {
+    constexpr int VEC = Elem<T>::kPer16;
+    constexpr int LPT = D / VEC;
+    constexpr int TPW = 32 / LPT;
+    constexpr int U = 4;
+    __shared__ float sm_m[kAttnWarps], sm_l[kAttnWarps];
+    __shared__ float sm_o[kAttnWarps][D];
+    __shared__ int sm_last;
+
+    const int w_idx = blockIdx.x, h = blockIdx.y;
+    const int i = a.p.dec_work[2 * w_idx], c = a.p.dec_work[2 * w_idx + 1];
+    const int row = a.p.req_off[i];
+    const int n_keys = a.p.req_ctx[i] + 1;
+    const int t0 = c * a.p.chunk, t1 = min(n_keys, t0 + a.p.chunk);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane % LPT;
+
+    float q[VEC];
+    load16(a.qkv + (size_t)row * 3 * a.H + h * D + sub * VEC, q);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) q[e] *= a.scale_log2;
+    const size_t head_base = ((size_t)h * a.kv_slots + a.p.req_kvoff[i]) * D + sub * VEC;
+    float m = kNegBig, l = 0.f, o[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) o[e] = 0.f;
+    attend_range<T, D, U>(q, a.kpool + head_base, a.vpool + head_base, t0 + warp * TPW, t1, kAttnWarps * TPW, m, l,
+                          o);
+    merge_groups<LPT, VEC>(m, l, o);
+    if (lane < LPT) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) sm_o[warp][sub * VEC + e] = o[e];
+    }
+    if (lane == 0) sm_m[warp] = m, sm_l[warp] = l;
+    __syncthreads();
+
+    const int nch = a.p.dec_nch[i];
+    float M = kNegBig, L = 0.f, O = 0.f;
+    const int d = threadIdx.x;
+    if (d < D) {
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, sm_m[w]);
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) {
+            const float cw = exp2f(sm_m[w] - M);
+            L += sm_l[w] * cw;
+            O += sm_o[w][d] * cw;
+        }
+    }
+    T *dst = a.out + (size_t)row * a.H + h * D;
+    if (nch == 1) {
+        if (d < D) dst[d] = Elem<T>::from_f(O / L);
+        return;
+    }
+    // several chunks: publish the partial, the last CTA of (request, head) merges
+    float *mine = a.part + ((size_t)w_idx * a.n_heads + h) * (D + 2);
+    if (d < D) mine[d] = O;
+    if (d == 0) mine[D] = M, mine[D + 1] = L;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int old = atomicAdd(&a.counters[i * a.n_heads + h], 1);
+        sm_last = (old == nch - 1);
+    }
+    __syncthreads();
+    if (!sm_last) return;
+    __threadfence();
+    if (d < D) {
+        const int wb = a.p.dec_wbegin[i];
+        float Mt = kNegBig;
+        for (int j = 0; j < nch; ++j) Mt = fmaxf(Mt, __ldcg(a.part + ((size_t)(wb + j) * a.n_heads + h) * (D + 2) + D));
+        float Lt = 0.f, Ot = 0.f;
+        for (int j = 0; j < nch; ++j) {
+            const float *pj = a.part + ((size_t)(wb + j) * a.n_heads + h) * (D + 2);
+            const float cw = exp2f(__ldcg(pj + D) - Mt);
+            Lt += __ldcg(pj + D + 1) * cw;
+            Ot += __ldcg(pj + d) * cw;
+        }
+        dst[d] = Elem<T>::from_f(Ot / Lt);
+    }
+    if (threadIdx.x == 0) a.counters[i * a.n_heads + h] = 0;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kAttnThreads) attn_prefill_kernel(const AttnArgs<T> a) {
+    constexpr int VEC = Elem<T>::kPer16;
+    constexpr int LPT = D / VEC;
+    constexpr int TPW = 32 / LPT;
+    constexpr int U = 4;
+    const int tile = blockIdx.x, h = blockIdx.y;
+    const int i = a.p.pre_tiles[2 * tile], r0 = a.p.pre_tiles[2 * tile + 1];  // r0: first row within the request
+    const int off = a.p.req_off[i];
+    const int n = a.p.req_off[i + 1] - off;
+    const int ctx = a.p.req_ctx[i];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane % LPT;
+    const size_t head_base = ((size_t)h * a.kv_slots + a.p.req_kvoff[i]) * D + sub * VEC;
+    const int r_end = min(n, r0 + kPrefillRowsPerTile);
+    for (int r = r0 + warp; r < r_end; r += kAttnWarps) {
+        const int row = off + r;
+        const int pos = ctx + r;
+        float q[VEC];
+        load16(a.qkv + (size_t)row * 3 * a.H + h * D + sub * VEC, q);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) q[e] *= a.scale_log2;
+        float m = kNegBig, l = 0.f, o[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[e] = 0.f;
+        attend_range<T, D, U>(q, a.kpool + head_base, a.vpool + head_base, 0, pos + 1, TPW, m, l, o);
+        merge_groups<LPT, VEC>(m, l, o);
+        if (lane < LPT) {
+            float res[VEC];
+            const float inv = 1.f / l;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) res[e] = o[e] * inv;
+            store16(a.out + (size_t)row * a.H + h * D + sub * VEC, res);
+        }
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStream_t st) {
+    if (decode && a.p.n_dec_work > 0) {
+        attn_decode_kernel<T, D><<<dim3(a.p.n_dec_work, a.n_heads), kAttnThreads, 0, st>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (prefill && a.p.n_pre_tiles > 0) {
+        attn_prefill_kernel<T, D><<<dim3(a.p.n_pre_tiles, a.n_heads), kAttnThreads, 0, st>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *out, const AttnPlan &p, int H,
+                      int n_heads, float *part, int *counters, cudaStream_t st, bool decode, bool prefill) {
+    const int D = H / n_heads;
+    AttnArgs<T> a;
+    a.qkv = qkv;
+    a.kpool = pool_layer;
+    a.vpool = pool_layer + (size_t)n_heads * kv_slots * D;
+    a.kv_slots = kv_slots;
+    a.out = out;
+    a.H = H;
+    a.n_heads = n_heads;
+    a.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+    a.p = p;
+    a.part = part;
+    a.counters = counters;
+    switch (D) {
+        case 16: return launch_attn<T, 16>(a, decode, prefill, st);
+        case 32: return launch_attn<T, 32>(a, decode, prefill, st);
+        case 64: return launch_attn<T, 64>(a, decode, prefill, st);
+        case 128: return launch_attn<T, 128>(a, decode, prefill, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template cudaError_t attention<float>(const float *, const float *, int64_t, float *, const AttnPlan &, int, int,
+                                      float *, int *, cudaStream_t, bool, bool);
+template cudaError_t attention<bf16>(const bf16 *, const bf16 *, int64_t, bf16 *, const AttnPlan &, int, int,
+                                     float *, int *, cudaStream_t, bool, bool);
+
+}  // namespace orca

@@ -1,0 +1,349 @@
+// Flattened linear layers on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Selective batching applies every non-attention operation to all requests'
+// rows at once, as one [sum L, H] matrix ("論文解説: Orca", Selective Batching;
+// garden.houmin.site Orca notes, 3.1.2): the weights are read once per
+// iteration for the whole batch.  The notes also observe that increment-phase
+// rows make these projections GEMV-like and initiation rows GEMM-like, so one
+// kernel has to serve sum L from 1 to tens of thousands.
+//
+// Orientation ("swap AB"): the weight is the MMA's A operand (M = 128 output
+// features per CTA), the token rows are the B operand (N = BN tokens, a
+// multiple of 16 up to 256).  Both are K-major in memory (w[f, k], x[t, k]), so
+// TMA loads 64-wide K slices with 128-byte swizzling straight into the layout
+// tcgen05.mma reads.  The fp32 accumulator tile (128 lanes x BN columns) lives
+// in tensor memory; lane = output feature, column = token.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
+// single-thread MMA issuer, warps 2-5 = epilogue (each reads its 32-lane
+// quarter of TMEM).  A ring of `stages` shared-memory stages with full/empty
+// mbarriers decouples loads from MMAs; tcgen05.commit releases a stage when the
+// MMAs reading it are done.
+//
+// Small sum L (decode) gives few output tiles, so K is split across CTAs
+// (split-K); each CTA writes an fp32 partial tile and the last CTA of the tile
+// to arrive (atomic counter, no waiting) sums the partials in split order and
+// runs the epilogue.  Epilogue: + bias, exact GeLU, + residual (fp32), store
+// fp32 or bf16 rows [token, feature] (coalesced along features).
+//
+// Every mbarrier wait is bounded (see common.cuh); on expiry the CTA records
+// an error bit, skips its remaining work and still frees its tensor memory.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace orca {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr int kMaxStages = 8;
+constexpr int kStageA = BM * BK * 2;  // 16 KiB
+constexpr int kGroup = 16;            // feature tiles per raster group
+constexpr size_t kSmemPerSm = 228 * 1024;
+constexpr size_t kSmemMaxCta = 227 * 1024;
+constexpr size_t kSmemReserve = 1024;  // per CTA, kept by the driver
+
+struct TcArgs {
+    int m_tok, n_out, num_kb, kb_per_split, splits, bn, stages;
+    int n_feat_tiles, n_tok_tiles;
+    uint32_t idesc, tmem_cols;
+    Epilogue e;
+    float *ws;
+    int *counters;
+    unsigned *err;
+};
+
+__device__ __forceinline__ void tile_coords(int lin, const TcArgs &a, int &ft, int &tt) {
+    const int per_group = kGroup * a.n_tok_tiles;
+    const int g = lin / per_group;
+    const int first = g * kGroup;
+    const int gsize = min(a.n_feat_tiles - first, kGroup);
+    const int r = lin - g * per_group;
+    ft = first + r % gsize;
+    tt = r / gsize;
+}
+
+__device__ __forceinline__ void epilogue_store(const Epilogue &e, int t, int f, float y, float bias) {
+    y += bias;
+    if (e.gelu) y = gelu_erf(y);
+    const size_t o = (size_t)t * e.ld_out + f;
+    if (e.resid)
+        e.out_f32[o] = e.resid[o] + y;
+    else if (e.out_f32)
+        e.out_f32[o] = y;
+    else
+        e.out_bf16[o] = __float2bfloat16_rn(y);
+}
+
+// AND of `v` over the 128 epilogue threads (named barrier 1).
+__device__ __forceinline__ bool epilogue_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int stage_b = a.bn * BK * 2;
+    const int stage_bytes = kStageA + stage_b;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.stages * stage_bytes);
+    uint64_t *empty = full + kMaxStages;
+    uint64_t *done = empty + kMaxStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);  // [0] abort, [1] last arriver
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int ft, tt;
+    tile_coords(blockIdx.x, a, ft, tt);
+    const int split = blockIdx.y;
+    const int kb0 = split * a.kb_per_split;
+    const int nkb = min(a.num_kb, kb0 + a.kb_per_split) - kb0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmw);
+        prefetch_tmap(&tmx);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // with one token tile the weights are read exactly once: stream them past L2
+            const bool stream_w = a.n_tok_tiles == 1;
+            const uint64_t pol_w = l2_policy_evict_first();
+            int issued = 0;
+            bool ok = true;
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % a.stages;
+                const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
+                if (!mbar_wait_bounded(&empty[s], ph ^ 1u, a.err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
+                uint8_t *sa = smem + (size_t)s * stage_bytes;
+                if (stream_w)
+                    tma_load_2d_hint(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM, pol_w);
+                else
+                    tma_load_2d(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM);
+                tma_load_2d(sa + kStageA, &tmx, &full[s], (kb0 + i) * BK, tt * a.bn);
+                ++issued;
+            }
+            if (!ok) {
+                flags[0] = 1;
+                // let the copies already in flight land before the CTA exits
+                for (int j = max(0, issued - a.stages); j < issued; ++j)
+                    mbar_wait_bounded(&full[j % a.stages], (uint32_t)(j / a.stages) & 1u, a.err);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = true;
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % a.stages;
+                const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
+                if (!mbar_wait_bounded(&full[s], ph, a.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+                const uint64_t ad = smem_desc_k128(sa), bd = smem_desc_k128(sa + kStageA);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)  // 16 bf16 = 32 B per MMA: +2 in the >>4 address field
+                    tc_mma_f16(tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), a.idesc,
+                               (uint32_t)((i | kk) != 0));
+                tc_commit(&empty[s]);
+            }
+            if (ok) {
+                tc_commit(done);
+            } else {
+                flags[0] = 1;
+                mbar_arrive(done);
+            }
+        }
+    } else {
+        // ------------------------------ epilogue ------------------------------
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;  // output feature within the tile
+        const int f = ft * BM + row;
+        const bool f_ok = f < a.n_out;
+        const int t_base = tt * a.bn;
+        const int t_lim = min(a.bn, a.m_tok - t_base);  // valid token columns
+        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+        bool ok = mbar_wait_bounded(done, 0, a.err);
+        tc_fence_after();
+        ok = ok && flags[0] == 0;
+        ok = epilogue_all(ok);  // the four epilogue warps take the same branch
+        const float bias = (a.e.bias && f_ok) ? a.e.bias[f] : 0.f;
+        __syncwarp();  // tcgen05.ld is .sync.aligned: the warp must be converged
+        if (ok && a.splits == 1) {
+            for (int c0 = 0; c0 < t_lim; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr + c0, v);
+                if (f_ok) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (c0 + j < t_lim) epilogue_store(a.e, t_base + c0 + j, f, v[j], bias);
+                }
+            }
+        } else if (ok) {
+            const int tile = blockIdx.x;
+            float *wsp = a.ws + (size_t)(tile * a.splits + split) * a.bn * BM;
+            for (int c0 = 0; c0 < t_lim; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr + c0, v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) wsp[(size_t)(c0 + j) * BM + row] = v[j];
+            }
+            __threadfence();
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (warp == 2 && lane == 0) flags[1] = (atomicAdd(&a.counters[tile], 1) == a.splits - 1);
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (flags[1]) {
+                __threadfence();
+                const float *base = a.ws + (size_t)tile * a.splits * a.bn * BM;
+                if (f_ok) {
+                    for (int c = 0; c < t_lim; ++c) {
+                        float acc = 0.f;
+                        for (int s = 0; s < a.splits; ++s) acc += __ldcg(base + ((size_t)s * a.bn + c) * BM + row);
+                        epilogue_store(a.e, t_base + c, f, acc, bias);
+                    }
+                }
+                if (warp == 2 && lane == 0) a.counters[tile] = 0;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, a.tmem_cols);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, k] matrix, box = 64 (k) x box_rows, 128B swizzle.
+bool make_map(CUtensorMap *m, const void *ptr, int rows, int k, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s) {
+    TcShape t{};
+    t.n_tok_tiles = ceil_div(std::max(m_tok, 1), 256);
+    t.bn = std::min(256, std::max(16, ceil_div(ceil_div(std::max(m_tok, 1), t.n_tok_tiles), 16) * 16));
+    t.n_feat_tiles = ceil_div(n_out, BM);
+    t.tmem_cols = 32;
+    while ((int)t.tmem_cols < t.bn) t.tmem_cols *= 2;
+    const int stage_bytes = kStageA + t.bn * BK * 2;
+    const int ctas_per_sm = t.bn <= 128 ? 2 : 1;
+    const size_t budget = std::min(kSmemMaxCta, kSmemPerSm / ctas_per_sm - kSmemReserve) - 1024 - 256;
+    t.stages = std::min<int>(kMaxStages, (int)(budget / stage_bytes));
+    t.smem = (size_t)t.stages * stage_bytes + 1024 + 256;
+    const int num_kb = k / BK;
+    const int tiles = t.n_tok_tiles * t.n_feat_tiles;
+    const int capacity = s.num_sms * ctas_per_sm;
+    int splits = 1;
+    if (tiles < capacity && tiles <= s.n_counters && s.ws) {
+        splits = std::max(1, std::min(capacity / tiles, num_kb / 4));
+        while (splits > 1 && (size_t)tiles * splits * t.bn * BM > s.ws_floats) --splits;
+    }
+    t.kb_per_split = ceil_div(num_kb, splits);
+    t.splits = ceil_div(num_kb, t.kb_per_split);
+    return t;
+}
+
+cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok, int n_out, int k,
+                         const Epilogue &e, const GemmScratch &s, cudaStream_t st) {
+    if (m_tok <= 0) return cudaSuccess;
+    if (k % BK != 0 || k <= 0 || n_out <= 0 || x_rows_cap < m_tok) return cudaErrorInvalidValue;
+    const TcShape t = gemm_tc_shape(m_tok, n_out, k, s);
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t ae = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)kSmemMaxCta);
+        if (ae != cudaSuccess) return ae;
+        attr_done = true;
+    }
+    CUtensorMap mw, mx;
+    if (!make_map(&mw, w, n_out, k, BM) || !make_map(&mx, x, x_rows_cap, k, t.bn)) return cudaErrorInvalidValue;
+    TcArgs a;
+    a.m_tok = m_tok;
+    a.n_out = n_out;
+    a.num_kb = k / BK;
+    a.kb_per_split = t.kb_per_split;
+    a.splits = t.splits;
+    a.bn = t.bn;
+    a.stages = t.stages;
+    a.n_feat_tiles = t.n_feat_tiles;
+    a.n_tok_tiles = t.n_tok_tiles;
+    a.idesc = idesc_bf16_f32(BM, t.bn);
+    a.tmem_cols = (uint32_t)t.tmem_cols;
+    a.e = e;
+    a.ws = s.ws;
+    a.counters = s.counters;
+    a.err = s.err;
+    dim3 grid(t.n_feat_tiles * t.n_tok_tiles, t.splits);
+    gemm_tc_kernel<<<grid, kThreads, t.smem, st>>>(mw, mx, a);
+    return cudaGetLastError();
+}
+
+}  // namespace orca

@@ -1,0 +1,247 @@
+// Row-wise kernels of one iteration: embedding, LayerNorm, K/V append, argmax.
+//
+// All act on the flattened [sum L, H] rows of selective batching
+// (garden.houmin.site Orca notes, 3.1.2: the token-wise operations do not care
+// which request a row belongs to).  Each is HBM-bound: one CTA per row, 16-byte
+// vector accesses along the row.
+#include <cfloat>
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace orca {
+
+namespace {
+
+constexpr int kRowThreads = 128;
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) embed_kernel(const int32_t *tokens, const int32_t *row_pos,
+                                                            const int32_t *prev_next, int prev_n, const T *tok_emb,
+                                                            const T *pos_emb, float *x, int H, int V, int max_pos,
+                                                            unsigned *err) {
+    constexpr int VEC = Elem<T>::kPer16;
+    const int r = blockIdx.x;
+    int t = tokens[r];
+    if (t < 0) {
+        int j = -1 - t;
+        if (j >= prev_n) {
+            if (threadIdx.x == 0) raise_err(err, ERR_BAD_TOKEN);
+            t = 0;
+        } else {
+            t = prev_next[j];
+        }
+    }
+    if (t < 0 || t >= V) {
+        if (threadIdx.x == 0) raise_err(err, ERR_BAD_TOKEN);
+        t = 0;
+    }
+    int p = row_pos[r];
+    if (p < 0 || p >= max_pos) {
+        if (threadIdx.x == 0) raise_err(err, ERR_BAD_POS);
+        p = 0;
+    }
+    const T *te = tok_emb + (size_t)t * H;
+    const T *pe = pos_emb + (size_t)p * H;
+    float *xr = x + (size_t)r * H;
+    for (int e = threadIdx.x * VEC; e < H; e += kRowThreads * VEC) {
+        float a[VEC], b[VEC];
+        load16(te + e, a);
+        load16(pe + e, b);
+#pragma unroll
+        for (int i = 0; i < VEC; i += 4) {
+            float s[4] = {a[i] + b[i], a[i + 1] + b[i + 1], a[i + 2] + b[i + 2], a[i + 3] + b[i + 3]};
+            store16(xr + e + i, s);
+        }
+    }
+}
+
+constexpr int kLnThreads = 256;
+constexpr int kLnMaxVec = 8;  // H <= kLnThreads * 4 * kLnMaxVec = 8192
+
+__device__ __forceinline__ float block_sum(float v, float *red) {
+    v = warp_sum(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    float t = 0.f;
+    if (w == 0) {
+        t = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
+        t = warp_sum(t);
+        if (l == 0) red[32] = t;
+    }
+    __syncthreads();
+    t = red[32];
+    __syncthreads();
+    return t;
+}
+
+template <typename T>
+__device__ __forceinline__ void store_vec4(T *p, const float *v);
+template <>
+__device__ __forceinline__ void store_vec4<float>(float *p, const float *v) {
+    store16(p, v);
+}
+template <>
+__device__ __forceinline__ void store_vec4<bf16>(bf16 *p, const float *v) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t *>(&a);
+    u.y = *reinterpret_cast<uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+
+// LayerNorm with biased variance, eps 1e-5, statistics in fp32 from registers
+// (two passes over the row held in registers).
+template <typename T>
+__global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const float *x, const int32_t *row_map,
+                                                               const float *g, const float *b, T *y, float *y32,
+                                                               int H) {
+    __shared__ float red[33];
+    const int r = blockIdx.x;
+    const int src = row_map ? row_map[r] : r;
+    const float *xr = x + (size_t)src * H;
+    float v[kLnMaxVec][4];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kLnMaxVec; ++i) {
+        int e = (threadIdx.x + i * kLnThreads) * 4;
+        if (e < H) {
+            float4 q = *reinterpret_cast<const float4 *>(xr + e);
+            v[i][0] = q.x, v[i][1] = q.y, v[i][2] = q.z, v[i][3] = q.w;
+            s += q.x + q.y + q.z + q.w;
+        }
+    }
+    const float mean = block_sum(s, red) / (float)H;
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kLnMaxVec; ++i) {
+        int e = (threadIdx.x + i * kLnThreads) * 4;
+        if (e < H) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float d = v[i][j] - mean;
+                ss += d * d;
+            }
+        }
+    }
+    const float var = block_sum(ss, red) / (float)H;
+    const float rstd = rsqrtf(var + 1e-5f);
+#pragma unroll
+    for (int i = 0; i < kLnMaxVec; ++i) {
+        int e = (threadIdx.x + i * kLnThreads) * 4;
+        if (e < H) {
+            float4 gg = *reinterpret_cast<const float4 *>(g + e);
+            float4 bb = *reinterpret_cast<const float4 *>(b + e);
+            float o[4] = {(v[i][0] - mean) * rstd * gg.x + bb.x, (v[i][1] - mean) * rstd * gg.y + bb.y,
+                          (v[i][2] - mean) * rstd * gg.z + bb.z, (v[i][3] - mean) * rstd * gg.w + bb.w};
+            store_vec4<T>(y + (size_t)r * H + e, o);
+            if (y32) store16(y32 + (size_t)r * H + e, o);
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) kv_append_kernel(const T *qkv, const int32_t *row_slot,
+                                                                T *pool_layer, int64_t kv_slots, int H, int d,
+                                                                int n_heads) {
+    constexpr int VEC = Elem<T>::kPer16;
+    const int r = blockIdx.x;
+    const int64_t slot = row_slot[r];
+    const T *src = qkv + (size_t)r * 3 * H + H;  // k then v, 2H contiguous values
+    for (int e = threadIdx.x * VEC; e < 2 * H; e += kRowThreads * VEC) {
+        const int which = e >= H;
+        const int c = e - which * H;
+        const int h = c / d, dd = c - h * d;
+        T *dst = pool_layer + (((int64_t)(which * n_heads + h) * kv_slots + slot) * d + dd);
+        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src + e);
+    }
+}
+
+constexpr int kArgmaxThreads = 512;
+
+__global__ void __launch_bounds__(kArgmaxThreads) argmax_kernel(const float *logits, int V, int32_t *next,
+                                                                int32_t *out2) {
+    __shared__ float sv[kArgmaxThreads / 32];
+    __shared__ int si[kArgmaxThreads / 32];
+    const float *lr = logits + (size_t)blockIdx.x * V;
+    float best = -FLT_MAX;
+    int idx = INT_MAX;
+    for (int j = threadIdx.x; j < V; j += kArgmaxThreads) {
+        float v = lr[j];
+        if (v > best || idx == INT_MAX) best = v, idx = j;  // ascending j: first occurrence wins
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, best, o);
+        int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+        if (ov > best || (ov == best && oi < idx)) best = ov, idx = oi;
+    }
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) sv[w] = best, si[w] = idx;
+    __syncthreads();
+    if (w == 0) {
+        best = l < kArgmaxThreads / 32 ? sv[l] : -FLT_MAX;
+        idx = l < kArgmaxThreads / 32 ? si[l] : INT_MAX;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float ov = __shfl_xor_sync(0xffffffffu, best, o);
+            int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+            if (ov > best || (ov == best && oi < idx)) best = ov, idx = oi;
+        }
+        if (l == 0) {
+            next[blockIdx.x] = idx;
+            if (out2) out2[blockIdx.x] = idx;
+        }
+    }
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t embed(const int32_t *tokens, const int32_t *row_pos, const int32_t *prev_next, int prev_n,
+                  const T *tok_emb, const T *pos_emb, float *x, int n_rows, int H, int V, int max_pos,
+                  unsigned *err, cudaStream_t st) {
+    if (n_rows <= 0) return cudaSuccess;
+    embed_kernel<T><<<n_rows, kRowThreads, 0, st>>>(tokens, row_pos, prev_next, prev_n, tok_emb, pos_emb, x, H, V,
+                                                    max_pos, err);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t layernorm(const float *x, const int32_t *row_map, const float *g, const float *b, T *y, float *y32,
+                      int n_rows, int H, cudaStream_t st) {
+    if (n_rows <= 0) return cudaSuccess;
+    if (H % 4 != 0 || H > kLnThreads * 4 * kLnMaxVec) return cudaErrorInvalidValue;
+    layernorm_kernel<T><<<n_rows, kLnThreads, 0, st>>>(x, row_map, g, b, y, y32, H);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t kv_append(const T *qkv, const int32_t *row_slot, T *pool_layer, int64_t kv_slots, int n_rows, int H,
+                      int n_heads, cudaStream_t st) {
+    if (n_rows <= 0) return cudaSuccess;
+    kv_append_kernel<T><<<n_rows, kRowThreads, 0, st>>>(qkv, row_slot, pool_layer, kv_slots, H, H / n_heads,
+                                                        n_heads);
+    return cudaGetLastError();
+}
+
+cudaError_t argmax_rows(const float *logits, int n_rows, int V, int32_t *next, int32_t *out2, cudaStream_t st) {
+    if (n_rows <= 0) return cudaSuccess;
+    argmax_kernel<<<n_rows, kArgmaxThreads, 0, st>>>(logits, V, next, out2);
+    return cudaGetLastError();
+}
+
+template cudaError_t embed<float>(const int32_t *, const int32_t *, const int32_t *, int, const float *,
+                                  const float *, float *, int, int, int, int, unsigned *, cudaStream_t);
+template cudaError_t embed<bf16>(const int32_t *, const int32_t *, const int32_t *, int, const bf16 *, const bf16 *,
+                                 float *, int, int, int, int, unsigned *, cudaStream_t);
+template cudaError_t layernorm<float>(const float *, const int32_t *, const float *, const float *, float *, float *,
+                                      int, int, cudaStream_t);
+template cudaError_t layernorm<bf16>(const float *, const int32_t *, const float *, const float *, bf16 *, float *,
+                                     int, int, cudaStream_t);
+template cudaError_t kv_append<float>(const float *, const int32_t *, float *, int64_t, int, int, int, cudaStream_t);
+template cudaError_t kv_append<bf16>(const bf16 *, const int32_t *, bf16 *, int64_t, int, int, int, cudaStream_t);
+
+}  // namespace orca

@@ -1,0 +1,84 @@
+// Host-side launchers of the device kernels (internal to liborca).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace orca {
+
+using bf16 = __nv_bfloat16;
+
+// Epilogue of a linear layer y[t, f] = sum_k x[t, k] w[f, k]:
+//   y += bias[f]; y = GeLU(y) if gelu;
+//   resid ? out_f32[t, f] = resid[t, f] + y : (out_f32 ? out_f32 : out_bf16)[t, f] = y.
+struct Epilogue {
+    const float *bias = nullptr;
+    int gelu = 0;
+    const float *resid = nullptr;
+    float *out_f32 = nullptr;
+    bf16 *out_bf16 = nullptr;
+    int ld_out = 0;
+};
+
+// Scratch shared by the split-K GEMM reduction.
+struct GemmScratch {
+    float *ws = nullptr;      // partial tiles
+    size_t ws_floats = 0;
+    int *counters = nullptr;  // per output tile, zero between launches
+    int n_counters = 0;
+    unsigned *err = nullptr;
+    int num_sms = 148;
+};
+
+// tcgen05 GEMM, bf16 operands, fp32 accumulation in tensor memory.
+// x: [x_rows_cap, k] row-major (rows >= m_tok are never stored), w: [n_out, k].
+cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok, int n_out, int k,
+                         const Epilogue &e, const GemmScratch &s, cudaStream_t st);
+// Shape the tcgen05 GEMM would use (for scratch sizing and accounting).
+struct TcShape {
+    int bn, n_tok_tiles, n_feat_tiles, splits, kb_per_split, stages, tmem_cols;
+    size_t smem;
+};
+TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s);
+
+// SIMT FFMA GEMM, fp32 operands.
+cudaError_t gemm_simt_f32(const float *x, const float *w, int m_tok, int n_out, int k, const Epilogue &e,
+                          cudaStream_t st);
+
+// x[r] = tok_emb[tok(r)] + pos_emb[row_pos[r]] (fp32 out).  tok(r) = tokens[r]
+// if >= 0, else prev_next[-1 - tokens[r]].
+template <typename T>
+cudaError_t embed(const int32_t *tokens, const int32_t *row_pos, const int32_t *prev_next, int prev_n,
+                  const T *tok_emb, const T *pos_emb, float *x, int n_rows, int H, int V, int max_pos,
+                  unsigned *err, cudaStream_t st);
+
+// y[r] = LN(x[src(r)]) with src(r) = row_map ? row_map[r] : r; optional fp32 copy.
+template <typename T>
+cudaError_t layernorm(const float *x, const int32_t *row_map, const float *g, const float *b, T *y, float *y32,
+                      int n_rows, int H, cudaStream_t st);
+
+// Copy this iteration's k, v rows (columns H..3H of qkv) into the pool layer.
+template <typename T>
+cudaError_t kv_append(const T *qkv, const int32_t *row_slot, T *pool_layer, int64_t kv_slots, int n_rows, int H,
+                      int n_heads, cudaStream_t st);
+
+struct AttnPlan {
+    const int32_t *req_off, *req_ctx, *req_kvoff;
+    const int32_t *dec_work, *dec_wbegin, *dec_nch;  // decode split-K work items
+    const int32_t *pre_tiles;                        // prefill (request, first row) tiles
+    int n_dec_work, n_pre_tiles, chunk;
+};
+
+// Attention for one layer.  Decode: requests with one input row, split-K over
+// their cached keys.  Prefill: requests with several rows, causal.
+template <typename T>
+cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *out, const AttnPlan &p, int H,
+                      int n_heads, float *part, int *counters, cudaStream_t st, bool decode, bool prefill);
+
+// next[b] = argmax_j logits[b, j] (lowest j on ties); also to out2 if non-null.
+cudaError_t argmax_rows(const float *logits, int n_rows, int V, int32_t *next, int32_t *out2, cudaStream_t st);
+
+constexpr int kPrefillRowsPerTile = 16;
+
+}  // namespace orca

@@ -1,0 +1,245 @@
+"""Parity of whole iterations through the C ABI against the oracle.
+
+Teacher forcing: the oracle's next tokens drive the scheduler, so the engine
+and the oracle always consume identical token streams.  Floating point is
+compared normwise (max |gpu - ref| / max |ref|) on the final-LayerNorm output
+of each request's last row and on the logits; the greedy token is compared
+exactly with the argmax of the engine's own logits (same precision) and for
+agreement with the oracle's token.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from iteration_level_scheduling_gb300 import synth
+from oracle import model as omodel
+from oracle import sched as osched
+from oracle.model import BatchItem, KVStore
+from gpu_util import kv_pool_tensor, load_context, make_engine, normwise
+
+pytestmark = pytest.mark.gpu
+
+TOL_FP32 = 1e-4
+TOL_BF16 = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from iteration_level_scheduling_gb300 import build
+    build.build()
+
+
+def run_trace_teacher_forced(cfg, w, specs, max_batch, mode, kv_slots, max_tokens=4096, feedback=False):
+    from iteration_level_scheduling_gb300 import native
+    eng = make_engine(cfg, w, max_tokens, max_batch, kv_slots)
+    s = native.Scheduler(max_batch, max_tokens, mode=mode, engine=eng, token_feedback=feedback)
+    for sp in specs:
+        s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len, sp.ctx0)
+    store = KVStore(cfg.n_layers, cfg.hidden)
+    worst_h = worst_l = 0.0
+    agree = total = iters = 0
+    prev_next = {}
+    while True:
+        st, b = s.next()
+        if st == 2:
+            break
+        if st == 0:
+            continue
+        toks = b.tokens.tolist()
+        items, p = [], 0
+        resolved = []
+        for rid, n, c in zip(b.request_id.tolist(), b.n_input.tolist(), b.ctx_len.tolist()):
+            tk = toks[p:p + n]
+            tk = [prev_next[-1 - t] if t < 0 else t for t in tk]
+            resolved += tk
+            items.append(BatchItem(rid, tk, c))
+            p += n
+        got = eng.run_iteration(b)
+        ref = omodel.iteration(w, cfg.n_heads, items, store)
+        hid = eng.last_hidden(b.n_req)
+        lg = eng.last_logits(b.n_req)
+        worst_h = max(worst_h, normwise(hid, ref.hidden))
+        worst_l = max(worst_l, normwise(lg, ref.logits))
+        assert got.tolist() == lg.argmax(1).tolist()  # argmax kernel == argmax of its own logits
+        agree += sum(int(a == r) for a, r in zip(got.tolist(), ref.next_tokens))
+        total += b.n_req
+        iters += 1
+        prev_next = dict(enumerate(ref.next_tokens))
+        s.complete(ref.next_tokens)  # teacher forcing: the oracle's tokens drive both
+    st = s.stats()
+    eng_stats = eng.stats()
+    s.close()
+    eng.close()
+    return dict(iters=iters, worst_h=worst_h, worst_l=worst_l, agree=agree / max(total, 1), total=total,
+                generated=st.generated, launches=eng_stats.launches)
+
+
+@pytest.mark.parametrize("mode,expect_iters", [(0, 50), (1, 90)])
+@pytest.mark.parametrize("affine", [False, True])
+def test_tiny_fp32_trace(mode, expect_iters, affine):
+    """Tiny fp32 decoder, 8 requests, outputs [5,50,8,12,40,3,30,7], max_batch 4:
+    iteration-level 50 iterations, request-level 90; every iteration matches the
+    oracle to 1e-4."""
+    cfg = synth.TINY
+    w = synth.make_weights(cfg, 0, random_affine=affine)
+    r = run_trace_teacher_forced(cfg, w, synth.tiny_requests(0), 4, mode, kv_slots=4 * 128)
+    assert r["iters"] == expect_iters
+    assert r["generated"] == 155
+    assert r["worst_h"] <= TOL_FP32 and r["worst_l"] <= TOL_FP32, r
+    assert r["agree"] >= 0.99, r
+
+
+def test_tiny_fp32_trace_token_feedback():
+    """Increment inputs passed as references to the previous iteration's outputs."""
+    cfg = synth.TINY
+    w = synth.make_weights(cfg, 1, random_affine=True)
+    r = run_trace_teacher_forced(cfg, w, synth.tiny_requests(1), 4, 0, kv_slots=4 * 128, feedback=True)
+    assert r["worst_l"] <= TOL_FP32 and r["agree"] == 1.0, r
+
+
+def run_one_batch(cfg, w, reqs, sample, seed_kv=0, max_tokens=None):
+    """Run one mixed iteration over all of `reqs` on the GPU; compare the
+    requests whose ids are in `sample` with the oracle (requests are
+    independent, so a sub-batch gives the same per-request result)."""
+    from iteration_level_scheduling_gb300 import native
+    B = len(reqs)
+    rows = sum(len(r.prompt) for r in reqs)
+    reserve = {r.rid: (r.ctx0 + len(r.prompt) + 8) for r in reqs}
+    eng = make_engine(cfg, w, max_tokens or rows, B, sum(reserve.values()))
+    pool = kv_pool_tensor(eng)
+    store = KVStore(cfg.n_layers, cfg.hidden)
+    offs = {}
+    for r in reqs:
+        offs[r.rid] = eng.kv_alloc(r.rid, reserve[r.rid])
+        if r.ctx0:
+            load_context(eng, pool, cfg, seed_kv, r.rid, offs[r.rid], r.ctx0, store if r.rid in sample else None)
+    torch.cuda.synchronize()
+    toks = [t for r in reqs for t in r.prompt]
+    b = native.BatchDesc([r.rid for r in reqs], [1 if r.ctx0 else 0 for r in reqs], [len(r.prompt) for r in reqs],
+                         [r.ctx0 for r in reqs], [offs[r.rid] for r in reqs], toks)
+    got = eng.run_iteration(b)
+    hid = eng.last_hidden(B)
+    lg = eng.last_logits(B)
+    assert got.tolist() == lg.argmax(1).tolist()
+    idx = [i for i, r in enumerate(reqs) if r.rid in sample]
+    items = [BatchItem(reqs[i].rid, reqs[i].prompt, reqs[i].ctx0) for i in idx]
+    ref = omodel.iteration(w, cfg.n_heads, items, store)
+    res = dict(h=normwise(hid[idx], ref.hidden), l=normwise(lg[idx], ref.logits),
+               agree=np.mean([got[i] == t for i, t in zip(idx, ref.next_tokens)]), n=len(idx))
+    eng.close()
+    return res
+
+
+def test_gpt2_medium_mixed_batch():
+    """GPT-2-medium shape, bf16: prompts (128, 64, 256) + 29 increment requests with
+    contexts U[1,1024] (sum L = 477); sampled requests against the oracle."""
+    cfg = synth.GPT2_MEDIUM
+    w = synth.make_weights(cfg, 0, random_affine=True)
+    reqs = synth.mixed_batch(0)
+    assert sum(len(r.prompt) for r in reqs) == 448 + 29
+    longest = sorted((r for r in reqs if r.ctx0), key=lambda r: -r.ctx0)[:4]
+    shortest = sorted((r for r in reqs if r.ctx0), key=lambda r: r.ctx0)[:2]
+    sample = {0, 1, 2} | {r.rid for r in longest + shortest}
+    res = run_one_batch(cfg, w, reqs, sample)
+    assert res["h"] <= TOL_BF16 and res["l"] <= TOL_BF16, res
+
+
+def test_gpt3_13b_width_two_layers():
+    """13B width (H=5120, 40 heads, FFN 20480, V=50257) at two layers: 64 requests
+    (2 initiation + 62 increment, contexts up to 1000), the decode regime of the
+    continuous-batching trace; sampled against the oracle."""
+    cfg = synth.GPT3_13B.with_layers(2)
+    w = synth.make_weights(cfg, 0, random_affine=True)
+    reqs = synth.mixed_batch(3, prompt_lens=(100, 37), n_incr=62, ctx_range=(32, 1000))
+    sample = {0, 1, 2, 3, 60, 63}
+    res = run_one_batch(cfg, w, reqs, sample)
+    assert res["h"] <= TOL_BF16 and res["l"] <= TOL_BF16, res
+
+
+@pytest.mark.parametrize("case", ["single_token", "one_long_prompt", "chunk_edges"])
+def test_edge_batches(case):
+    cfg = synth.ModelConfig(n_layers=2, hidden=256, n_heads=2, ffn=512, vocab=1000, max_pos=1024, dtype="bf16")
+    w = synth.make_weights(cfg, 5, random_affine=True)
+    if case == "single_token":
+        reqs = [synth.RequestSpec(0, 0.0, [7], 1)]
+    elif case == "one_long_prompt":
+        reqs = [synth.RequestSpec(0, 0.0, list(range(3, 3 + 600)), 1)]
+    else:  # decode contexts at the split-K chunk boundaries
+        reqs = [synth.RequestSpec(i, 0.0, [i + 1], 1, c) for i, c in enumerate([1, 63, 64, 255, 256, 257, 511, 1000])]
+    res = run_one_batch(cfg, w, reqs, {r.rid for r in reqs})
+    assert res["h"] <= TOL_BF16 and res["l"] <= TOL_BF16, res
+
+
+def test_invalid_descriptors_rejected():
+    from iteration_level_scheduling_gb300 import native
+    cfg = synth.TINY
+    w = synth.make_weights(cfg, 0)
+    eng = make_engine(cfg, w, 64, 4, 256)
+    off = eng.kv_alloc(1, 32)
+    good = dict(request_id=[1], phase=[0], n_input=[3], ctx_len=[0], kv_offset=[off], tokens=[1, 2, 3])
+    bad = [dict(phase=[1]), dict(kv_offset=[off + 1]), dict(tokens=[1, 2, 512]), dict(n_input=[3], ctx_len=[30],
+           phase=[1]), dict(request_id=[2]), dict(tokens=[1, 2, -1])]
+    for change in bad:
+        d = dict(good)
+        d.update(change)
+        with pytest.raises(native.OrcaError) as e:
+            eng.run_iteration(native.BatchDesc(**d))
+        assert e.value.code == native.ERR_INVALID
+    assert eng.run_iteration(native.BatchDesc(**good)).shape == (1,)
+    with pytest.raises(native.OrcaError) as e:
+        eng.kv_alloc(2, 10 ** 6)
+    assert e.value.code == native.ERR_KV_FULL
+    eng.close()
+
+
+def test_planned_path_equals_synchronous_path():
+    """Device-resident plans with token feedback give the same tokens, hidden states
+    and launches as the synchronous host path."""
+    from iteration_level_scheduling_gb300 import native
+    cfg = synth.ModelConfig(n_layers=2, hidden=256, n_heads=2, ffn=512, vocab=1000, max_pos=512, dtype="bf16")
+    w = synth.make_weights(cfg, 2, random_affine=True)
+    trace = synth.poisson_trace(2, n=24, rate=1.0, prompt_range=(2, 40), out_range=(1, 12), vocab=1000)
+
+    def sync_run():
+        eng = make_engine(cfg, w, 512, 8, 8 * 64)
+        s = native.Scheduler(8, 512, kv_reserve=64, engine=eng)
+        for sp in trace:
+            s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len)
+        s.run()
+        out = {sp.rid: s.tokens(sp.rid).tolist() for sp in trace}
+        s.close()
+        eng.close()
+        return out
+
+    def planned_run():
+        eng = make_engine(cfg, w, 512, 8, 8 * 64)
+        s = native.Scheduler(8, 512, kv_reserve=64, engine=eng, token_feedback=True)
+        for sp in trace:
+            s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len)
+        plans, batches = [], []
+        while True:  # dry run: output lengths are fixed, so the schedule does not depend on token values
+            st, b = s.next()
+            if st == 2:
+                break
+            if st == 0:
+                continue
+            buf = np.zeros(eng.plan_words(b), np.int32)
+            eng.plan_build(b, buf)
+            plans.append(buf)
+            batches.append(b.request_id.tolist())
+            s.complete([0] * b.n_req)
+        dev = [torch.from_numpy(p).cuda() for p in plans]
+        outs = [torch.zeros(len(bt), dtype=torch.int32, device="cuda") for bt in batches]
+        for p, d, o in zip(plans, dev, outs):
+            eng.run_planned(p, d.data_ptr(), o.data_ptr())
+        eng.sync()
+        res = {sp.rid: [] for sp in trace}
+        for bt, o in zip(batches, outs):
+            for rid, t in zip(bt, o.cpu().tolist()):
+                res[rid].append(t)
+        s.close()
+        eng.close()
+        return res
+
+    assert sync_run() == planned_run()

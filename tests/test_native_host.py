@@ -1,0 +1,139 @@
+"""Host-side parts of liborca.so that need no GPU: the library loads, exports
+every function include/orca.h declares, and its C++ scheduler and K/V pool
+make exactly the oracle's decisions (bit-exact batches, offsets and slots)."""
+
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+from iteration_level_scheduling_gb300 import build, synth
+from oracle import sched as osched
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def native():
+    build.build()
+    from iteration_level_scheduling_gb300 import native as n
+    return n
+
+
+def test_header_symbols_exported(native):
+    hdr = open(os.path.join(ROOT, "include", "orca.h")).read()
+    declared = sorted(set(re.findall(r"^\s*(?:const\s+)?[\w ]+?\**\s*\b(orca_\w+)\s*\(", hdr, re.M)))
+    assert len(declared) >= 20
+    for name in declared:
+        assert hasattr(native.lib, name), name
+    assert set(declared) == set(native.EXPORTS)
+
+
+def test_strerror(native):
+    assert native.lib.orca_strerror(0) == b"ok"
+    assert b"K/V" in native.lib.orca_strerror(native.ERR_KV_FULL)
+
+
+def drive_native(native, specs, max_batch, max_tokens, kv_slots, kv_reserve=0, mode=0, feedback=False):
+    s = native.Scheduler(max_batch, max_tokens, kv_slots, kv_reserve, mode, feedback)
+    for sp in specs:
+        s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len, sp.ctx0)
+    recs = []
+    while True:
+        st, b = s.next()
+        if st == 2:
+            break
+        if st == 0:
+            continue
+        toks = [(int(r) * 31 + s.stats().clock) % 50000 for r in b.request_id]
+        recs.append((s.stats().clock, b))
+        s.complete(toks)
+    return s, recs
+
+
+def drive_oracle(specs, max_batch, max_tokens, kv_slots, kv_reserve=0, mode="iteration"):
+    return osched.run(specs, max_batch, max_tokens, kv_slots, kv_reserve, mode,
+                      token_fn=lambda it: [(rid * 31 + it.k) % 50000 for rid in it.rids])
+
+
+def assert_same(native_recs, oracle_recs):
+    assert len(native_recs) == len(oracle_recs)
+    for (k, b), it in zip(native_recs, oracle_recs):
+        assert k == it.k
+        assert b.request_id.tolist() == it.rids
+        assert b.phase.tolist() == it.phase
+        assert b.n_input.tolist() == it.n_input
+        assert b.ctx_len.tolist() == it.ctx
+        assert b.kv_offset.tolist() == it.kv_off
+        assert b.tokens.tolist() == it.tokens
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_worked_example_native(native, mode):
+    outs = [5, 50, 8, 12, 40, 3, 30, 7]
+    specs = [synth.RequestSpec(i, 0.0, [1, 2], L) for i, L in enumerate(outs)]
+    s, recs = drive_native(native, specs, 4, 4096, 10 ** 6, mode=mode)
+    assert len(recs) == (50 if mode == 0 else 90)
+    st = s.stats()
+    assert st.generated == sum(outs) and st.finished == 8 and st.kv_reserved == 0
+    _, orecs = drive_oracle(specs, 4, 4096, 10 ** 6, mode="iteration" if mode == 0 else "request")
+    assert_same(recs, orecs)
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_native_matches_oracle_random_traces(native, seed):
+    rnd = random.Random(100 + seed)
+    trace = synth.poisson_trace(seed, n=80, rate=rnd.choice([0.1, 0.5, 3.0]), prompt_range=(1, 60),
+                                out_range=(1, 40), vocab=1000)
+    mb, mt = rnd.randint(1, 16), rnd.randint(60, 300)
+    slots = rnd.randint(100, 1500)
+    reserve = rnd.choice([0, 0, 100])
+    for mode in (0, 1):
+        s, recs = drive_native(native, trace, mb, mt, slots, reserve, mode)
+        _, orecs = drive_oracle(trace, mb, mt, slots, reserve, "iteration" if mode == 0 else "request")
+        assert_same(recs, orecs)
+        for sp in trace:
+            r = s.request(sp.rid)
+            assert r.state == 2 and r.n_generated == sp.out_len
+
+
+def test_native_cfg3_trace_prefix(native):
+    """The 13B continuous-batching trace: 1000 requests, 64 x 1024-token reservations."""
+    trace = synth.poisson_trace(0, n=1000, rate=0.5, with_tokens=False)
+    s, recs = drive_native(native, trace, 64, 4096, 64 * 1024, kv_reserve=1024)
+    _, orecs = drive_oracle(trace, 64, 4096, 64 * 1024, kv_reserve=1024)
+    assert_same(recs, orecs)
+    assert max(len(b.request_id) for _, b in recs) == 64
+
+
+def test_cached_context_requests_and_kv_full(native):
+    s = native.Scheduler(8, 4096, kv_slots=1000, kv_reserve=300)
+    assert s.submit(0, 0.0, [5], 10, ctx0=200) == 0
+    assert s.submit(1, 0.0, [6], 10, ctx0=250) == 300
+    assert s.submit(2, 0.0, [7], 10, ctx0=100) == 600
+    with pytest.raises(native.OrcaError) as e:
+        s.submit(3, 0.0, [8], 10, ctx0=100)
+    assert e.value.code == native.ERR_KV_FULL
+    with pytest.raises(native.OrcaError):
+        s.submit(4, 0.0, [1] * 295, 10)  # 295 + 10 - 1 > 300
+    st, b = s.next()
+    assert st == 1 and b.phase.tolist() == [1, 1, 1] and b.ctx_len.tolist() == [200, 250, 100]
+    assert b.tokens.tolist() == [5, 6, 7]
+
+
+def test_token_feedback_references(native):
+    s = native.Scheduler(4, 4096, kv_slots=100, token_feedback=True)
+    s.submit(0, 0.0, [1, 2, 3], 3)
+    s.submit(1, 1.0, [4], 3)
+    st, b = s.next()
+    assert b.tokens.tolist() == [1, 2, 3]
+    s.complete([9])
+    st, b = s.next()
+    # request 0 was index 0 of the previous iteration -> -1; request 1 is new
+    assert b.request_id.tolist() == [0, 1] and b.tokens.tolist() == [-1, 4]
+    s.complete([10, 11])
+    st, b = s.next()
+    assert b.tokens.tolist() == [-1, -2]
+    assert s.tokens(0).tolist() == [9, 10]
