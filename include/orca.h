@@ -217,7 +217,9 @@ int orca_engine_timing_read(orca_engine *eng, orca_kernel_time *out, int32_t cap
  *   else          : out_f32 or out_bf16 (exactly one non-NULL) = y.
  * dtype BF16: x, w bf16 (tcgen05 tensor cores, fp32 accumulation; k % 64 == 0);
  * dtype FP32: x, w fp32 (SIMT FFMA).  Rows of out have stride ld_out.
- * Uses the engine's stream and scratch. */
+ * Asynchronous on the engine's stream (uses the engine's split-K scratch, so
+ * calls on one engine must not overlap); orca_engine_sync waits and reports
+ * device-side errors.  Errors: INVALID (shape / pointer combination), CUDA. */
 int orca_op_linear(orca_engine *eng, int32_t dtype, const void *x, const void *w, int32_t m_tok, int32_t n_out,
                    int32_t k, const float *bias, int32_t gelu, const float *resid, float *out_f32, void *out_bf16,
                    int32_t ld_out);
@@ -257,6 +259,12 @@ int orca_sched_destroy(orca_sched *s);
  * the token budget), KV_FULL (ctx0 > 0 only). */
 int orca_sched_submit(orca_sched *s, int64_t id, double arrival, const int32_t *prompt, int32_t prompt_len,
                       int32_t out_len, int32_t ctx0, int64_t *out_kv_offset);
+
+/* Turn token feedback on or off from the next iteration on.  References are
+ * only emitted to iterations that ran while feedback was on, so a caller may
+ * schedule some iterations on the host only (feedback off) and then hand the
+ * following ones to the engine. */
+int orca_sched_set_token_feedback(orca_sched *s, int32_t enable);
 
 /* Select the batch for the current iteration.  *status = 1 and *out filled
  * (arrays owned by the scheduler, valid until the next call) when there is

@@ -709,7 +709,7 @@ int orca_op_linear(orca_engine *E, int32_t dtype, const void *x, const void *w, 
         cudaGetLastError();
         return ORCA_ERR_CUDA;
     }
-    return orca_engine_sync(E);
+    return ORCA_OK;
 }
 
 }  // extern "C"

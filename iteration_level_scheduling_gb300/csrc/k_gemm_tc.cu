@@ -31,6 +31,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -284,6 +285,20 @@ bool make_map(CUtensorMap *m, const void *ptr, int rows, int k, int box_rows) {
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Optional tuning overrides (ORCA_GEMM_SPLITS, ORCA_GEMM_STAGES), read once.
+int env_int(const char *name) {
+    const char *v = getenv(name);
+    return v ? atoi(v) : 0;
+}
+int override_splits() {
+    static int v = env_int("ORCA_GEMM_SPLITS");
+    return v;
+}
+int override_stages() {
+    static int v = env_int("ORCA_GEMM_STAGES");
+    return v;
+}
+
 }  // namespace
 
 TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s) {
@@ -297,6 +312,8 @@ TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s) {
     const int ctas_per_sm = t.bn <= 128 ? 2 : 1;
     const size_t budget = std::min(kSmemMaxCta, kSmemPerSm / ctas_per_sm - kSmemReserve) - 1024 - 256;
     t.stages = std::min<int>(kMaxStages, (int)(budget / stage_bytes));
+    if (override_stages() > 0)
+        t.stages = std::min<int>(std::min(override_stages(), kMaxStages), (int)((kSmemMaxCta - 1280) / stage_bytes));
     t.smem = (size_t)t.stages * stage_bytes + 1024 + 256;
     const int num_kb = k / BK;
     const int tiles = t.n_tok_tiles * t.n_feat_tiles;
@@ -304,6 +321,7 @@ TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s) {
     int splits = 1;
     if (tiles < capacity && tiles <= s.n_counters && s.ws) {
         splits = std::max(1, std::min(capacity / tiles, num_kb / 4));
+        if (override_splits() > 0) splits = std::min(override_splits(), num_kb);
         while (splits > 1 && (size_t)tiles * splits * t.bn * BM > s.ws_floats) --splits;
     }
     t.kb_per_split = ceil_div(num_kb, splits);

@@ -67,6 +67,7 @@ struct orca_sched {
     std::vector<Request *> batch;          // batch of the last orca_sched_next
     bool batch_open = false;
     int64_t clock = 0, iterations = 0, generated = 0, finished = 0;
+    int64_t feedback_since = 0;  // first iteration run with token feedback on
     // descriptor arrays handed out by orca_sched_next
     std::vector<int64_t> d_id, d_kv;
     std::vector<int32_t> d_phase, d_n, d_ctx, d_tok;
@@ -186,6 +187,13 @@ int orca_sched_submit(orca_sched *s, int64_t id, double arrival, const int32_t *
     return ORCA_OK;
 }
 
+int orca_sched_set_token_feedback(orca_sched *s, int32_t enable) {
+    if (!s) return ORCA_ERR_INVALID;
+    if (enable && !s->cfg.token_feedback) s->feedback_since = s->iterations;
+    s->cfg.token_feedback = enable ? 1 : 0;
+    return ORCA_OK;
+}
+
 int orca_sched_next(orca_sched *s, orca_batch *out, int32_t *status) {
     if (!s || !out || !status) return ORCA_ERR_INVALID;
     if (s->batch_open) return ORCA_ERR_INVALID;  // previous batch not completed
@@ -229,7 +237,7 @@ int orca_sched_next(orca_sched *s, orca_batch *out, int32_t *status) {
         s->d_ctx[i] = r->ctx;
         if (r->ctx == 0) {
             s->d_tok.insert(s->d_tok.end(), r->prompt.begin(), r->prompt.end());
-        } else if (s->cfg.token_feedback && r->last_iter == s->iterations - 1 && r->last_iter >= 0) {
+        } else if (s->cfg.token_feedback && r->last_iter == s->iterations - 1 && r->last_iter >= s->feedback_since) {
             s->d_tok.push_back(-1 - r->last_index);
         } else {
             s->d_tok.push_back(r->pending);

@@ -30,7 +30,7 @@ EXPORTS = [
     "orca_kv_layout_get", "orca_run_iteration", "orca_plan_words", "orca_plan_build", "orca_run_planned",
     "orca_engine_sync", "orca_get_last_hidden", "orca_get_last_logits", "orca_engine_stats_get",
     "orca_engine_timing", "orca_engine_timing_read", "orca_op_linear", "orca_sched_create", "orca_sched_destroy",
-    "orca_sched_submit", "orca_sched_next", "orca_sched_complete", "orca_sched_stats_get", "orca_sched_request_get",
+    "orca_sched_submit", "orca_sched_set_token_feedback", "orca_sched_next", "orca_sched_complete", "orca_sched_stats_get", "orca_sched_request_get",
     "orca_sched_request_tokens", "orca_sched_run",
 ]
 
@@ -116,6 +116,7 @@ _sig = {
     "orca_sched_destroy": (C.c_int, [P]),
     "orca_sched_submit": (C.c_int, [P, C.c_int64, C.c_double, P, C.c_int32, C.c_int32, C.c_int32,
                                     C.POINTER(C.c_int64)]),
+    "orca_sched_set_token_feedback": (C.c_int, [P, C.c_int32]),
     "orca_sched_next": (C.c_int, [P, C.POINTER(Batch), C.POINTER(C.c_int32)]),
     "orca_sched_complete": (C.c_int, [P, P]),
     "orca_sched_stats_get": (C.c_int, [P, C.POINTER(SchedStats)]),
@@ -259,9 +260,11 @@ class Engine:
                      flops=buf[i].flops) for i in range(n.value)]
 
     def op_linear(self, dtype: int, x: int, w: int, m: int, n: int, k: int, bias: int = 0, gelu: bool = False,
-                  resid: int = 0, out_f32: int = 0, out_bf16: int = 0, ld_out: int = 0):
+                  resid: int = 0, out_f32: int = 0, out_bf16: int = 0, ld_out: int = 0, sync: bool = True):
         check(lib.orca_op_linear(self._h, dtype, P(x), P(w), m, n, k, P(bias or None), int(gelu), P(resid or None),
                                  P(out_f32 or None), P(out_bf16 or None), ld_out or n), "orca_op_linear")
+        if sync:
+            self.sync()
 
 
 class Scheduler:
@@ -294,6 +297,9 @@ class Scheduler:
         check(lib.orca_sched_submit(self._h, rid, float(arrival), _ptr(p), len(p), out_len, ctx0, C.byref(off)),
               "orca_sched_submit")
         return off.value
+
+    def set_token_feedback(self, enable: bool) -> None:
+        check(lib.orca_sched_set_token_feedback(self._h, int(enable)), "orca_sched_set_token_feedback")
 
     def next(self):
         """Returns (status, BatchDesc or None); status 1 batch, 0 idle tick, 2 done."""

@@ -137,3 +137,16 @@ def test_token_feedback_references(native):
     st, b = s.next()
     assert b.tokens.tolist() == [-1, -2]
     assert s.tokens(0).tolist() == [9, 10]
+
+
+def test_token_feedback_enabled_midway(native):
+    s = native.Scheduler(4, 4096, kv_slots=100)
+    s.submit(0, 0.0, [1, 2], 5)
+    st, b = s.next()
+    s.complete([7])
+    s.set_token_feedback(True)
+    st, b = s.next()
+    assert b.tokens.tolist() == [7]  # the previous iteration ran without feedback: literal token
+    s.complete([8])
+    st, b = s.next()
+    assert b.tokens.tolist() == [-1]
