@@ -109,8 +109,7 @@ struct orca_engine {
 
     ~orca_engine() {
         for (cudaEvent_t e : events) cudaEventDestroy(e);
-        void *dev[] = {kv, x, y32, logits, h, qkv, attn, f, y, next, d_plan, gs.ws, gs.counters, attn_part, attn_cnt,
-                       d_err};
+        void *dev[] = {kv, x, y32, logits, h, qkv, attn, f, y, next, d_plan, attn_part, attn_cnt, d_err};
         for (void *p : dev)
             if (p) cudaFree(p);
         if (h_plan) cudaFreeHost(h_plan);
@@ -489,8 +488,6 @@ int orca_engine_create(const orca_model_config *cfg, const orca_weights *w, void
     E->attn_part_work = (int64_t)B * ceil_div(c.max_pos, 64);
     E->plan_cap = kHdr + 64 + 8 * (int64_t)B + 3 * (int64_t)R + 2 * E->attn_part_work + 2 * ((int64_t)R / 16 + B);
     E->gs.num_sms = E->num_sms;
-    E->gs.n_counters = 2 * E->num_sms;
-    E->gs.ws_floats = (size_t)E->gs.n_counters * 256 * 128;
     int rc = ORCA_OK;
     const size_t kv_bytes = (size_t)c.n_layers * 2 * H * (size_t)c.kv_slots * es;
     if (rc == ORCA_OK) rc = dev_alloc(&E->kv, kv_bytes);
@@ -504,8 +501,6 @@ int orca_engine_create(const orca_model_config *cfg, const orca_weights *w, void
     if (rc == ORCA_OK) rc = dev_alloc(&E->logits, B * (size_t)c.vocab * 4);
     if (rc == ORCA_OK) rc = dev_alloc(&E->next, B * 4);
     if (rc == ORCA_OK) rc = dev_alloc(&E->d_plan, (size_t)E->plan_cap * 4);
-    if (rc == ORCA_OK) rc = dev_alloc(&E->gs.ws, E->gs.ws_floats * 4);
-    if (rc == ORCA_OK) rc = dev_alloc(&E->gs.counters, (size_t)E->gs.n_counters * 4);
     if (rc == ORCA_OK) rc = dev_alloc(&E->attn_part, (size_t)E->attn_part_work * c.n_heads * (d + 2) * 4);
     if (rc == ORCA_OK) rc = dev_alloc(&E->attn_cnt, B * c.n_heads * 4);
     if (rc == ORCA_OK) rc = dev_alloc(&E->d_err, 4);
@@ -516,8 +511,7 @@ int orca_engine_create(const orca_model_config *cfg, const orca_weights *w, void
     if (rc == ORCA_OK) {
         *E->h_err = 0;
         E->gs.err = E->d_err;
-        if (cudaMemset(E->gs.counters, 0, (size_t)E->gs.n_counters * 4) != cudaSuccess ||
-            cudaMemset(E->attn_cnt, 0, B * c.n_heads * 4) != cudaSuccess || cudaMemset(E->d_err, 0, 4) != cudaSuccess ||
+        if (cudaMemset(E->attn_cnt, 0, B * c.n_heads * 4) != cudaSuccess || cudaMemset(E->d_err, 0, 4) != cudaSuccess ||
             cudaMemset(E->next, 0, B * 4) != cudaSuccess)
             rc = ORCA_ERR_CUDA;
     }

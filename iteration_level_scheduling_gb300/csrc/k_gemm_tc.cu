@@ -20,11 +20,17 @@
 // mbarriers decouples loads from MMAs; tcgen05.commit releases a stage when the
 // MMAs reading it are done.
 //
-// Small sum L (decode) gives few output tiles, so K is split across CTAs
-// (split-K); each CTA writes an fp32 partial tile and the last CTA of the tile
-// to arrive (atomic counter, no waiting) sums the partials in split order and
-// runs the epilogue.  Epilogue: + bias, exact GeLU, + residual (fp32), store
-// fp32 or bf16 rows [token, feature] (coalesced along features).
+// Small sum L (decode) gives few output tiles, so K is split across the CTAs
+// of a thread-block cluster (split-K, up to 8 ways).  Each CTA stages its fp32
+// accumulator tile in its own shared memory; after a cluster barrier every CTA
+// reduces a slice of the tile's token rows by reading all partial tiles over
+// distributed shared memory, in split order (deterministic), and runs the
+// epilogue for that slice.  No global workspace, no atomics, no CTA waits on a
+// flag written by another.
+//
+// Epilogue: + bias, exact GeLU, + residual (fp32), store fp32 or bf16 rows
+// [token, feature] with 16-byte (fp32) or 8-byte (bf16) stores along the
+// feature dimension, four rows per warp in flight.
 //
 // Every mbarrier wait is bounded (see common.cuh); on expiry the CTA records
 // an error bit, skips its remaining work and still frees its tensor memory.
@@ -43,20 +49,24 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
+constexpr int kWarps = kThreads / 32;
 constexpr int kMaxStages = 8;
+constexpr int kMinStages = 4;  // the staged accumulator tile (bn x 512 B) must fit in the ring
+constexpr int kMaxSplits = 8;  // portable cluster size
 constexpr int kStageA = BM * BK * 2;  // 16 KiB
 constexpr int kGroup = 16;            // feature tiles per raster group
+constexpr int kRows = 4;              // epilogue rows per warp in flight
 constexpr size_t kSmemPerSm = 228 * 1024;
 constexpr size_t kSmemMaxCta = 227 * 1024;
 constexpr size_t kSmemReserve = 1024;  // per CTA, kept by the driver
+constexpr size_t kSmemExtra = 1024 + 256;  // alignment slack + barriers
 
 struct TcArgs {
     int m_tok, n_out, num_kb, kb_per_split, splits, bn, stages;
     int n_feat_tiles, n_tok_tiles;
     uint32_t idesc, tmem_cols;
     Epilogue e;
-    float *ws;
-    int *counters;
+    int vec_out;  // output / residual rows allow 16-byte (fp32) or 8-byte (bf16) vector access
     unsigned *err;
 };
 
@@ -68,18 +78,6 @@ __device__ __forceinline__ void tile_coords(int lin, const TcArgs &a, int &ft, i
     const int r = lin - g * per_group;
     ft = first + r % gsize;
     tt = r / gsize;
-}
-
-__device__ __forceinline__ void epilogue_store(const Epilogue &e, int t, int f, float y, float bias) {
-    y += bias;
-    if (e.gelu) y = gelu_erf(y);
-    const size_t o = (size_t)t * e.ld_out + f;
-    if (e.resid)
-        e.out_f32[o] = e.resid[o] + y;
-    else if (e.out_f32)
-        e.out_f32[o] = y;
-    else
-        e.out_bf16[o] = __float2bfloat16_rn(y);
 }
 
 // AND of `v` over the 128 epilogue threads (named barrier 1).
@@ -96,24 +94,55 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
     return r != 0;
 }
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Hardware barrier over every thread of every CTA of the cluster (all CTAs of
+// a cluster are co-resident by construction, so it cannot wait on a CTA that
+// is not running).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float4 dsmem_ld4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stage_b = a.bn * BK * 2;
     const int stage_bytes = kStageA + stage_b;
+    float *stage_c = reinterpret_cast<float *>(smem);  // accumulator tile [bn][128] after the mainloop
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.stages * stage_bytes);
     uint64_t *empty = full + kMaxStages;
     uint64_t *done = empty + kMaxStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
-    volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);  // [0] abort, [1] last arriver
+    volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);  // [0] abort
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = a.splits;
+    const int split = S > 1 ? (int)cluster_rank() : 0;
     int ft, tt;
-    tile_coords(blockIdx.x, a, ft, tt);
-    const int split = blockIdx.y;
+    tile_coords(blockIdx.x / S, a, ft, tt);
     const int kb0 = split * a.kb_per_split;
     const int nkb = min(a.num_kb, kb0 + a.kb_per_split) - kb0;
+    const int t_base = tt * a.bn;
+    const int t_lim = min(a.bn, a.m_tok - t_base);  // valid token columns of this tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
@@ -122,7 +151,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(done, 1);
         flags[0] = 0;
-        flags[1] = 0;
         fence_mbar_init();
         prefetch_tmap(&tmw);
         prefetch_tmap(&tmx);
@@ -156,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d_hint(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM, pol_w);
                 else
                     tma_load_2d(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM);
-                tma_load_2d(sa + kStageA, &tmx, &full[s], (kb0 + i) * BK, tt * a.bn);
+                tma_load_2d(sa + kStageA, &tmx, &full[s], (kb0 + i) * BK, t_base);
                 ++issued;
             }
             if (!ok) {
@@ -193,59 +221,109 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ------------------------------ epilogue ------------------------------
+        // --------- epilogue phase 1: TMEM -> shared memory tile [token][feature] ---------
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;  // output feature within the tile
-        const int f = ft * BM + row;
-        const bool f_ok = f < a.n_out;
-        const int t_base = tt * a.bn;
-        const int t_lim = min(a.bn, a.m_tok - t_base);  // valid token columns
-        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
         bool ok = mbar_wait_bounded(done, 0, a.err);
         tc_fence_after();
-        ok = ok && flags[0] == 0;
-        ok = epilogue_all(ok);  // the four epilogue warps take the same branch
-        const float bias = (a.e.bias && f_ok) ? a.e.bias[f] : 0.f;
-        __syncwarp();  // tcgen05.ld is .sync.aligned: the warp must be converged
-        if (ok && a.splits == 1) {
-            for (int c0 = 0; c0 < t_lim; c0 += 16) {
-                float v[16];
-                tmem_ld16(taddr + c0, v);
-                if (f_ok) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (c0 + j < t_lim) epilogue_store(a.e, t_base + c0 + j, f, v[j], bias);
-                }
-            }
-        } else if (ok) {
-            const int tile = blockIdx.x;
-            float *wsp = a.ws + (size_t)(tile * a.splits + split) * a.bn * BM;
+        ok = epilogue_all(ok && flags[0] == 0);  // the four epilogue warps take the same branch
+        __syncwarp();                            // tcgen05.ld is .sync.aligned
+        if (ok) {
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
             for (int c0 = 0; c0 < t_lim; c0 += 16) {
                 float v[16];
                 tmem_ld16(taddr + c0, v);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) wsp[(size_t)(c0 + j) * BM + row] = v[j];
+                for (int j = 0; j < 16; ++j) stage_c[(c0 + j) * BM + row] = v[j];
             }
-            __threadfence();
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (warp == 2 && lane == 0) flags[1] = (atomicAdd(&a.counters[tile], 1) == a.splits - 1);
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (flags[1]) {
-                __threadfence();
-                const float *base = a.ws + (size_t)tile * a.splits * a.bn * BM;
-                if (f_ok) {
-                    for (int c = 0; c < t_lim; ++c) {
-                        float acc = 0.f;
-                        for (int s = 0; s < a.splits; ++s) acc += __ldcg(base + ((size_t)s * a.bn + c) * BM + row);
-                        epilogue_store(a.e, t_base + c, f, acc, bias);
-                    }
-                }
-                if (warp == 2 && lane == 0) a.counters[tile] = 0;
-            }
+        } else if (threadIdx.x == 64) {
+            flags[0] = 1;
         }
     }
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    if (S > 1)
+        cluster_sync_all();
+    else
+        __syncthreads();
+
+    // --------- epilogue phase 2: reduce the split partials, bias / GeLU / residual, store ---------
+    if (flags[0] == 0) {
+        const Epilogue &e = a.e;
+        const int f0 = ft * BM + 4 * lane;
+        const bool full4 = a.vec_out && f0 + 3 < a.n_out;
+        float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e.bias) {
+            if (f0 + 0 < a.n_out) bias.x = e.bias[f0 + 0];
+            if (f0 + 1 < a.n_out) bias.y = e.bias[f0 + 1];
+            if (f0 + 2 < a.n_out) bias.z = e.bias[f0 + 2];
+            if (f0 + 3 < a.n_out) bias.w = e.bias[f0 + 3];
+        }
+        const int rs = (t_lim + S - 1) / S;
+        const int r0 = split * rs, r1 = min(t_lim, r0 + rs);
+        const uint32_t cbase = smem_u32(stage_c) + 16u * lane;
+        for (int t0 = r0 + warp * kRows; t0 < r1; t0 += kWarps * kRows) {
+            float4 acc[kRows];
+            float4 res[kRows];
+#pragma unroll
+            for (int u = 0; u < kRows; ++u) {
+                const int t = t0 + u;
+                acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                res[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t < r1) {
+                    if (S == 1) {
+                        acc[u] = *reinterpret_cast<const float4 *>(stage_c + t * BM + 4 * lane);
+                    } else {
+                        const uint32_t local = cbase + (uint32_t)(t * BM * 4);
+                        for (int s = 0; s < S; ++s) acc[u] = add4(acc[u], dsmem_ld4(dsmem_map(local, (uint32_t)s)));
+                    }
+                    if (e.resid && full4)
+                        res[u] = *reinterpret_cast<const float4 *>(e.resid + (size_t)(t_base + t) * e.ld_out + f0);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kRows; ++u) {
+                const int t = t0 + u;
+                if (t >= r1) break;
+                float y[4] = {acc[u].x + bias.x, acc[u].y + bias.y, acc[u].z + bias.z, acc[u].w + bias.w};
+                if (e.gelu) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) y[q] = gelu_erf(y[q]);
+                }
+                const size_t o = (size_t)(t_base + t) * e.ld_out + f0;
+                if (full4) {
+                    if (e.resid) {
+                        *reinterpret_cast<float4 *>(e.out_f32 + o) =
+                            make_float4(res[u].x + y[0], res[u].y + y[1], res[u].z + y[2], res[u].w + y[3]);
+                    } else if (e.out_f32) {
+                        *reinterpret_cast<float4 *>(e.out_f32 + o) = make_float4(y[0], y[1], y[2], y[3]);
+                    } else {
+                        __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]), hi = __floats2bfloat162_rn(y[2], y[3]);
+                        uint2 pk;
+                        pk.x = *reinterpret_cast<uint32_t *>(&lo);
+                        pk.y = *reinterpret_cast<uint32_t *>(&hi);
+                        *reinterpret_cast<uint2 *>(e.out_bf16 + o) = pk;
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (f0 + q >= a.n_out) break;
+                        if (e.resid)
+                            e.out_f32[o + q] = e.resid[o + q] + y[q];
+                        else if (e.out_f32)
+                            e.out_f32[o + q] = y[q];
+                        else
+                            e.out_bf16[o + q] = __float2bfloat16_rn(y[q]);
+                    }
+                }
+            }
+        }
+    }
+    __syncwarp();
+    if (S > 1)
+        cluster_sync_all();  // peers may still be reading this CTA's tile
+    else
+        __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -310,20 +388,18 @@ TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s) {
     while ((int)t.tmem_cols < t.bn) t.tmem_cols *= 2;
     const int stage_bytes = kStageA + t.bn * BK * 2;
     const int ctas_per_sm = t.bn <= 128 ? 2 : 1;
-    const size_t budget = std::min(kSmemMaxCta, kSmemPerSm / ctas_per_sm - kSmemReserve) - 1024 - 256;
+    const size_t budget = std::min(kSmemMaxCta, kSmemPerSm / ctas_per_sm - kSmemReserve) - kSmemExtra;
     t.stages = std::min<int>(kMaxStages, (int)(budget / stage_bytes));
     if (override_stages() > 0)
-        t.stages = std::min<int>(std::min(override_stages(), kMaxStages), (int)((kSmemMaxCta - 1280) / stage_bytes));
-    t.smem = (size_t)t.stages * stage_bytes + 1024 + 256;
+        t.stages = std::max(kMinStages, std::min<int>(std::min(override_stages(), kMaxStages),
+                                                      (int)((kSmemMaxCta - kSmemExtra) / stage_bytes)));
+    t.smem = (size_t)t.stages * stage_bytes + kSmemExtra;
     const int num_kb = k / BK;
     const int tiles = t.n_tok_tiles * t.n_feat_tiles;
     const int capacity = s.num_sms * ctas_per_sm;
     int splits = 1;
-    if (tiles < capacity && tiles <= s.n_counters && s.ws) {
-        splits = std::max(1, std::min(capacity / tiles, num_kb / 4));
-        if (override_splits() > 0) splits = std::min(override_splits(), num_kb);
-        while (splits > 1 && (size_t)tiles * splits * t.bn * BM > s.ws_floats) --splits;
-    }
+    if (tiles < capacity) splits = std::max(1, std::min({kMaxSplits, capacity / tiles, num_kb / 4}));
+    if (override_splits() > 0) splits = std::min({override_splits(), kMaxSplits, num_kb});
     t.kb_per_split = ceil_div(num_kb, splits);
     t.splits = ceil_div(num_kb, t.kb_per_split);
     return t;
@@ -334,6 +410,7 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok
     if (m_tok <= 0) return cudaSuccess;
     if (k % BK != 0 || k <= 0 || n_out <= 0 || x_rows_cap < m_tok) return cudaErrorInvalidValue;
     const TcShape t = gemm_tc_shape(m_tok, n_out, k, s);
+    if (t.stages < kMinStages) return cudaErrorInvalidValue;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t ae = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -356,12 +433,24 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok
     a.idesc = idesc_bf16_f32(BM, t.bn);
     a.tmem_cols = (uint32_t)t.tmem_cols;
     a.e = e;
-    a.ws = s.ws;
-    a.counters = s.counters;
+    const uintptr_t align_mask = e.out_bf16 ? 7 : 15;
+    a.vec_out = (e.ld_out % 4 == 0) &&
+                !(reinterpret_cast<uintptr_t>(e.out_f32 ? (const void *)e.out_f32 : (const void *)e.out_bf16) & align_mask) &&
+                !(reinterpret_cast<uintptr_t>(e.resid) & 15);
     a.err = s.err;
-    dim3 grid(t.n_feat_tiles * t.n_tok_tiles, t.splits);
-    gemm_tc_kernel<<<grid, kThreads, t.smem, st>>>(mw, mx, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(t.n_feat_tiles * t.n_tok_tiles * t.splits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = t.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)t.splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = t.splits > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, mw, mx, a);
 }
 
 }  // namespace orca

@@ -21,12 +21,8 @@ struct Epilogue {
     int ld_out = 0;
 };
 
-// Scratch shared by the split-K GEMM reduction.
+// Launch context of the tensor-core GEMM: the device error word and the SM count.
 struct GemmScratch {
-    float *ws = nullptr;      // partial tiles
-    size_t ws_floats = 0;
-    int *counters = nullptr;  // per output tile, zero between launches
-    int n_counters = 0;
     unsigned *err = nullptr;
     int num_sms = 148;
 };
