@@ -51,7 +51,6 @@ constexpr int BK = 64;
 constexpr int kThreads = 192;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxStages = 8;
-constexpr int kMinStages = 4;  // the staged accumulator tile (bn x 512 B) must fit in the ring
 constexpr int kMaxSplits = 8;  // portable cluster size
 constexpr int kStageA = BM * BK * 2;  // 16 KiB
 constexpr int kGroup = 16;            // feature tiles per raster group
@@ -387,12 +386,14 @@ TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s) {
     t.tmem_cols = 32;
     while ((int)t.tmem_cols < t.bn) t.tmem_cols *= 2;
     const int stage_bytes = kStageA + t.bn * BK * 2;
-    const int ctas_per_sm = t.bn <= 128 ? 2 : 1;
+    const size_t max_stages_1cta = (kSmemMaxCta - kSmemExtra) / stage_bytes;
+    int ctas_per_sm = t.bn <= 128 ? 2 : 1;
     const size_t budget = std::min(kSmemMaxCta, kSmemPerSm / ctas_per_sm - kSmemReserve) - kSmemExtra;
     t.stages = std::min<int>(kMaxStages, (int)(budget / stage_bytes));
-    if (override_stages() > 0)
-        t.stages = std::max(kMinStages, std::min<int>(std::min(override_stages(), kMaxStages),
-                                                      (int)((kSmemMaxCta - kSmemExtra) / stage_bytes)));
+    if (override_stages() > 0) t.stages = std::min<int>(std::min(override_stages(), kMaxStages), (int)max_stages_1cta);
+    // the ring must also hold the staged fp32 accumulator tile (bn x 512 B) after the mainloop
+    while ((size_t)t.stages * stage_bytes < (size_t)t.bn * BM * 4 && t.stages < (int)max_stages_1cta) ++t.stages;
+    if ((size_t)t.stages * stage_bytes + kSmemExtra > kSmemPerSm / 2 - kSmemReserve) ctas_per_sm = 1;
     t.smem = (size_t)t.stages * stage_bytes + kSmemExtra;
     const int num_kb = k / BK;
     const int tiles = t.n_tok_tiles * t.n_feat_tiles;
@@ -410,7 +411,7 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok
     if (m_tok <= 0) return cudaSuccess;
     if (k % BK != 0 || k <= 0 || n_out <= 0 || x_rows_cap < m_tok) return cudaErrorInvalidValue;
     const TcShape t = gemm_tc_shape(m_tok, n_out, k, s);
-    if (t.stages < kMinStages) return cudaErrorInvalidValue;
+    if ((size_t)t.stages * (kStageA + t.bn * BK * 2) < (size_t)t.bn * BM * 4) return cudaErrorInvalidValue;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t ae = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
