@@ -149,7 +149,7 @@ int decode_chunk(const orca_engine *E, const orca_batch *b) {
     int64_t keys = 0, n = 0;
     for (int i = 0; i < b->n_req; ++i)
         if (b->n_input[i] == 1) keys += (int64_t)b->ctx_len[i] + 1, ++n;
-    int chunk = 256;
+    int chunk = 512;
     // shrink the chunk until the decode grid has a few CTAs per SM
     while (chunk > 64) {
         int64_t items = 0;
@@ -349,13 +349,13 @@ int run_plan(orca_engine *E, const int32_t *hp, const int32_t *dp, int32_t *dev_
             ORCA_TRY(E->launch(ORCA_K_ATTN_DECODE, l, es * (2.0 * dec_keys * H + 2.0 * hp[P_NDEC] * H),
                                4.0 * dec_keys * H, [&] {
                                    return attention<T>(qkv, pool_l, E->cfg.kv_slots, attn, ap, H, nh, E->attn_part,
-                                                       E->attn_cnt, st, true, false);
+                                                       E->attn_cnt, E->d_err, st, true, false);
                                }));
         if (ap.n_pre_tiles > 0)
             ORCA_TRY(E->launch(ORCA_K_ATTN_PREFILL, l, es * (2.0 * pre_keys * H + 2.0 * (R - hp[P_NDEC]) * H),
                                4.0 * pre_pairs * H, [&] {
                                    return attention<T>(qkv, pool_l, E->cfg.kv_slots, attn, ap, H, nh, E->attn_part,
-                                                       E->attn_cnt, st, false, true);
+                                                       E->attn_cnt, E->d_err, st, false, true);
                                }));
         {
             Epilogue e;

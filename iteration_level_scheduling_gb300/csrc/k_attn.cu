@@ -14,9 +14,10 @@
 // head of one request are contiguous (head_dim * elem bytes per token).
 //
 // decode  : requests with one input row (increment phase).  Work item =
-//           (request, chunk of `chunk` keys) x head; a request whose keys span
-//           several chunks is merged by the last CTA to finish (per-(request,
-//           head) arrival counter; no CTA ever waits on another).
+//           (request, chunk of `chunk` keys) x head, its K/V rows streamed into
+//           shared memory by bulk asynchronous copies; a request whose keys
+//           span several chunks is merged by the last CTA to finish (per-
+//           (request, head) arrival counter; no CTA ever waits on another).
 // prefill : requests with several input rows (initiation phase, or any
 //           multi-row request).  Work item = (request, 16 query rows) x head;
 //           each warp owns one query row and attends causally over keys
@@ -46,6 +47,7 @@ struct AttnArgs {
     AttnPlan p;
     float *part;
     int *counters;
+    unsigned *err;
 };
 
 // One warp attends its query (q, already scaled, VEC values of its lane's
@@ -121,53 +123,162 @@ __device__ __forceinline__ void merge_groups(float &m, float &l, float *o) {
     }
 }
 
+// Decode: the K and V rows of one (request, head, chunk) are contiguous in the
+// pool, so a producer warp streams them into a ring of shared-memory stages
+// with bulk asynchronous copies (kDecTok tokens of K and of V per stage,
+// completing on an mbarrier); four consumer warps score and accumulate from
+// shared memory and release each stage through a second mbarrier.
+constexpr int kDecStages = 4;
+constexpr int kDecConsumers = 4;
+constexpr int kDecThreads = 32 * (kDecConsumers + 1);
+
+// Tokens per stage: at least 32, and at least one warp-wide step per consumer.
 template <typename T, int D>
-__global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArgs<T> a) {
+constexpr int dec_tok() {
+    return 32 > kDecConsumers * (32 / (D / Elem<T>::kPer16)) ? 32 : kDecConsumers * (32 / (D / Elem<T>::kPer16));
+}
+
+template <typename T, int D>
+struct DecodeSmem {
+    static constexpr int kTok = dec_tok<T, D>();
+    T kv[kDecStages][2][kTok][D];
+    uint64_t full[kDecStages], empty[kDecStages];
+    float m[kDecConsumers], l[kDecConsumers];
+    float o[kDecConsumers][D];
+    int last, abort;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const AttnArgs<T> a) {
     constexpr int VEC = Elem<T>::kPer16;
     constexpr int LPT = D / VEC;
-    constexpr int TPW = 32 / LPT;
-    constexpr int U = 4;
-    __shared__ float sm_m[kAttnWarps], sm_l[kAttnWarps];
-    __shared__ float sm_o[kAttnWarps][D];
-    __shared__ int sm_last;
+    constexpr int TPW = 32 / LPT;                      // tokens per warp-wide step
+    constexpr int kDecTok = DecodeSmem<T, D>::kTok;
+    constexpr int PER_WARP = kDecTok / kDecConsumers;  // tokens of a stage per consumer warp
+    constexpr int STEPS = PER_WARP / TPW;
+    static_assert(PER_WARP % TPW == 0, "stage split");
+    extern __shared__ __align__(128) uint8_t dyn_smem[];
+    DecodeSmem<T, D> &sm = *reinterpret_cast<DecodeSmem<T, D> *>(dyn_smem);
 
     const int w_idx = blockIdx.x, h = blockIdx.y;
     const int i = a.p.dec_work[2 * w_idx], c = a.p.dec_work[2 * w_idx + 1];
     const int row = a.p.req_off[i];
     const int n_keys = a.p.req_ctx[i] + 1;
     const int t0 = c * a.p.chunk, t1 = min(n_keys, t0 + a.p.chunk);
+    const int n_it = (t1 - t0 + kDecTok - 1) / kDecTok;
+    const size_t head_base = ((size_t)h * a.kv_slots + a.p.req_kvoff[i]) * D;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sub = lane % LPT;
 
-    float q[VEC];
-    load16(a.qkv + (size_t)row * 3 * a.H + h * D + sub * VEC, q);
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) q[e] *= a.scale_log2;
-    const size_t head_base = ((size_t)h * a.kv_slots + a.p.req_kvoff[i]) * D + sub * VEC;
-    float m = kNegBig, l = 0.f, o[VEC];
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) o[e] = 0.f;
-    attend_range<T, D, U>(q, a.kpool + head_base, a.vpool + head_base, t0 + warp * TPW, t1, kAttnWarps * TPW, m, l,
-                          o);
-    merge_groups<LPT, VEC>(m, l, o);
-    if (lane < LPT) {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) sm_o[warp][sub * VEC + e] = o[e];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kDecStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kDecConsumers);
+        }
+        sm.abort = 0;
+        fence_mbar_init();
     }
-    if (lane == 0) sm_m[warp] = m, sm_l[warp] = l;
     __syncthreads();
+
+    if (warp == kDecConsumers) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();  // every cached row is read once per iteration
+            int issued = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it % kDecStages;
+                const uint32_t ph = (uint32_t)(it / kDecStages) & 1u;
+                if (!mbar_wait_bounded(&sm.empty[s], ph ^ 1u, a.err)) {
+                    sm.abort = 1;
+                    break;
+                }
+                const int t = t0 + it * kDecTok;
+                const uint32_t bytes = (uint32_t)(min(kDecTok, t1 - t) * D * sizeof(T));
+                mbar_arrive_expect_tx(&sm.full[s], 2 * bytes);
+                bulk_load(&sm.kv[s][0][0][0], a.kpool + head_base + (size_t)t * D, bytes, &sm.full[s], pol);
+                bulk_load(&sm.kv[s][1][0][0], a.vpool + head_base + (size_t)t * D, bytes, &sm.full[s], pol);
+                ++issued;
+            }
+            if (sm.abort)  // let the copies in flight land before the CTA exits
+                for (int j = max(0, issued - kDecStages); j < issued; ++j)
+                    mbar_wait_bounded(&sm.full[j % kDecStages], (uint32_t)(j / kDecStages) & 1u, a.err);
+        }
+    } else {
+        // ------------------------------ consumers -----------------------------
+        const int g = lane / LPT, sub = lane % LPT;
+        float q[VEC];
+        load16(a.qkv + (size_t)row * 3 * a.H + h * D + sub * VEC, q);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) q[e] *= a.scale_log2;
+        float m = kNegBig, l = 0.f, o[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[e] = 0.f;
+        for (int it = 0; it < n_it; ++it) {
+            const int s = it % kDecStages;
+            const uint32_t ph = (uint32_t)(it / kDecStages) & 1u;
+            if (!mbar_wait_bounded(&sm.full[s], ph, a.err)) {
+                sm.abort = 1;
+                break;
+            }
+            const int ntok = min(kDecTok, t1 - (t0 + it * kDecTok));
+            float sc[STEPS], vv[STEPS][VEC];
+#pragma unroll
+            for (int st = 0; st < STEPS; ++st) {
+                const int j = warp * PER_WARP + st * TPW + g;
+                const bool valid = j < ntok;
+                float kk[VEC];
+                if (valid) {
+                    load16(&sm.kv[s][0][j][sub * VEC], kk);
+                    load16(&sm.kv[s][1][j][sub * VEC], vv[st]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) kk[e] = 0.f, vv[st][e] = 0.f;
+                }
+                float acc = 0.f;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc = fmaf(q[e], kk[e], acc);
+#pragma unroll
+                for (int off = LPT / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                sc[st] = valid ? acc : kNegBig;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);  // this warp's rows of stage s are in registers
+            float mx = m;
+#pragma unroll
+            for (int st = 0; st < STEPS; ++st) mx = fmaxf(mx, sc[st]);
+            const float corr = exp2f(m - mx);
+            l *= corr;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[e] *= corr;
+#pragma unroll
+            for (int st = 0; st < STEPS; ++st) {
+                const float pr = sc[st] > kNegBig ? exp2f(sc[st] - mx) : 0.f;
+                l += pr;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = fmaf(pr, vv[st][e], o[e]);
+            }
+            m = mx;
+        }
+        merge_groups<LPT, VEC>(m, l, o);
+        if (lane < LPT) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) sm.o[warp][sub * VEC + e] = o[e];
+        }
+        if (lane == 0) sm.m[warp] = m, sm.l[warp] = l;
+    }
+    __syncthreads();
+    if (sm.abort) return;
 
     const int nch = a.p.dec_nch[i];
     float M = kNegBig, L = 0.f, O = 0.f;
     const int d = threadIdx.x;
     if (d < D) {
 #pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, sm_m[w]);
+        for (int w = 0; w < kDecConsumers; ++w) M = fmaxf(M, sm.m[w]);
 #pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w) {
-            const float cw = exp2f(sm_m[w] - M);
-            L += sm_l[w] * cw;
-            O += sm_o[w][d] * cw;
+        for (int w = 0; w < kDecConsumers; ++w) {
+            const float cw = exp2f(sm.m[w] - M);
+            L += sm.l[w] * cw;
+            O += sm.o[w][d] * cw;
         }
     }
     T *dst = a.out + (size_t)row * a.H + h * D;
@@ -183,10 +294,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
     __syncthreads();
     if (threadIdx.x == 0) {
         const int old = atomicAdd(&a.counters[i * a.n_heads + h], 1);
-        sm_last = (old == nch - 1);
+        sm.last = (old == nch - 1);
     }
     __syncthreads();
-    if (!sm_last) return;
+    if (!sm.last) return;
     __threadfence();
     if (d < D) {
         const int wb = a.p.dec_wbegin[i];
@@ -244,7 +355,14 @@ __global__ void __launch_bounds__(kAttnThreads) attn_prefill_kernel(const AttnAr
 template <typename T, int D>
 cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStream_t st) {
     if (decode && a.p.n_dec_work > 0) {
-        attn_decode_kernel<T, D><<<dim3(a.p.n_dec_work, a.n_heads), kAttnThreads, 0, st>>>(a);
+        static bool attr = false;
+        if (!attr) {
+            cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)sizeof(DecodeSmem<T, D>));
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        attn_decode_kernel<T, D><<<dim3(a.p.n_dec_work, a.n_heads), kDecThreads, sizeof(DecodeSmem<T, D>), st>>>(a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -260,7 +378,8 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
 
 template <typename T>
 cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *out, const AttnPlan &p, int H,
-                      int n_heads, float *part, int *counters, cudaStream_t st, bool decode, bool prefill) {
+                      int n_heads, float *part, int *counters, unsigned *err, cudaStream_t st, bool decode,
+                      bool prefill) {
     const int D = H / n_heads;
     AttnArgs<T> a;
     a.qkv = qkv;
@@ -274,6 +393,7 @@ cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *ou
     a.p = p;
     a.part = part;
     a.counters = counters;
+    a.err = err;
     switch (D) {
         case 16: return launch_attn<T, 16>(a, decode, prefill, st);
         case 32: return launch_attn<T, 32>(a, decode, prefill, st);
@@ -284,8 +404,8 @@ cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *ou
 }
 
 template cudaError_t attention<float>(const float *, const float *, int64_t, float *, const AttnPlan &, int, int,
-                                      float *, int *, cudaStream_t, bool, bool);
+                                      float *, int *, unsigned *, cudaStream_t, bool, bool);
 template cudaError_t attention<bf16>(const bf16 *, const bf16 *, int64_t, bf16 *, const AttnPlan &, int, int,
-                                     float *, int *, cudaStream_t, bool, bool);
+                                     float *, int *, unsigned *, cudaStream_t, bool, bool);
 
 }  // namespace orca

@@ -273,8 +273,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (S == 1) {
                         acc[u] = *reinterpret_cast<const float4 *>(stage_c + t * BM + 4 * lane);
                     } else {
+                        // issue every peer's load before the first add (fixed split order for the sum)
                         const uint32_t local = cbase + (uint32_t)(t * BM * 4);
-                        for (int s = 0; s < S; ++s) acc[u] = add4(acc[u], dsmem_ld4(dsmem_map(local, (uint32_t)s)));
+                        float4 v[kMaxSplits];
+#pragma unroll
+                        for (int s = 0; s < kMaxSplits; ++s)
+                            if (s < S) v[s] = dsmem_ld4(dsmem_map(local, (uint32_t)s));
+#pragma unroll
+                        for (int s = 0; s < kMaxSplits; ++s)
+                            if (s < S) acc[u] = add4(acc[u], v[s]);
                     }
                     if (e.resid && full4)
                         res[u] = *reinterpret_cast<const float4 *>(e.resid + (size_t)(t_base + t) * e.ld_out + f0);

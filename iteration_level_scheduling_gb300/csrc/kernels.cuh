@@ -70,7 +70,8 @@ struct AttnPlan {
 // their cached keys.  Prefill: requests with several rows, causal.
 template <typename T>
 cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *out, const AttnPlan &p, int H,
-                      int n_heads, float *part, int *counters, cudaStream_t st, bool decode, bool prefill);
+                      int n_heads, float *part, int *counters, unsigned *err, cudaStream_t st, bool decode,
+                      bool prefill);
 
 // next[b] = argmax_j logits[b, j] (lowest j on ties); also to out2 if non-null.
 cudaError_t argmax_rows(const float *logits, int n_rows, int V, int32_t *next, int32_t *out2, cudaStream_t st);
