@@ -92,6 +92,8 @@ struct orca_engine {
     int32_t *h_plan = nullptr, *d_plan = nullptr;
     int64_t plan_cap = 0;
     GemmScratch gs;
+    float *part = nullptr;  // split-K partial slabs of the residual projections
+    size_t part_cap = 0;
     float *attn_part = nullptr;
     int *attn_cnt = nullptr;
     int64_t attn_part_work = 0;
@@ -109,7 +111,7 @@ struct orca_engine {
 
     ~orca_engine() {
         for (cudaEvent_t e : events) cudaEventDestroy(e);
-        void *dev[] = {kv, x, y32, logits, h, qkv, attn, f, y, next, d_plan, attn_part, attn_cnt, d_err};
+        void *dev[] = {kv, x, y32, logits, h, qkv, attn, f, y, next, d_plan, part, attn_part, attn_cnt, d_err};
         for (void *p : dev)
             if (p) cudaFree(p);
         if (h_plan) cudaFreeHost(h_plan);
@@ -284,9 +286,11 @@ int build(orca_engine *E, const orca_batch *b, int32_t *buf, int64_t cap) {
 }
 
 template <typename T>
-cudaError_t linear(orca_engine *E, const void *x, int x_cap, const void *w, int m, int n, int k, const Epilogue &e) {
+cudaError_t linear(orca_engine *E, const void *x, int x_cap, const void *w, int m, int n, int k, const Epilogue &e,
+                   int *n_partials = nullptr) {
+    if (n_partials) *n_partials = 0;
     if constexpr (std::is_same<T, bf16>::value)
-        return gemm_tc_bf16((const bf16 *)x, x_cap, (const bf16 *)w, m, n, k, e, E->gs, E->st);
+        return gemm_tc_bf16((const bf16 *)x, x_cap, (const bf16 *)w, m, n, k, e, E->gs, E->st, n_partials);
     else
         return gemm_simt_f32((const float *)x, (const float *)w, m, n, k, e, E->st);
 }
@@ -328,23 +332,37 @@ int run_plan(orca_engine *E, const int32_t *hp, const int32_t *dp, int32_t *dev_
         return embed<T>(tokens, row_pos, E->next, prev_n, (const T *)E->tok_emb, (const T *)E->pos_emb, E->x, R, H,
                         V, E->cfg.max_pos, E->d_err, st);
     }));
+    // split-K partial slabs of the last residual projection, completed by the next LayerNorm
+    int pend_n = 0;
+    const float *pend_bias = nullptr;
+    const bool bf = std::is_same<T, bf16>::value;
     for (int l = 0; l < E->L; ++l) {
         const orca_layer_weights &W = E->layers[l];
         T *pool_l = (T *)E->kv + (size_t)l * layer_elems;
-        ORCA_TRY(E->launch(ORCA_K_LN, l, R * H * (4 + es), 0, [&] {
-            return layernorm<T>(E->x, nullptr, W.ln1_g, W.ln1_b, h, nullptr, R, H, st);
+        ORCA_TRY(E->launch(ORCA_K_LN, l, R * H * (4 + es) + 4.0 * R * H * (pend_n ? pend_n + 1 : 0), 0, [&] {
+            return layernorm<T>(E->x, nullptr, W.ln1_g, W.ln1_b, h, nullptr, R, H, st, E->part, pend_n, R, pend_bias);
         }));
         {
             Epilogue e;
             e.bias = W.b_qkv;
-            if (std::is_same<T, bf16>::value) e.out_bf16 = (bf16 *)qkv; else e.out_f32 = (float *)qkv;
+            if (bf) {
+                e.out_bf16 = (bf16 *)qkv;
+                // k and v rows go straight to the pool at each row's slot (the K/V append)
+                e.kv_pool = (bf16 *)pool_l;
+                e.row_slot = row_slot;
+                e.kv_slots = E->cfg.kv_slots;
+                e.kv_h = H, e.kv_hd = E->d, e.kv_nh = nh;
+            } else {
+                e.out_f32 = (float *)qkv;
+            }
             e.ld_out = 3 * H;
             ORCA_TRY(E->launch(ORCA_K_GEMM_QKV, l, es * (3.0 * H * H + (double)R * H + 3.0 * R * H),
                                2.0 * R * 3 * H * H, [&] { return linear<T>(E, h, cap, W.w_qkv, R, 3 * H, H, e); }));
         }
-        ORCA_TRY(E->launch(ORCA_K_KV_APPEND, l, 4.0 * R * H * es, 0, [&] {
-            return kv_append<T>(qkv, row_slot, pool_l, E->cfg.kv_slots, R, H, nh, st);
-        }));
+        if (!bf)
+            ORCA_TRY(E->launch(ORCA_K_KV_APPEND, l, 4.0 * R * H * es, 0, [&] {
+                return kv_append<T>(qkv, row_slot, pool_l, E->cfg.kv_slots, R, H, nh, st);
+            }));
         if (ap.n_dec_work > 0)
             ORCA_TRY(E->launch(ORCA_K_ATTN_DECODE, l, es * (2.0 * dec_keys * H + 2.0 * hp[P_NDEC] * H),
                                4.0 * dec_keys * H, [&] {
@@ -357,17 +375,20 @@ int run_plan(orca_engine *E, const int32_t *hp, const int32_t *dp, int32_t *dev_
                                    return attention<T>(qkv, pool_l, E->cfg.kv_slots, attn, ap, H, nh, E->attn_part,
                                                        E->attn_cnt, E->d_err, st, false, true);
                                }));
+        int np_o = 0;
         {
             Epilogue e;
             e.bias = W.b_o;
             e.resid = E->x;
             e.out_f32 = E->x;
             e.ld_out = H;
+            e.part = E->part;
+            e.part_cap = E->part_cap;
             ORCA_TRY(E->launch(ORCA_K_GEMM_O, l, es * ((double)H * H + (double)R * H) + 8.0 * R * H,
-                               2.0 * R * H * H, [&] { return linear<T>(E, attn, cap, W.w_o, R, H, H, e); }));
+                               2.0 * R * H * H, [&] { return linear<T>(E, attn, cap, W.w_o, R, H, H, e, &np_o); }));
         }
-        ORCA_TRY(E->launch(ORCA_K_LN, l, R * H * (4 + es), 0, [&] {
-            return layernorm<T>(E->x, nullptr, W.ln2_g, W.ln2_b, h, nullptr, R, H, st);
+        ORCA_TRY(E->launch(ORCA_K_LN, l, R * H * (4 + es) + 4.0 * R * H * (np_o ? np_o + 1 : 0), 0, [&] {
+            return layernorm<T>(E->x, nullptr, W.ln2_g, W.ln2_b, h, nullptr, R, H, st, E->part, np_o, R, W.b_o);
         }));
         {
             Epilogue e;
@@ -384,12 +405,15 @@ int run_plan(orca_engine *E, const int32_t *hp, const int32_t *dp, int32_t *dev_
             e.resid = E->x;
             e.out_f32 = E->x;
             e.ld_out = H;
+            e.part = E->part;
+            e.part_cap = E->part_cap;
             ORCA_TRY(E->launch(ORCA_K_GEMM_FFN2, l, es * ((double)H * F + (double)R * F) + 8.0 * R * H,
-                               2.0 * R * H * F, [&] { return linear<T>(E, f, cap, W.w_2, R, H, F, e); }));
+                               2.0 * R * H * F, [&] { return linear<T>(E, f, cap, W.w_2, R, H, F, e, &pend_n); }));
+            pend_bias = W.b_2;
         }
     }
-    ORCA_TRY(E->launch(ORCA_K_FINAL_LN, -1, B * H * (8 + es), 0, [&] {
-        return layernorm<T>(E->x, last_row, E->lnf_g, E->lnf_b, y, E->y32, B, H, st);
+    ORCA_TRY(E->launch(ORCA_K_FINAL_LN, -1, B * H * (8 + es) + 4.0 * B * H * (pend_n ? pend_n + 1 : 0), 0, [&] {
+        return layernorm<T>(E->x, last_row, E->lnf_g, E->lnf_b, y, E->y32, B, H, st, E->part, pend_n, R, pend_bias);
     }));
     {
         Epilogue e;
@@ -488,6 +512,8 @@ int orca_engine_create(const orca_model_config *cfg, const orca_weights *w, void
     E->attn_part_work = (int64_t)B * ceil_div(c.max_pos, 64);
     E->plan_cap = kHdr + 64 + 8 * (int64_t)B + 3 * (int64_t)R + 2 * E->attn_part_work + 2 * ((int64_t)R / 16 + B);
     E->gs.num_sms = E->num_sms;
+    // up to 8 partial slabs of up to 512 rows (split-K is only chosen when the rows are few)
+    E->part_cap = E->bf ? (size_t)8 * std::min<size_t>(R, 512) * H : 0;
     int rc = ORCA_OK;
     const size_t kv_bytes = (size_t)c.n_layers * 2 * H * (size_t)c.kv_slots * es;
     if (rc == ORCA_OK) rc = dev_alloc(&E->kv, kv_bytes);
@@ -501,6 +527,7 @@ int orca_engine_create(const orca_model_config *cfg, const orca_weights *w, void
     if (rc == ORCA_OK) rc = dev_alloc(&E->logits, B * (size_t)c.vocab * 4);
     if (rc == ORCA_OK) rc = dev_alloc(&E->next, B * 4);
     if (rc == ORCA_OK) rc = dev_alloc(&E->d_plan, (size_t)E->plan_cap * 4);
+    if (rc == ORCA_OK && E->part_cap) rc = dev_alloc(&E->part, E->part_cap * 4);
     if (rc == ORCA_OK) rc = dev_alloc(&E->attn_part, (size_t)E->attn_part_work * c.n_heads * (d + 2) * 4);
     if (rc == ORCA_OK) rc = dev_alloc(&E->attn_cnt, B * c.n_heads * 4);
     if (rc == ORCA_OK) rc = dev_alloc(&E->d_err, 4);

@@ -51,7 +51,8 @@ constexpr int BK = 64;
 constexpr int kThreads = 192;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxStages = 8;
-constexpr int kMaxSplits = 8;  // portable cluster size
+constexpr int kMaxSplits = 8;         // split-K ways (partial slabs); also the DSMEM unroll bound
+constexpr int kMaxClusterSplits = 2;  // split-K ways reduced inside a cluster
 constexpr int kStageA = BM * BK * 2;  // 16 KiB
 constexpr int kGroup = 16;            // feature tiles per raster group
 constexpr int kRows = 4;              // epilogue rows per warp in flight
@@ -66,8 +67,10 @@ struct TcArgs {
     uint32_t idesc, tmem_cols;
     Epilogue e;
     int vec_out;  // output / residual rows allow 16-byte (fp32) or 8-byte (bf16) vector access
+    int mode;     // kDirect, kCluster (split-K reduced over DSMEM) or kPartial (split-K slabs to e.part)
     unsigned *err;
 };
+enum { kDirect = 0, kCluster = 1, kPartial = 2 };
 
 __device__ __forceinline__ void tile_coords(int lin, const TcArgs &a, int &ft, int &tt) {
     const int per_group = kGroup * a.n_tok_tiles;
@@ -135,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = a.splits;
-    const int split = S > 1 ? (int)cluster_rank() : 0;
+    const int split = a.mode == kCluster ? (int)cluster_rank() : (int)(blockIdx.x % S);
     int ft, tt;
     tile_coords(blockIdx.x / S, a, ft, tt);
     const int kb0 = split * a.kb_per_split;
@@ -241,13 +244,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncwarp();
-    if (S > 1)
+    if (a.mode == kCluster)
         cluster_sync_all();
     else
         __syncthreads();
 
     // --------- epilogue phase 2: reduce the split partials, bias / GeLU / residual, store ---------
-    if (flags[0] == 0) {
+    if (flags[0] == 0 && a.mode == kPartial) {
+        // this split's partial tile, as is, to slab `split` of the workspace
+        const int f0 = ft * BM + 4 * lane;
+        if (f0 < a.n_out) {
+            float *slab = a.e.part + (size_t)split * a.m_tok * a.n_out;
+            for (int t = warp; t < t_lim; t += kWarps)
+                *reinterpret_cast<float4 *>(slab + (size_t)(t_base + t) * a.n_out + f0) =
+                    *reinterpret_cast<const float4 *>(stage_c + t * BM + 4 * lane);
+        }
+    } else if (flags[0] == 0) {
         const Epilogue &e = a.e;
         const int f0 = ft * BM + 4 * lane;
         const bool full4 = a.vec_out && f0 + 3 < a.n_out;
@@ -258,8 +270,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (f0 + 2 < a.n_out) bias.z = e.bias[f0 + 2];
             if (f0 + 3 < a.n_out) bias.w = e.bias[f0 + 3];
         }
-        const int rs = (t_lim + S - 1) / S;
-        const int r0 = split * rs, r1 = min(t_lim, r0 + rs);
+        const int SC = a.mode == kCluster ? S : 1;  // CTAs sharing this tile's epilogue
+        const int rs = (t_lim + SC - 1) / SC;
+        const int r0 = (SC > 1 ? split : 0) * rs, r1 = min(t_lim, r0 + rs);
+        // K/V append: output features >= kv_h go to the pool at the row's slot
+        bf16 *kv_dst = nullptr;
+        if (e.kv_pool && f0 >= e.kv_h && f0 < a.n_out) {
+            int c = f0 - e.kv_h;
+            const int which = c >= e.kv_h;
+            c -= which * e.kv_h;
+            const int head = c / e.kv_hd;
+            kv_dst = e.kv_pool + ((size_t)(which * e.kv_nh + head) * e.kv_slots) * e.kv_hd + (c - head * e.kv_hd);
+        }
         const uint32_t cbase = smem_u32(stage_c) + 16u * lane;
         for (int t0 = r0 + warp * kRows; t0 < r1; t0 += kWarps * kRows) {
             float4 acc[kRows];
@@ -270,17 +292,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                 res[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (t < r1) {
-                    if (S == 1) {
+                    if (SC == 1) {
                         acc[u] = *reinterpret_cast<const float4 *>(stage_c + t * BM + 4 * lane);
                     } else {
                         // issue every peer's load before the first add (fixed split order for the sum)
                         const uint32_t local = cbase + (uint32_t)(t * BM * 4);
-                        float4 v[kMaxSplits];
+                        float4 v[kMaxClusterSplits];
 #pragma unroll
-                        for (int s = 0; s < kMaxSplits; ++s)
+                        for (int s = 0; s < kMaxClusterSplits; ++s)
                             if (s < S) v[s] = dsmem_ld4(dsmem_map(local, (uint32_t)s));
 #pragma unroll
-                        for (int s = 0; s < kMaxSplits; ++s)
+                        for (int s = 0; s < kMaxClusterSplits; ++s)
                             if (s < S) acc[u] = add4(acc[u], v[s]);
                     }
                     if (e.resid && full4)
@@ -308,7 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint2 pk;
                         pk.x = *reinterpret_cast<uint32_t *>(&lo);
                         pk.y = *reinterpret_cast<uint32_t *>(&hi);
-                        *reinterpret_cast<uint2 *>(e.out_bf16 + o) = pk;
+                        if (kv_dst)
+                            *reinterpret_cast<uint2 *>(kv_dst + (size_t)e.row_slot[t_base + t] * e.kv_hd) = pk;
+                        else
+                            *reinterpret_cast<uint2 *>(e.out_bf16 + o) = pk;
                     }
                 } else {
 #pragma unroll
@@ -326,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncwarp();
-    if (S > 1)
+    if (a.mode == kCluster)
         cluster_sync_all();  // peers may still be reading this CTA's tile
     else
         __syncthreads();
@@ -385,7 +410,7 @@ int override_stages() {
 
 }  // namespace
 
-TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s) {
+TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool allow_partial, size_t part_cap) {
     TcShape t{};
     t.n_tok_tiles = ceil_div(std::max(m_tok, 1), 256);
     t.bn = std::min(256, std::max(16, ceil_div(ceil_div(std::max(m_tok, 1), t.n_tok_tiles), 16) * 16));
@@ -408,16 +433,24 @@ TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s) {
     int splits = 1;
     if (tiles < capacity) splits = std::max(1, std::min({kMaxSplits, capacity / tiles, num_kb / 4}));
     if (override_splits() > 0) splits = std::min({override_splits(), kMaxSplits, num_kb});
+    if (allow_partial && n_out % 4 == 0) {
+        while (splits > 1 && (size_t)splits * m_tok * n_out > part_cap) --splits;
+    } else {
+        splits = std::min(splits, kMaxClusterSplits);  // clusters beyond a pair schedule poorly
+    }
     t.kb_per_split = ceil_div(num_kb, splits);
     t.splits = ceil_div(num_kb, t.kb_per_split);
     return t;
 }
 
 cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok, int n_out, int k,
-                         const Epilogue &e, const GemmScratch &s, cudaStream_t st) {
+                         const Epilogue &e, const GemmScratch &s, cudaStream_t st, int *n_partials) {
+    if (n_partials) *n_partials = 0;
     if (m_tok <= 0) return cudaSuccess;
     if (k % BK != 0 || k <= 0 || n_out <= 0 || x_rows_cap < m_tok) return cudaErrorInvalidValue;
-    const TcShape t = gemm_tc_shape(m_tok, n_out, k, s);
+    if (e.kv_pool && (e.kv_hd % 4 != 0 || !e.row_slot || !e.out_bf16)) return cudaErrorInvalidValue;
+    const bool allow_partial = e.part != nullptr && !(reinterpret_cast<uintptr_t>(e.part) & 15);
+    const TcShape t = gemm_tc_shape(m_tok, n_out, k, s, allow_partial, e.part_cap);
     if ((size_t)t.stages * (kStageA + t.bn * BK * 2) < (size_t)t.bn * BM * 4) return cudaErrorInvalidValue;
     static bool attr_done = false;
     if (!attr_done) {
@@ -445,7 +478,10 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok
     a.vec_out = (e.ld_out % 4 == 0) &&
                 !(reinterpret_cast<uintptr_t>(e.out_f32 ? (const void *)e.out_f32 : (const void *)e.out_bf16) & align_mask) &&
                 !(reinterpret_cast<uintptr_t>(e.resid) & 15);
+    if (e.kv_pool && !a.vec_out) return cudaErrorInvalidValue;
+    a.mode = t.splits == 1 ? kDirect : (allow_partial ? kPartial : kCluster);
     a.err = s.err;
+    if (a.mode == kPartial && n_partials) *n_partials = t.splits;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(t.n_feat_tiles * t.n_tok_tiles * t.splits);
     cfg.blockDim = dim3(kThreads);
@@ -457,7 +493,7 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = t.splits > 1 ? 1 : 0;
+    cfg.numAttrs = a.mode == kCluster ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, mw, mx, a);
 }
 

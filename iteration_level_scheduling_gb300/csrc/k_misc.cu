@@ -95,13 +95,14 @@ __device__ __forceinline__ void store_vec4<bf16>(bf16 *p, const float *v) {
 // LayerNorm with biased variance, eps 1e-5, statistics in fp32 from registers
 // (two passes over the row held in registers).
 template <typename T>
-__global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const float *x, const int32_t *row_map,
-                                                               const float *g, const float *b, T *y, float *y32,
-                                                               int H) {
+__global__ void __launch_bounds__(kLnThreads) layernorm_kernel(float *x, const int32_t *row_map, const float *g,
+                                                               const float *b, T *y, float *y32, int H,
+                                                               const float *part, int n_part, int part_rows,
+                                                               const float *add_bias) {
     __shared__ float red[33];
     const int r = blockIdx.x;
     const int src = row_map ? row_map[r] : r;
-    const float *xr = x + (size_t)src * H;
+    float *xr = x + (size_t)src * H;
     float v[kLnMaxVec][4];
     float s = 0.f;
 #pragma unroll
@@ -109,6 +110,16 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const float *x, c
         int e = (threadIdx.x + i * kLnThreads) * 4;
         if (e < H) {
             float4 q = *reinterpret_cast<const float4 *>(xr + e);
+            if (n_part > 0) {
+                // complete the residual row: x + bias + the split-K partials, in split order
+                float4 acc = add_bias ? *reinterpret_cast<const float4 *>(add_bias + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int sp = 0; sp < n_part; ++sp) {
+                    const float4 pv = *reinterpret_cast<const float4 *>(part + ((size_t)sp * part_rows + src) * H + e);
+                    acc.x += pv.x, acc.y += pv.y, acc.z += pv.z, acc.w += pv.w;
+                }
+                q.x += acc.x, q.y += acc.y, q.z += acc.z, q.w += acc.w;
+                *reinterpret_cast<float4 *>(xr + e) = q;
+            }
             v[i][0] = q.x, v[i][1] = q.y, v[i][2] = q.z, v[i][3] = q.w;
             s += q.x + q.y + q.z + q.w;
         }
@@ -210,11 +221,12 @@ cudaError_t embed(const int32_t *tokens, const int32_t *row_pos, const int32_t *
 }
 
 template <typename T>
-cudaError_t layernorm(const float *x, const int32_t *row_map, const float *g, const float *b, T *y, float *y32,
-                      int n_rows, int H, cudaStream_t st) {
+cudaError_t layernorm(float *x, const int32_t *row_map, const float *g, const float *b, T *y, float *y32, int n_rows,
+                      int H, cudaStream_t st, const float *part, int n_part, int part_rows, const float *add_bias) {
     if (n_rows <= 0) return cudaSuccess;
     if (H % 4 != 0 || H > kLnThreads * 4 * kLnMaxVec) return cudaErrorInvalidValue;
-    layernorm_kernel<T><<<n_rows, kLnThreads, 0, st>>>(x, row_map, g, b, y, y32, H);
+    layernorm_kernel<T><<<n_rows, kLnThreads, 0, st>>>(x, row_map, g, b, y, y32, H, part, n_part, part_rows,
+                                                       add_bias);
     return cudaGetLastError();
 }
 
@@ -237,10 +249,10 @@ template cudaError_t embed<float>(const int32_t *, const int32_t *, const int32_
                                   const float *, float *, int, int, int, int, unsigned *, cudaStream_t);
 template cudaError_t embed<bf16>(const int32_t *, const int32_t *, const int32_t *, int, const bf16 *, const bf16 *,
                                  float *, int, int, int, int, unsigned *, cudaStream_t);
-template cudaError_t layernorm<float>(const float *, const int32_t *, const float *, const float *, float *, float *,
-                                      int, int, cudaStream_t);
-template cudaError_t layernorm<bf16>(const float *, const int32_t *, const float *, const float *, bf16 *, float *,
-                                     int, int, cudaStream_t);
+template cudaError_t layernorm<float>(float *, const int32_t *, const float *, const float *, float *, float *, int,
+                                      int, cudaStream_t, const float *, int, int, const float *);
+template cudaError_t layernorm<bf16>(float *, const int32_t *, const float *, const float *, bf16 *, float *, int, int,
+                                     cudaStream_t, const float *, int, int, const float *);
 template cudaError_t kv_append<float>(const float *, const int32_t *, float *, int64_t, int, int, int, cudaStream_t);
 template cudaError_t kv_append<bf16>(const bf16 *, const int32_t *, bf16 *, int64_t, int, int, int, cudaStream_t);
 

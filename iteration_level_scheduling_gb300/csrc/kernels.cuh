@@ -19,6 +19,18 @@ struct Epilogue {
     float *out_f32 = nullptr;
     bf16 *out_bf16 = nullptr;
     int ld_out = 0;
+    // Optional split-K partial output: when set and K is split, each split
+    // writes its fp32 partial product (no bias / GeLU / residual) to slab s of
+    // part ([s][m_tok][n_out]) and the caller reduces them.
+    float *part = nullptr;
+    size_t part_cap = 0;  // floats available at part
+    // Optional K/V append (bf16 QKV projection): output features >= kv_h are
+    // k (then v) rows, written to the pool layer at the row's slot instead of
+    // to out_bf16.  Pool layout [K|V][head][slot][kv_hd].
+    bf16 *kv_pool = nullptr;
+    const int32_t *row_slot = nullptr;
+    int64_t kv_slots = 0;
+    int kv_h = 0, kv_hd = 0, kv_nh = 0;
 };
 
 // Launch context of the tensor-core GEMM: the device error word and the SM count.
@@ -29,14 +41,17 @@ struct GemmScratch {
 
 // tcgen05 GEMM, bf16 operands, fp32 accumulation in tensor memory.
 // x: [x_rows_cap, k] row-major (rows >= m_tok are never stored), w: [n_out, k].
+// Returns in *n_partials the number of partial slabs written (0: the full
+// epilogue was applied).
 cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok, int n_out, int k,
-                         const Epilogue &e, const GemmScratch &s, cudaStream_t st);
+                         const Epilogue &e, const GemmScratch &s, cudaStream_t st, int *n_partials = nullptr);
 // Shape the tcgen05 GEMM would use (for scratch sizing and accounting).
 struct TcShape {
     int bn, n_tok_tiles, n_feat_tiles, splits, kb_per_split, stages, tmem_cols;
     size_t smem;
 };
-TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s);
+TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool allow_partial = false,
+                      size_t part_cap = 0);
 
 // SIMT FFMA GEMM, fp32 operands.
 cudaError_t gemm_simt_f32(const float *x, const float *w, int m_tok, int n_out, int k, const Epilogue &e,
@@ -50,9 +65,13 @@ cudaError_t embed(const int32_t *tokens, const int32_t *row_pos, const int32_t *
                   unsigned *err, cudaStream_t st);
 
 // y[r] = LN(x[src(r)]) with src(r) = row_map ? row_map[r] : r; optional fp32 copy.
+// With n_part > 0 the row is first completed from the split-K partials of the
+// preceding projection: x[src] += add_bias + sum_s part[s][src] (written back
+// to x), part slabs having part_rows rows of H floats.
 template <typename T>
-cudaError_t layernorm(const float *x, const int32_t *row_map, const float *g, const float *b, T *y, float *y32,
-                      int n_rows, int H, cudaStream_t st);
+cudaError_t layernorm(float *x, const int32_t *row_map, const float *g, const float *b, T *y, float *y32, int n_rows,
+                      int H, cudaStream_t st, const float *part = nullptr, int n_part = 0, int part_rows = 0,
+                      const float *add_bias = nullptr);
 
 // Copy this iteration's k, v rows (columns H..3H of qkv) into the pool layer.
 template <typename T>
