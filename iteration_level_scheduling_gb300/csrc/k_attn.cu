@@ -19,11 +19,14 @@
 //           span several chunks is merged by the last CTA to finish (per-
 //           (request, head) arrival counter; no CTA ever waits on another).
 // prefill : requests with several input rows (initiation phase, or any
-//           multi-row request).  Work item = (request, 16 query rows) x head;
-//           each warp owns one query row and attends causally over keys
-//           0..pos of its request.
+//           multi-row request).  Work item = (request, 64 query rows) x head.
+//           bf16 with head_dim 64/128: flash-attention tiles on the tensor
+//           cores (below).  Otherwise each warp owns one query row at a time
+//           and attends causally over keys 0..pos of its request.
 // Scores use exp2 with log2(e)/sqrt(head_dim) folded into q; the softmax is
 // the online (running max / running sum) form, exact up to rounding.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -352,6 +355,220 @@ __global__ void __launch_bounds__(kAttnThreads) attn_prefill_kernel(const AttnAr
     }
 }
 
+// ---------------------------------------------------------------------------
+// Prefill on tensor cores (bf16, head_dim 64 or 128): flash-attention tiling.
+// CTA = (request, 64 query rows, head), 4 warps x 16 rows.  K/V tiles of 64
+// keys are double-buffered in shared memory (cp.async, 16-byte chunks stored
+// XOR-swizzled by row so ldmatrix reads are conflict-free); S = Q K^T and
+// O += P V run on mma.sync m16n8k16 with fp32 accumulators; the softmax is the
+// online form, rows held in registers.  Causal: row r of the request sits at
+// position ctx + r and sees keys 0 .. ctx + r.
+// ---------------------------------------------------------------------------
+constexpr int kPreRows = 64;  // query rows per CTA (== kPrefillRowsPerTile)
+constexpr int kPreKeys = 64;  // keys per tile
+
+template <int D>
+struct PrefillSmem {
+    bf16 q[kPreRows * D];
+    bf16 k[2][kPreKeys * D];
+    bf16 v[2][kPreKeys * D];
+};
+
+// byte offset of 16-byte chunk `ch` of row `row` in a swizzled [rows][D] bf16 tile
+template <int D>
+__device__ __forceinline__ uint32_t swz(int row, int ch) {
+    return (uint32_t)(row * D * 2 + ((ch ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float *c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const AttnArgs<bf16> a) {
+    constexpr int CH = D / 8;   // 16-byte chunks per row
+    constexpr int NT = D / 8;   // n-tiles of the output (8 columns each)
+    constexpr int KS = D / 16;  // k-steps of S = Q K^T
+    extern __shared__ __align__(128) uint8_t dyn_smem[];
+    PrefillSmem<D> &sm = *reinterpret_cast<PrefillSmem<D> *>(dyn_smem);
+    const uint32_t sq = smem_u32(sm.q), sk0 = smem_u32(sm.k[0]), sv0 = smem_u32(sm.v[0]);
+    constexpr uint32_t kTileBytes = kPreKeys * D * 2;
+
+    const int tile = blockIdx.x, h = blockIdx.y;
+    const int i = a.p.pre_tiles[2 * tile], q0 = a.p.pre_tiles[2 * tile + 1];
+    const int off = a.p.req_off[i];
+    const int n = a.p.req_off[i + 1] - off;
+    const int ctx = a.p.req_ctx[i];
+    const int rows = min(kPreRows, n - q0);
+    const int n_keys = ctx + q0 + rows;  // keys any row of this tile may see
+    const int n_kt = (n_keys + kPreKeys - 1) / kPreKeys;
+    const bf16 *gk = a.kpool + ((size_t)h * a.kv_slots + a.p.req_kvoff[i]) * D;
+    const bf16 *gv = a.vpool + ((size_t)h * a.kv_slots + a.p.req_kvoff[i]) * D;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // Q tile (rows beyond the request are zero-filled)
+    for (int c = tid; c < kPreRows * CH; c += 128) {
+        const int r = c / CH, ch = c % CH;
+        const bool ok = r < rows;
+        const bf16 *src = a.qkv + (size_t)(off + q0 + (ok ? r : 0)) * 3 * a.H + h * D + ch * 8;
+        cp_async16(sq + swz<D>(r, ch), src, ok);
+    }
+    auto load_kv = [&](int kt, int buf) {
+        for (int c = tid; c < kPreKeys * CH; c += 128) {
+            const int r = c / CH, ch = c % CH;
+            const int t = kt * kPreKeys + r;
+            const bool ok = t < n_keys;
+            const size_t so = (size_t)(ok ? t : 0) * D + ch * 8;
+            cp_async16(sk0 + buf * kTileBytes + swz<D>(r, ch), gk + so, ok);
+            cp_async16(sv0 + buf * kTileBytes + swz<D>(r, ch), gv + so, ok);
+        }
+    };
+    load_kv(0, 0);
+    cp_async_commit();
+
+    const int g = lane >> 2, tg = lane & 3;
+    const int row_lo = warp * 16 + g, row_hi = row_lo + 8;  // this thread's two rows within the tile
+    const int pos_lo = ctx + q0 + row_lo, pos_hi = ctx + q0 + row_hi;
+    uint32_t qa[KS][4];
+    float o[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    float m_lo = kNegBig, m_hi = kNegBig, l_lo = 0.f, l_hi = 0.f;
+
+    for (int kt = 0; kt < n_kt; ++kt) {
+        const int buf = kt & 1;
+        if (kt + 1 < n_kt) {
+            load_kv(kt + 1, buf ^ 1);
+            cp_async_commit();
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        if (kt == 0) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int r = warp * 16 + (lane & 15);
+                const int ch = ks * 2 + (lane >> 4);
+                ldsm_x4(sq + swz<D>(r, ch), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+            }
+        }
+        const uint32_t skb = sk0 + buf * kTileBytes, svb = sv0 + buf * kTileBytes;
+        // S = Q K^T for this warp's 16 rows x 64 keys
+        float sc[kPreKeys / 8][4];
+#pragma unroll
+        for (int j = 0; j < kPreKeys / 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+            for (int jn = 0; jn < kPreKeys / 16; ++jn) {  // two 8-key n-tiles per ldmatrix.x4
+                const int key = jn * 16 + (lane & 7) + ((lane >> 4) << 3);
+                const int ch = ks * 2 + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(skb + swz<D>(key, ch), b0, b1, b2, b3);
+                mma_bf16(sc[2 * jn], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+                mma_bf16(sc[2 * jn + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+            }
+        }
+        // scale, causal mask, online softmax
+        float mx_lo = m_lo, mx_hi = m_hi;
+#pragma unroll
+        for (int j = 0; j < kPreKeys / 8; ++j) {
+            const int key = kt * kPreKeys + j * 8 + 2 * tg;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                sc[j][e] = (key + e <= pos_lo) ? sc[j][e] * a.scale_log2 : kNegBig;
+                sc[j][2 + e] = (key + e <= pos_hi) ? sc[j][2 + e] * a.scale_log2 : kNegBig;
+                mx_lo = fmaxf(mx_lo, sc[j][e]);
+                mx_hi = fmaxf(mx_hi, sc[j][2 + e]);
+            }
+        }
+#pragma unroll
+        for (int sh = 1; sh < 4; sh <<= 1) {
+            mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, sh));
+            mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, sh));
+        }
+        const float c_lo = exp2f(m_lo - mx_lo), c_hi = exp2f(m_hi - mx_hi);
+        m_lo = mx_lo, m_hi = mx_hi;
+        float s_lo = 0.f, s_hi = 0.f;
+#pragma unroll
+        for (int j = 0; j < kPreKeys / 8; ++j) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                sc[j][e] = sc[j][e] > kNegBig ? exp2f(sc[j][e] - mx_lo) : 0.f;
+                sc[j][2 + e] = sc[j][2 + e] > kNegBig ? exp2f(sc[j][2 + e] - mx_hi) : 0.f;
+                s_lo += sc[j][e];
+                s_hi += sc[j][2 + e];
+            }
+        }
+        l_lo = l_lo * c_lo + s_lo;  // per-thread partial sums; reduced across the quad at the end
+        l_hi = l_hi * c_hi + s_hi;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            o[j][0] *= c_lo, o[j][1] *= c_lo;
+            o[j][2] *= c_hi, o[j][3] *= c_hi;
+        }
+        // O += P V
+#pragma unroll
+        for (int kk = 0; kk < kPreKeys / 16; ++kk) {
+            const uint32_t p0 = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
+            const uint32_t p1 = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
+            const uint32_t p2 = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+            const uint32_t p3 = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+#pragma unroll
+            for (int jn = 0; jn < NT / 2; ++jn) {  // two 8-column output tiles per ldmatrix.x4.trans
+                const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                const int ch = jn * 2 + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(svb + swz<D>(key, ch), b0, b1, b2, b3);
+                mma_bf16(o[2 * jn], p0, p1, p2, p3, b0, b1);
+                mma_bf16(o[2 * jn + 1], p0, p1, p2, p3, b2, b3);
+            }
+        }
+        __syncthreads();  // every warp is done with `buf` before it is refilled
+    }
+#pragma unroll
+    for (int sh = 1; sh < 4; sh <<= 1) {
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, sh);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, sh);
+    }
+    const float inv_lo = 1.f / l_lo, inv_hi = 1.f / l_hi;
+    bf16 *out_lo = a.out + (size_t)(off + q0 + row_lo) * a.H + h * D + 2 * tg;
+    bf16 *out_hi = a.out + (size_t)(off + q0 + row_hi) * a.H + h * D + 2 * tg;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        if (row_lo < rows) *reinterpret_cast<uint32_t *>(out_lo + j * 8) = pack_bf16(o[j][0] * inv_lo, o[j][1] * inv_lo);
+        if (row_hi < rows) *reinterpret_cast<uint32_t *>(out_hi + j * 8) = pack_bf16(o[j][2] * inv_hi, o[j][3] * inv_hi);
+    }
+}
+
 template <typename T, int D>
 cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStream_t st) {
     if (decode && a.p.n_dec_work > 0) {
@@ -367,7 +584,19 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
         if (e != cudaSuccess) return e;
     }
     if (prefill && a.p.n_pre_tiles > 0) {
-        attn_prefill_kernel<T, D><<<dim3(a.p.n_pre_tiles, a.n_heads), kAttnThreads, 0, st>>>(a);
+        if constexpr (std::is_same<T, bf16>::value && (D == 64 || D == 128)) {
+            static bool attr = false;
+            if (!attr) {
+                cudaError_t e = cudaFuncSetAttribute(attn_prefill_mma_kernel<D>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     (int)sizeof(PrefillSmem<D>));
+                if (e != cudaSuccess) return e;
+                attr = true;
+            }
+            attn_prefill_mma_kernel<D><<<dim3(a.p.n_pre_tiles, a.n_heads), 128, sizeof(PrefillSmem<D>), st>>>(a);
+        } else {
+            attn_prefill_kernel<T, D><<<dim3(a.p.n_pre_tiles, a.n_heads), kAttnThreads, 0, st>>>(a);
+        }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -95,6 +95,6 @@ cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *ou
 // next[b] = argmax_j logits[b, j] (lowest j on ties); also to out2 if non-null.
 cudaError_t argmax_rows(const float *logits, int n_rows, int V, int32_t *next, int32_t *out2, cudaStream_t st);
 
-constexpr int kPrefillRowsPerTile = 16;
+constexpr int kPrefillRowsPerTile = 64;
 
 }  // namespace orca
