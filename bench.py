@@ -381,20 +381,27 @@ def run_orca(args, rank, world, local_rank):
         t_roof_sum += t_roof
 
     # per-kernel breakdown from the engine's events
+    # Each record is one launch of the sampled layer (layer >= 0) or a per-iteration
+    # kernel (layer == -1); a layer launch stands for n_layers launches of the
+    # iteration, so the per-iteration time of a kind is sum(ms * weight) / steps.
     kinds = {}
     for r in recs:
         k = "gemm_tc (all linear layers)" if r["kind"].startswith("gemm") or r["kind"] == "lm_head" else r["kind"]
-        d = kinds.setdefault(k, dict(ms=0.0, bytes=0.0, flops=0.0, n=0))
-        d["ms"] += r["ms"]
-        d["bytes"] += r["bytes"]
-        d["flops"] += r["flops"]
-        d["n"] += 1
-    tot_ms = sum(d["ms"] for d in kinds.values()) or 1.0
-    breakdown = {k: {"share": d["ms"] / tot_ms, "launches": d["n"], "avg_us": 1000 * d["ms"] / max(d["n"], 1),
+        wgt = cfg.n_layers if r["layer"] >= 0 else 1
+        for key in (k, "lm_head (gemm_tc)") if r["kind"] == "lm_head" else (k,):
+            d = kinds.setdefault(key, dict(ms=0.0, bytes=0.0, flops=0.0, n=0, est=0.0))
+            d["ms"] += r["ms"]
+            d["bytes"] += r["bytes"]
+            d["flops"] += r["flops"]
+            d["n"] += 1
+            d["est"] += r["ms"] * wgt
+    est_tot = sum(d["est"] for k, d in kinds.items() if k != "lm_head (gemm_tc)") or 1.0
+    breakdown = {k: {"share_of_iteration": d["est"] / est_tot, "est_ms_per_iteration": d["est"] / args.steps,
+                     "launches_timed": d["n"], "avg_us": 1000 * d["ms"] / max(d["n"], 1),
                      "GB/s": d["bytes"] / (d["ms"] / 1000) / 1e9 if d["ms"] else None,
                      "TFLOP/s": d["flops"] / (d["ms"] / 1000) / 1e12 if d["ms"] else None}
-                 for k, d in sorted(kinds.items(), key=lambda kv: -kv[1]["ms"])}
-    dom_name, dom = max(kinds.items(), key=lambda kv: kv[1]["ms"])
+                 for k, d in sorted(kinds.items(), key=lambda kv: -kv[1]["est"])}
+    dom_name, dom = max(((k, d) for k, d in kinds.items() if k != "lm_head (gemm_tc)"), key=lambda kv: kv[1]["est"])
     t_hbm = dom["bytes"] / (peaks["hbm"] * 1e9)
     t_tc = dom["flops"] / (peaks["tc_sus"] * 1e12)
     if t_tc > t_hbm:

@@ -91,6 +91,13 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start its
+// independent prologue early, and wait here until every earlier kernel has
+// completed and its writes are visible.  Every kernel calls pdl_wait() before
+// it reads or writes anything another kernel touches.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
 
 // ---------------------------------------------------------------------------

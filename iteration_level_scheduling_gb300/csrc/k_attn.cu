@@ -163,6 +163,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const AttnArgs
     extern __shared__ __align__(128) uint8_t dyn_smem[];
     DecodeSmem<T, D> &sm = *reinterpret_cast<DecodeSmem<T, D> *>(dyn_smem);
 
+    pdl_trigger();
+    pdl_wait();
     const int w_idx = blockIdx.x, h = blockIdx.y;
     const int i = a.p.dec_work[2 * w_idx], c = a.p.dec_work[2 * w_idx + 1];
     const int row = a.p.req_off[i];
@@ -324,6 +326,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_prefill_kernel(const AttnAr
     constexpr int LPT = D / VEC;
     constexpr int TPW = 32 / LPT;
     constexpr int U = 4;
+    pdl_trigger();
+    pdl_wait();
     const int tile = blockIdx.x, h = blockIdx.y;
     const int i = a.p.pre_tiles[2 * tile], r0 = a.p.pre_tiles[2 * tile + 1];  // r0: first row within the request
     const int off = a.p.req_off[i];
@@ -420,6 +424,8 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const AttnArgs<bf
     PrefillSmem<D> &sm = *reinterpret_cast<PrefillSmem<D> *>(dyn_smem);
     const uint32_t sq = smem_u32(sm.q), sk0 = smem_u32(sm.k[0]), sv0 = smem_u32(sm.v[0]);
     constexpr uint32_t kTileBytes = kPreKeys * D * 2;
+    pdl_trigger();
+    pdl_wait();
 
     const int tile = blockIdx.x, h = blockIdx.y;
     const int i = a.p.pre_tiles[2 * tile], q0 = a.p.pre_tiles[2 * tile + 1];
@@ -579,8 +585,8 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        attn_decode_kernel<T, D><<<dim3(a.p.n_dec_work, a.n_heads), kDecThreads, sizeof(DecodeSmem<T, D>), st>>>(a);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(attn_decode_kernel<T, D>, dim3(a.p.n_dec_work, a.n_heads), dim3(kDecThreads),
+                                   sizeof(DecodeSmem<T, D>), st, a);
         if (e != cudaSuccess) return e;
     }
     if (prefill && a.p.n_pre_tiles > 0) {
@@ -593,9 +599,13 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
                 if (e != cudaSuccess) return e;
                 attr = true;
             }
-            attn_prefill_mma_kernel<D><<<dim3(a.p.n_pre_tiles, a.n_heads), 128, sizeof(PrefillSmem<D>), st>>>(a);
+            cudaError_t e = launch_pdl(attn_prefill_mma_kernel<D>, dim3(a.p.n_pre_tiles, a.n_heads), dim3(128),
+                                       sizeof(PrefillSmem<D>), st, a);
+            if (e != cudaSuccess) return e;
         } else {
-            attn_prefill_kernel<T, D><<<dim3(a.p.n_pre_tiles, a.n_heads), kAttnThreads, 0, st>>>(a);
+            cudaError_t e = launch_pdl(attn_prefill_kernel<T, D>, dim3(a.p.n_pre_tiles, a.n_heads),
+                                       dim3(kAttnThreads), 0, st, a);
+            if (e != cudaSuccess) return e;
         }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) gemm_simt_f32_kernel(const float *x, cons
                                                             Epilogue e) {
     __shared__ float xs[TK][TB + 1];
     __shared__ float ws[TK][TB + 1];
+    pdl_trigger();
+    pdl_wait();
     const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
     const int t0 = blockIdx.y * TB, f0 = blockIdx.x * TB;
     float acc[4][4] = {};
@@ -67,8 +69,7 @@ cudaError_t gemm_simt_f32(const float *x, const float *w, int m_tok, int n_out, 
     if (m_tok <= 0) return cudaSuccess;
     if (!e.out_f32) return cudaErrorInvalidValue;
     dim3 grid((n_out + TB - 1) / TB, (m_tok + TB - 1) / TB);
-    gemm_simt_f32_kernel<<<grid, 256, 0, st>>>(x, w, m_tok, n_out, k, e);
-    return cudaGetLastError();
+    return launch_pdl(gemm_simt_f32_kernel, grid, dim3(256), 0, st, x, w, m_tok, n_out, k, e);
 }
 
 }  // namespace orca

@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_base = tt * a.bn;
     const int t_lim = min(a.bn, a.m_tok - t_base);  // valid token columns of this tile
 
+    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(&full[s], 1);
@@ -171,9 +172,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             // with one token tile the weights are read exactly once: stream them past L2
             const bool stream_w = a.n_tok_tiles == 1;
             const uint64_t pol_w = l2_policy_evict_first();
-            int issued = 0;
+            // The weights do not depend on earlier kernels: fill the first stages
+            // with weight slices before waiting for the previous kernel, then
+            // add the activation slices.
+            const int pre = min(nkb, a.stages);
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full[i], (uint32_t)stage_bytes);
+                uint8_t *sa = smem + (size_t)i * stage_bytes;
+                if (stream_w)
+                    tma_load_2d_hint(sa, &tmw, &full[i], (kb0 + i) * BK, ft * BM, pol_w);
+                else
+                    tma_load_2d(sa, &tmw, &full[i], (kb0 + i) * BK, ft * BM);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i)
+                tma_load_2d(smem + (size_t)i * stage_bytes + kStageA, &tmx, &full[i], (kb0 + i) * BK, t_base);
+            int issued = pre;
             bool ok = true;
-            for (int i = 0; i < nkb; ++i) {
+            for (int i = pre; i < nkb; ++i) {
                 const int s = i % a.stages;
                 const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
                 if (!mbar_wait_bounded(&empty[s], ph ^ 1u, a.err)) {
@@ -195,8 +211,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = max(0, issued - a.stages); j < issued; ++j)
                     mbar_wait_bounded(&full[j % a.stages], (uint32_t)(j / a.stages) & 1u, a.err);
             }
+        } else {
+            pdl_wait();
         }
     } else if (warp == 1) {
+        pdl_wait();
         if (lane == 0) {
             bool ok = true;
             for (int i = 0; i < nkb; ++i) {
@@ -224,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // --------- epilogue phase 1: TMEM -> shared memory tile [token][feature] ---------
+        pdl_wait();
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;  // output feature within the tile
         bool ok = mbar_wait_bounded(done, 0, a.err);
@@ -487,13 +507,15 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = t.smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)t.splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)t.splits;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = a.mode == kCluster ? 1 : 0;
+    cfg.numAttrs = a.mode == kCluster ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, mw, mx, a);
 }
 

@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(kRowThreads) embed_kernel(const int32_t *token
                                                             const T *pos_emb, float *x, int H, int V, int max_pos,
                                                             unsigned *err) {
     constexpr int VEC = Elem<T>::kPer16;
+    pdl_trigger();
+    pdl_wait();
     const int r = blockIdx.x;
     int t = tokens[r];
     if (t < 0) {
@@ -100,6 +102,8 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(float *x, const i
                                                                const float *part, int n_part, int part_rows,
                                                                const float *add_bias) {
     __shared__ float red[33];
+    pdl_trigger();
+    pdl_wait();
     const int r = blockIdx.x;
     const int src = row_map ? row_map[r] : r;
     float *xr = x + (size_t)src * H;
@@ -158,6 +162,8 @@ __global__ void __launch_bounds__(kRowThreads) kv_append_kernel(const T *qkv, co
                                                                 T *pool_layer, int64_t kv_slots, int H, int d,
                                                                 int n_heads) {
     constexpr int VEC = Elem<T>::kPer16;
+    pdl_trigger();
+    pdl_wait();
     const int r = blockIdx.x;
     const int64_t slot = row_slot[r];
     const T *src = qkv + (size_t)r * 3 * H + H;  // k then v, 2H contiguous values
@@ -176,6 +182,8 @@ __global__ void __launch_bounds__(kArgmaxThreads) argmax_kernel(const float *log
                                                                 int32_t *out2) {
     __shared__ float sv[kArgmaxThreads / 32];
     __shared__ int si[kArgmaxThreads / 32];
+    pdl_trigger();
+    pdl_wait();
     const float *lr = logits + (size_t)blockIdx.x * V;
     float best = -FLT_MAX;
     int idx = INT_MAX;
@@ -215,9 +223,8 @@ cudaError_t embed(const int32_t *tokens, const int32_t *row_pos, const int32_t *
                   const T *tok_emb, const T *pos_emb, float *x, int n_rows, int H, int V, int max_pos,
                   unsigned *err, cudaStream_t st) {
     if (n_rows <= 0) return cudaSuccess;
-    embed_kernel<T><<<n_rows, kRowThreads, 0, st>>>(tokens, row_pos, prev_next, prev_n, tok_emb, pos_emb, x, H, V,
-                                                    max_pos, err);
-    return cudaGetLastError();
+    return launch_pdl(embed_kernel<T>, dim3(n_rows), dim3(kRowThreads), 0, st, tokens, row_pos, prev_next, prev_n,
+                      tok_emb, pos_emb, x, H, V, max_pos, err);
 }
 
 template <typename T>
@@ -225,24 +232,21 @@ cudaError_t layernorm(float *x, const int32_t *row_map, const float *g, const fl
                       int H, cudaStream_t st, const float *part, int n_part, int part_rows, const float *add_bias) {
     if (n_rows <= 0) return cudaSuccess;
     if (H % 4 != 0 || H > kLnThreads * 4 * kLnMaxVec) return cudaErrorInvalidValue;
-    layernorm_kernel<T><<<n_rows, kLnThreads, 0, st>>>(x, row_map, g, b, y, y32, H, part, n_part, part_rows,
-                                                       add_bias);
-    return cudaGetLastError();
+    return launch_pdl(layernorm_kernel<T>, dim3(n_rows), dim3(kLnThreads), 0, st, x, row_map, g, b, y, y32, H, part,
+                      n_part, part_rows, add_bias);
 }
 
 template <typename T>
 cudaError_t kv_append(const T *qkv, const int32_t *row_slot, T *pool_layer, int64_t kv_slots, int n_rows, int H,
                       int n_heads, cudaStream_t st) {
     if (n_rows <= 0) return cudaSuccess;
-    kv_append_kernel<T><<<n_rows, kRowThreads, 0, st>>>(qkv, row_slot, pool_layer, kv_slots, H, H / n_heads,
-                                                        n_heads);
-    return cudaGetLastError();
+    return launch_pdl(kv_append_kernel<T>, dim3(n_rows), dim3(kRowThreads), 0, st, qkv, row_slot, pool_layer, kv_slots,
+                      H, H / n_heads, n_heads);
 }
 
 cudaError_t argmax_rows(const float *logits, int n_rows, int V, int32_t *next, int32_t *out2, cudaStream_t st) {
     if (n_rows <= 0) return cudaSuccess;
-    argmax_kernel<<<n_rows, kArgmaxThreads, 0, st>>>(logits, V, next, out2);
-    return cudaGetLastError();
+    return launch_pdl(argmax_kernel, dim3(n_rows), dim3(kArgmaxThreads), 0, st, logits, V, next, out2);
 }
 
 template cudaError_t embed<float>(const int32_t *, const int32_t *, const int32_t *, int, const float *,
