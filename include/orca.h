@@ -224,6 +224,23 @@ int orca_op_linear(orca_engine *eng, int32_t dtype, const void *x, const void *w
                    int32_t k, const float *bias, int32_t gelu, const float *resid, float *out_f32, void *out_bf16,
                    int32_t ld_out);
 
+/* Attention of one layer for a batch of requests (the kernels of
+ * orca_run_iteration), on device data.  Layout as inside an iteration:
+ *   qkv      [sum(n_input), 3*hidden] rows of the batch, request by request;
+ *            only the q columns [0, hidden) are read (dtype elements).
+ *   kv_layer one layer of a K/V pool: [K|V][n_heads][kv_slots][head_dim]; the
+ *            rows of this iteration must already be in it.
+ *   out      [sum(n_input), hidden].
+ * n_input, ctx_len, kv_offset: HOST arrays of n_req entries.  Row j of
+ * request i sits at position ctx_len[i] + j and attends to keys 0 ..
+ * ctx_len[i] + j of slots kv_offset[i] ... ([houmin] 3.1.2: attention runs per
+ * request).  Requests with one row take the split-K decode kernel, others the
+ * prefill kernel.  n_req <= max_batch of the engine; asynchronous on the
+ * engine stream, using the engine's scratch.  Errors: INVALID, CUDA. */
+int orca_op_attention(orca_engine *eng, int32_t dtype, const void *qkv, const void *kv_layer, int64_t kv_slots,
+                      int32_t n_heads, int32_t head_dim, int32_t n_req, const int32_t *n_input,
+                      const int32_t *ctx_len, const int64_t *kv_offset, void *out);
+
 /* ------------------------------------------------------------------------ */
 /* iteration-level scheduler ([houmin] 3.1.1, [0h-n0] scheduler algorithm,    */
 /* [arcsin2] 4.2)                                                            */

@@ -703,6 +703,96 @@ int orca_engine_timing_read(orca_engine *E, orca_kernel_time *out, int32_t cap, 
     return ORCA_OK;
 }
 
+int orca_op_attention(orca_engine *E, int32_t dtype, const void *qkv, const void *kv_layer, int64_t kv_slots,
+                      int32_t n_heads, int32_t head_dim, int32_t n_req, const int32_t *n_input,
+                      const int32_t *ctx_len, const int64_t *kv_offset, void *out) {
+    if (!E || !qkv || !kv_layer || !out || !n_input || !ctx_len || !kv_offset) return ORCA_ERR_INVALID;
+    if (n_req < 1 || n_req > E->cfg.max_batch || n_heads < 1 || kv_slots < 1 || kv_slots > INT32_MAX)
+        return ORCA_ERR_INVALID;
+    if (head_dim != 16 && head_dim != 32 && head_dim != 64 && head_dim != 128) return ORCA_ERR_INVALID;
+    if (dtype != ORCA_DTYPE_FP32 && dtype != ORCA_DTYPE_BF16) return ORCA_ERR_INVALID;
+    if (n_heads > E->nh) return ORCA_ERR_INVALID;  // split-K counters are sized for the engine's heads
+    // describe the batch through the iteration's layout rules (ids and tokens are not read)
+    std::vector<int64_t> ids(n_req);
+    std::vector<int32_t> phase(n_req);
+    int64_t rows = 0;
+    for (int i = 0; i < n_req; ++i) {
+        if (n_input[i] < 1 || ctx_len[i] < 0 || kv_offset[i] < 0 ||
+            kv_offset[i] + (int64_t)ctx_len[i] + n_input[i] > kv_slots)
+            return ORCA_ERR_INVALID;
+        ids[i] = i;
+        phase[i] = ctx_len[i] > 0;
+        rows += n_input[i];
+    }
+    std::vector<int32_t> toks((size_t)rows, 0);
+    orca_batch b{n_req, ids.data(), phase.data(), n_input, ctx_len, kv_offset, toks.data()};
+    Layout lay;
+    int rc = layout(E, &b, &lay);
+    if (rc != ORCA_OK) return rc;
+    if (lay.off[P_TOTAL] > E->plan_cap ||
+        (int64_t)lay.n_dec_work * n_heads * (head_dim + 2) > E->attn_part_work * E->nh * (E->d + 2))
+        return ORCA_ERR_INVALID;
+    // the engine's plan buffers are reused: wait for any iteration still reading them
+    if (cudaStreamSynchronize(E->st) != cudaSuccess) {
+        cudaGetLastError();
+        return ORCA_ERR_CUDA;
+    }
+    int32_t *buf = E->h_plan;
+    int32_t *req_off = buf + lay.off[P_REQOFF], *req_ctx = buf + lay.off[P_REQCTX], *req_kv = buf + lay.off[P_REQKV];
+    int32_t *dec_wb = buf + lay.off[P_DECWB], *dec_nch = buf + lay.off[P_DECNCH];
+    int32_t *dec_work = buf + lay.off[P_DECWORK], *pre_tiles = buf + lay.off[P_PRETILES];
+    int r = 0, work = 0, tiles = 0;
+    for (int i = 0; i < n_req; ++i) {
+        req_off[i] = r;
+        req_ctx[i] = ctx_len[i];
+        req_kv[i] = (int32_t)kv_offset[i];
+        if (n_input[i] == 1) {
+            const int nch = ceil_div((int64_t)ctx_len[i] + 1, lay.chunk);
+            dec_wb[i] = work;
+            dec_nch[i] = nch;
+            for (int c = 0; c < nch; ++c, ++work) dec_work[2 * work] = i, dec_work[2 * work + 1] = c;
+        } else {
+            dec_wb[i] = -1;
+            dec_nch[i] = 0;
+            for (int q = 0; q < n_input[i]; q += kPrefillRowsPerTile, ++tiles)
+                pre_tiles[2 * tiles] = i, pre_tiles[2 * tiles + 1] = q;
+        }
+        r += n_input[i];
+    }
+    req_off[n_req] = r;
+    if (cudaMemcpyAsync(E->d_plan, E->h_plan, (size_t)lay.off[P_TOTAL] * 4, cudaMemcpyHostToDevice, E->st) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return ORCA_ERR_CUDA;
+    }
+    const int32_t *dp = E->d_plan;
+    AttnPlan ap;
+    ap.req_off = dp + lay.off[P_REQOFF];
+    ap.req_ctx = dp + lay.off[P_REQCTX];
+    ap.req_kvoff = dp + lay.off[P_REQKV];
+    ap.dec_work = dp + lay.off[P_DECWORK];
+    ap.dec_wbegin = dp + lay.off[P_DECWB];
+    ap.dec_nch = dp + lay.off[P_DECNCH];
+    ap.pre_tiles = dp + lay.off[P_PRETILES];
+    ap.n_dec_work = lay.n_dec_work;
+    ap.n_pre_tiles = lay.n_pre_tiles;
+    ap.chunk = lay.chunk;
+    const int H = n_heads * head_dim;
+    cudaError_t ce;
+    if (dtype == ORCA_DTYPE_BF16)
+        ce = attention<bf16>((const bf16 *)qkv, (const bf16 *)kv_layer, kv_slots, (bf16 *)out, ap, H, n_heads,
+                             E->attn_part, E->attn_cnt, E->d_err, E->st, true, true);
+    else
+        ce = attention<float>((const float *)qkv, (const float *)kv_layer, kv_slots, (float *)out, ap, H, n_heads,
+                              E->attn_part, E->attn_cnt, E->d_err, E->st, true, true);
+    E->launches += (ap.n_dec_work > 0) + (ap.n_pre_tiles > 0);
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        return ORCA_ERR_CUDA;
+    }
+    return ORCA_OK;
+}
+
 int orca_op_linear(orca_engine *E, int32_t dtype, const void *x, const void *w, int32_t m, int32_t n, int32_t k,
                    const float *bias, int32_t gelu, const float *resid, float *out_f32, void *out_bf16,
                    int32_t ld_out) {

@@ -29,7 +29,7 @@ EXPORTS = [
     "orca_strerror", "orca_engine_create", "orca_engine_destroy", "orca_kv_alloc", "orca_kv_free",
     "orca_kv_layout_get", "orca_run_iteration", "orca_plan_words", "orca_plan_build", "orca_run_planned",
     "orca_engine_sync", "orca_get_last_hidden", "orca_get_last_logits", "orca_engine_stats_get",
-    "orca_engine_timing", "orca_engine_timing_read", "orca_op_linear", "orca_sched_create", "orca_sched_destroy",
+    "orca_engine_timing", "orca_engine_timing_read", "orca_op_linear", "orca_op_attention", "orca_sched_create", "orca_sched_destroy",
     "orca_sched_submit", "orca_sched_set_token_feedback", "orca_sched_next", "orca_sched_complete", "orca_sched_stats_get", "orca_sched_request_get",
     "orca_sched_request_tokens", "orca_sched_run",
 ]
@@ -112,6 +112,7 @@ _sig = {
     "orca_engine_timing_read": (C.c_int, [P, C.POINTER(KernelTime), C.c_int32, C.POINTER(C.c_int32)]),
     "orca_op_linear": (C.c_int, [P, C.c_int32, P, P, C.c_int32, C.c_int32, C.c_int32, P, C.c_int32, P, P, P,
                                  C.c_int32]),
+    "orca_op_attention": (C.c_int, [P, C.c_int32, P, P, C.c_int64, C.c_int32, C.c_int32, C.c_int32, P, P, P, P]),
     "orca_sched_create": (C.c_int, [C.POINTER(SchedConfig), P, C.POINTER(P)]),
     "orca_sched_destroy": (C.c_int, [P]),
     "orca_sched_submit": (C.c_int, [P, C.c_int64, C.c_double, P, C.c_int32, C.c_int32, C.c_int32,
@@ -265,6 +266,18 @@ class Engine:
                                  P(out_f32 or None), P(out_bf16 or None), ld_out or n), "orca_op_linear")
         if sync:
             self.sync()
+
+    def op_attention(self, dtype: int, qkv: int, kv_layer: int, kv_slots: int, n_heads: int, head_dim: int,
+                     n_input, ctx_len, kv_offset, out: int, sync: bool = True):
+        n, c, o = _attn_host_arrays(n_input, ctx_len, kv_offset)
+        check(lib.orca_op_attention(self._h, dtype, P(qkv), P(kv_layer), kv_slots, n_heads, head_dim, len(n),
+                                    _ptr(n), _ptr(c), _ptr(o), P(out)), "orca_op_attention")
+        if sync:
+            self.sync()
+
+
+def _attn_host_arrays(n_input, ctx_len, kv_offset):
+    return _i32(n_input), _i32(ctx_len), _i64(kv_offset)
 
 
 class Scheduler:
