@@ -47,6 +47,8 @@ extern "C" {
                                   /* bounded wait); the engine stays usable         */
 #define ORCA_ERR_NOT_FOUND (-5)   /* unknown request id                             */
 #define ORCA_ERR_OOM (-6)         /* host or device allocation failed               */
+#define ORCA_ERR_LIMIT (-7)       /* sizes exceed the fixed scratch of an           */
+                                  /* allocation-free entry point                    */
 
 #define ORCA_DTYPE_FP32 0 /* every tensor fp32; SIMT FFMA kernels              */
 #define ORCA_DTYPE_BF16 1 /* matrices, embeddings, K/V, GEMM operands in bf16; */
@@ -240,6 +242,39 @@ int orca_op_linear(orca_engine *eng, int32_t dtype, const void *x, const void *w
 int orca_op_attention(orca_engine *eng, int32_t dtype, const void *qkv, const void *kv_layer, int64_t kv_slots,
                       int32_t n_heads, int32_t head_dim, int32_t n_req, const int32_t *n_input,
                       const int32_t *ctx_len, const int64_t *kv_offset, void *out);
+
+/* Allocation-free decode attention.  The Orca paper has no counterpart to this
+ * entry point: it exists for callers that cannot allocate device memory at
+ * call time -- for
+ * example code running inside a memory-constrained host process that has
+ * handed all device memory to its own allocator, or a runtime that forbids
+ * cudaMalloc on its serving thread -- and so cannot create an engine.  It runs
+ * the same split-K decode kernel as orca_op_attention for requests that have
+ * exactly one input row each (increment phase), with the kernel's scratch
+ * (plan tables, per-(request, head) arrival counters, split-K partials) in a
+ * fixed device array of about 16.2 MiB inside this library.  Every GPU that loads the
+ * library holds that array until the process exits.
+ *   qkv [n_req, 3*hidden], kv_layer [K|V][n_heads][kv_slots][head_dim],
+ *   out [n_req, hidden]: device pointers, owned by the caller.
+ *   ctx_len, kv_offset: HOST arrays of n_req entries; request i attends to
+ *   slots kv_offset[i] .. kv_offset[i] + ctx_len[i] (ctx_len[i] + 1 keys).
+ *   stream: cudaStream_t (NULL = legacy default stream).
+ * Limits: n_req <= 256, n_heads <= 128, head_dim in {16, 32, 64, 128}, and the
+ * split-K partials (work items x n_heads x (head_dim + 2) floats, a work item
+ * being 64 to 512 keys of one request) within 4 Mi floats; beyond them the call
+ * returns ORCA_ERR_LIMIT and does nothing.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  The first call
+ * on a device looks up the array's device address (once per device, with that
+ * device current), so make it before any stream capture.  The host tables are
+ * copied from pageable memory, which waits for the stream's earlier work.
+ * Every call shares the one array and it keeps the last call's contents (the
+ * counters are cleared at each call): calls that overlap on the GPU -- on
+ * different streams, or from different threads -- race and must not be made.
+ * Device-side wait timeouts are not reported by this entry point.
+ * Errors: INVALID (arguments), LIMIT (sizes), CUDA. */
+int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, const void *kv_layer, int64_t kv_slots,
+                                  int32_t n_heads, int32_t head_dim, int32_t n_req, const int32_t *ctx_len,
+                                  const int64_t *kv_offset, void *out, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* iteration-level scheduler ([houmin] 3.1.1, [0h-n0] scheduler algorithm,    */

@@ -468,6 +468,7 @@ const char *orca_strerror(int code) {
         case ORCA_ERR_DEVICE_FLAG: return "a kernel recorded an error";
         case ORCA_ERR_NOT_FOUND: return "unknown request id";
         case ORCA_ERR_OOM: return "allocation failed";
+        case ORCA_ERR_LIMIT: return "sizes exceed the fixed scratch of the allocation-free entry point";
         default: return "unknown status";
     }
 }

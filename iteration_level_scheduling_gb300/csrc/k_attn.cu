@@ -642,6 +642,134 @@ cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *ou
     }
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free decode attention (orca_attention_decode_noalloc in orca.h).
+// The split-K decode kernel above, with its scratch -- plan tables, arrival
+// counters and partials -- carved out of one file-scope device array instead
+// of engine-allocated buffers.  Host code must not use the array's name as a
+// pointer (that is a host-side stand-in): its device address is looked up
+// once per device with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kNaMaxReq = 256;
+constexpr int kNaMaxHeads = 128;
+constexpr size_t kNaPartFloats = size_t(1) << 22;                    // 16 MiB of partials
+constexpr size_t kNaCounterWords = size_t(kNaMaxReq) * kNaMaxHeads;  // 128 KiB
+constexpr size_t kNaPlanWords = 8 * kNaMaxReq + 2 * 8192;            // tables + up to 8192 work items
+constexpr size_t kNaScratchBytes = 4 * (kNaPartFloats + kNaCounterWords + kNaPlanWords);
+constexpr int kNaMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaScratchBytes];
+
+struct NaDevice {
+    bool ready = false;
+    unsigned char *scratch = nullptr;  // device address of g_noalloc_scratch
+    int num_sms = 0;
+};
+NaDevice g_na_dev[kNaMaxDevices];
+int32_t g_na_plan[kNaPlanWords];  // host staging of the tables (pageable)
+
+}  // namespace
+
+}  // namespace orca
+
+extern "C" int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, const void *kv_layer, int64_t kv_slots,
+                                             int32_t n_heads, int32_t head_dim, int32_t n_req,
+                                             const int32_t *ctx_len, const int64_t *kv_offset, void *out,
+                                             void *stream) {
+    using namespace orca;
+    constexpr int kOk = 0, kInvalid = -1, kCuda = -3, kLimit = -7;  // ORCA_OK / _ERR_INVALID / _CUDA / _LIMIT
+    if (!qkv || !kv_layer || !out || !ctx_len || !kv_offset || n_req < 1 || n_heads < 1 || kv_slots < 1 ||
+        kv_slots > INT32_MAX)
+        return kInvalid;
+    if (dtype != 0 && dtype != 1) return kInvalid;
+    if (head_dim != 16 && head_dim != 32 && head_dim != 64 && head_dim != 128) return kInvalid;
+    for (int i = 0; i < n_req; ++i)
+        if (ctx_len[i] < 0 || kv_offset[i] < 0 || kv_offset[i] + (int64_t)ctx_len[i] + 1 > kv_slots) return kInvalid;
+    if (n_req > kNaMaxReq || n_heads > kNaMaxHeads) return kLimit;
+
+    // once per device, with that device current: the array's device address
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNaMaxDevices) {
+        cudaGetLastError();
+        return kCuda;
+    }
+    NaDevice &nd = g_na_dev[dev];
+    if (!nd.ready) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p ||
+            cudaDeviceGetAttribute(&nd.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return kCuda;
+        }
+        nd.scratch = static_cast<unsigned char *>(p);
+        nd.ready = true;
+    }
+
+    // split-K chunking as in the engine: shrink chunks until there are a few CTAs per SM
+    int chunk = 512;
+    while (chunk > 64) {
+        int64_t items = 0;
+        for (int i = 0; i < n_req; ++i) items += ((int64_t)ctx_len[i] + chunk) / chunk;
+        if (items * n_heads >= 4LL * nd.num_sms) break;
+        chunk /= 2;
+    }
+    int64_t n_work = 0;
+    for (int i = 0; i < n_req; ++i) n_work += ((int64_t)ctx_len[i] + chunk) / chunk;
+    const size_t words = 6 * (size_t)n_req + 1 + 2 * (size_t)n_work;
+    if (words > kNaPlanWords || (size_t)n_work * n_heads * (head_dim + 2) > kNaPartFloats) return kLimit;
+
+    // tables: req_off, req_ctx, req_kvoff, dec_wbegin, dec_nch, dec_work
+    int32_t *req_off = g_na_plan, *req_ctx = req_off + n_req + 1, *req_kv = req_ctx + n_req;
+    int32_t *dec_wb = req_kv + n_req, *dec_nch = dec_wb + n_req, *dec_work = dec_nch + n_req;
+    int w = 0;
+    for (int i = 0; i < n_req; ++i) {
+        const int nch = (int)(((int64_t)ctx_len[i] + chunk) / chunk);
+        req_off[i] = i;
+        req_ctx[i] = ctx_len[i];
+        req_kv[i] = (int32_t)kv_offset[i];
+        dec_wb[i] = w;
+        dec_nch[i] = nch;
+        for (int c = 0; c < nch; ++c, ++w) dec_work[2 * w] = i, dec_work[2 * w + 1] = c;
+    }
+    req_off[n_req] = n_req;
+
+    float *part = reinterpret_cast<float *>(nd.scratch);
+    int32_t *counters = reinterpret_cast<int32_t *>(part + kNaPartFloats);
+    int32_t *plan = counters + kNaCounterWords;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(counters, 0, sizeof(int32_t) * (size_t)n_req * n_heads, st) != cudaSuccess ||
+        cudaMemcpyAsync(plan, g_na_plan, sizeof(int32_t) * words, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+        cudaGetLastError();
+        return kCuda;
+    }
+    AttnPlan ap;
+    ap.req_off = plan;
+    ap.req_ctx = plan + (req_ctx - g_na_plan);
+    ap.req_kvoff = plan + (req_kv - g_na_plan);
+    ap.dec_wbegin = plan + (dec_wb - g_na_plan);
+    ap.dec_nch = plan + (dec_nch - g_na_plan);
+    ap.dec_work = plan + (dec_work - g_na_plan);
+    ap.pre_tiles = nullptr;
+    ap.n_dec_work = (int)n_work;
+    ap.n_pre_tiles = 0;
+    ap.chunk = chunk;
+    const int H = n_heads * head_dim;
+    cudaError_t ce =
+        dtype == 1 ? attention<bf16>((const bf16 *)qkv, (const bf16 *)kv_layer, kv_slots, (bf16 *)out, ap, H, n_heads,
+                                     part, counters, nullptr, st, true, false)
+                   : attention<float>((const float *)qkv, (const float *)kv_layer, kv_slots, (float *)out, ap, H,
+                                      n_heads, part, counters, nullptr, st, true, false);
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        return kCuda;
+    }
+    return kOk;
+}
+
+namespace orca {
+
 template cudaError_t attention<float>(const float *, const float *, int64_t, float *, const AttnPlan &, int, int,
                                       float *, int *, unsigned *, cudaStream_t, bool, bool);
 template cudaError_t attention<bf16>(const bf16 *, const bf16 *, int64_t, bf16 *, const AttnPlan &, int, int,

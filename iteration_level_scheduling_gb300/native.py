@@ -20,7 +20,7 @@ if not os.path.exists(LIB):
     raise RuntimeError(f"liborca.so is not built ({LIB}); run iteration_level_scheduling_gb300.build.build()")
 lib = C.CDLL(LIB)
 
-OK, ERR_INVALID, ERR_KV_FULL, ERR_CUDA, ERR_DEVICE_FLAG, ERR_NOT_FOUND, ERR_OOM = 0, -1, -2, -3, -4, -5, -6
+OK, ERR_INVALID, ERR_KV_FULL, ERR_CUDA, ERR_DEVICE_FLAG, ERR_NOT_FOUND, ERR_OOM, ERR_LIMIT = 0, -1, -2, -3, -4, -5, -6, -7
 DTYPE_FP32, DTYPE_BF16 = 0, 1
 KERNEL_KINDS = ["embed", "layernorm", "gemm_qkv", "kv_append", "attn_decode", "attn_prefill", "gemm_o",
                 "gemm_ffn1", "gemm_ffn2", "lm_head", "argmax", "final_ln"]
@@ -29,7 +29,8 @@ EXPORTS = [
     "orca_strerror", "orca_engine_create", "orca_engine_destroy", "orca_kv_alloc", "orca_kv_free",
     "orca_kv_layout_get", "orca_run_iteration", "orca_plan_words", "orca_plan_build", "orca_run_planned",
     "orca_engine_sync", "orca_get_last_hidden", "orca_get_last_logits", "orca_engine_stats_get",
-    "orca_engine_timing", "orca_engine_timing_read", "orca_op_linear", "orca_op_attention", "orca_sched_create", "orca_sched_destroy",
+    "orca_engine_timing", "orca_engine_timing_read", "orca_op_linear", "orca_op_attention",
+    "orca_attention_decode_noalloc", "orca_sched_create", "orca_sched_destroy",
     "orca_sched_submit", "orca_sched_set_token_feedback", "orca_sched_next", "orca_sched_complete", "orca_sched_stats_get", "orca_sched_request_get",
     "orca_sched_request_tokens", "orca_sched_run",
 ]
@@ -113,6 +114,8 @@ _sig = {
     "orca_op_linear": (C.c_int, [P, C.c_int32, P, P, C.c_int32, C.c_int32, C.c_int32, P, C.c_int32, P, P, P,
                                  C.c_int32]),
     "orca_op_attention": (C.c_int, [P, C.c_int32, P, P, C.c_int64, C.c_int32, C.c_int32, C.c_int32, P, P, P, P]),
+    "orca_attention_decode_noalloc": (C.c_int, [C.c_int32, P, P, C.c_int64, C.c_int32, C.c_int32, C.c_int32, P, P,
+                                                P, P]),
     "orca_sched_create": (C.c_int, [C.POINTER(SchedConfig), P, C.POINTER(P)]),
     "orca_sched_destroy": (C.c_int, [P]),
     "orca_sched_submit": (C.c_int, [P, C.c_int64, C.c_double, P, C.c_int32, C.c_int32, C.c_int32,
@@ -278,6 +281,14 @@ class Engine:
 
 def _attn_host_arrays(n_input, ctx_len, kv_offset):
     return _i32(n_input), _i32(ctx_len), _i64(kv_offset)
+
+
+def attention_decode_noalloc(dtype: int, qkv: int, kv_layer: int, kv_slots: int, n_heads: int, head_dim: int,
+                             ctx_len, kv_offset, out: int, stream: int = 0) -> None:
+    """Decode attention without any device allocation (see orca.h); asynchronous."""
+    c, o = _i32(ctx_len), _i64(kv_offset)
+    check(lib.orca_attention_decode_noalloc(dtype, P(qkv), P(kv_layer), kv_slots, n_heads, head_dim, len(c), _ptr(c),
+                                            _ptr(o), P(out), P(stream or None)), "orca_attention_decode_noalloc")
 
 
 class Scheduler:
