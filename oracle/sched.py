@@ -13,7 +13,7 @@ the free K/V capacity (a reservation per admitted request) and, as in
 Admission stops at the first request that does not fit (the pseudocode's
 ``break``): later requests never overtake an earlier one.
 
-Readings taken where the pages are silent (all listed in the design doc):
+Readings taken where the pages are silent:
 
 * Candidates are ordered by (arrival, request id).  Under FCFS admission with
   ``break`` every running request arrived no later than any waiting one, so
