@@ -67,10 +67,14 @@ typedef struct orca_model_config {
     int32_t max_tokens; /* per-iteration budget on sum(n_input), the flattened rows */
     int32_t max_batch;  /* requests per iteration */
     int64_t kv_slots;   /* K/V pool size in tokens (all layers share the index) */
+    int32_t pack_weights; /* bf16 only: 1 = keep an engine-owned copy of w_qkv, w_o, w_1, w_2 and
+                             of tok_emb (as LM head) repacked tile-contiguous for streaming
+                             (see orca_pack_weight); 0 = read the caller's matrices directly */
 } orca_model_config;
 
-/* Per-layer weights: device pointers, borrowed (not copied) by the engine and
- * read on every iteration, so they must outlive it.  Matrices are row-major
+/* Per-layer weights: device pointers, borrowed by the engine and read on every
+ * iteration, so they must outlive it (with pack_weights the four matrices are
+ * copied at creation and need not).  Matrices are row-major
  * [out, in] in the model dtype; vectors are fp32.
  *   w_qkv [3H, H] (rows 0..H-1 produce q, H..2H-1 k, 2H..3H-1 v; head j is the
  *   j-th group of head_dim rows of each), w_o [H, H], w_1 [F, H], w_2 [H, F]. */
@@ -222,9 +226,18 @@ int orca_engine_timing_read(orca_engine *eng, orca_kernel_time *out, int32_t cap
  * Asynchronous on the engine's stream (uses the engine's split-K scratch, so
  * calls on one engine must not overlap); orca_engine_sync waits and reports
  * device-side errors.  Errors: INVALID (shape / pointer combination), CUDA. */
-int orca_op_linear(orca_engine *eng, int32_t dtype, const void *x, const void *w, int32_t m_tok, int32_t n_out,
-                   int32_t k, const float *bias, int32_t gelu, const float *resid, float *out_f32, void *out_bf16,
-                   int32_t ld_out);
+int orca_op_linear(orca_engine *eng, int32_t dtype, const void *x, const void *w, int32_t w_packed, int32_t m_tok,
+                   int32_t n_out, int32_t k, const float *bias, int32_t gelu, const float *resid, float *out_f32,
+                   void *out_bf16, int32_t ld_out);
+
+/* Repack a bf16 weight w [n_out, k] (k % 64 == 0) for streaming: tiles of 128
+ * rows x 64 columns, tile (ft, kb) stored contiguously at element offset
+ * (ft * k/64 + kb) * 8192 in exactly the 128-byte-swizzled layout the tensor
+ * cores read from shared memory, rows past n_out zero.  `out` (device) must
+ * hold orca_packed_weight_elems(n_out, k) bf16 elements.  Asynchronous on the
+ * engine stream.  A packed weight is passed to orca_op_linear with w_packed = 1. */
+int64_t orca_packed_weight_elems(int32_t n_out, int32_t k);
+int orca_pack_weight(orca_engine *eng, const void *w, int32_t n_out, int32_t k, void *out);
 
 /* Attention of one layer for a batch of requests (the kernels of
  * orca_run_iteration), on device data.  Layout as inside an iteration:

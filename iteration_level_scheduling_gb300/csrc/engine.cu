@@ -82,6 +82,9 @@ struct orca_engine {
     const void *tok_emb = nullptr, *pos_emb = nullptr;
     const float *lnf_g = nullptr, *lnf_b = nullptr;
     std::vector<orca_layer_weights> layers;
+    bool packed = false;  // layers[].w_* and lm_head point into `packed_buf`
+    void *packed_buf = nullptr;
+    const void *lm_head = nullptr;
 
     orca::KVPool pool{0};
     void *kv = nullptr;
@@ -111,7 +114,8 @@ struct orca_engine {
 
     ~orca_engine() {
         for (cudaEvent_t e : events) cudaEventDestroy(e);
-        void *dev[] = {kv, x, y32, logits, h, qkv, attn, f, y, next, d_plan, part, attn_part, attn_cnt, d_err};
+        void *dev[] = {kv, x, y32, logits, h, qkv, attn, f, y, next, d_plan, part, attn_part, attn_cnt, d_err,
+                       packed_buf};
         for (void *p : dev)
             if (p) cudaFree(p);
         if (h_plan) cudaFreeHost(h_plan);
@@ -290,7 +294,8 @@ cudaError_t linear(orca_engine *E, const void *x, int x_cap, const void *w, int 
                    int *n_partials = nullptr) {
     if (n_partials) *n_partials = 0;
     if constexpr (std::is_same<T, bf16>::value)
-        return gemm_tc_bf16((const bf16 *)x, x_cap, (const bf16 *)w, m, n, k, e, E->gs, E->st, n_partials);
+        return gemm_tc_bf16((const bf16 *)x, x_cap, (const bf16 *)w, E->packed, m, n, k, e, E->gs, E->st,
+                            n_partials);
     else
         return gemm_simt_f32((const float *)x, (const float *)w, m, n, k, e, E->st);
 }
@@ -420,7 +425,7 @@ int run_plan(orca_engine *E, const int32_t *hp, const int32_t *dp, int32_t *dev_
         e.out_f32 = E->logits;
         e.ld_out = V;
         ORCA_TRY(E->launch(ORCA_K_LM_HEAD, -1, es * ((double)V * H + (double)B * H) + 4.0 * B * V,
-                           2.0 * B * V * H, [&] { return linear<T>(E, y, E->cfg.max_batch, E->tok_emb, B, V, H, e); }));
+                           2.0 * B * V * H, [&] { return linear<T>(E, y, E->cfg.max_batch, E->lm_head, B, V, H, e); }));
     }
     ORCA_TRY(E->launch(ORCA_K_ARGMAX, -1, 4.0 * B * V, 0,
                        [&] { return argmax_rows(E->logits, B, V, E->next, dev_out, st); }));
@@ -507,6 +512,7 @@ int orca_engine_create(const orca_model_config *cfg, const orca_weights *w, void
         E->has_weights = true;
         E->tok_emb = w->tok_emb, E->pos_emb = w->pos_emb, E->lnf_g = w->lnf_g, E->lnf_b = w->lnf_b;
         E->layers.assign(w->layers, w->layers + c.n_layers);
+        E->lm_head = w->tok_emb;
     }
     const size_t R = c.max_tokens, B = c.max_batch, H = c.hidden, F = c.ffn, es = E->es;
     // decode split-K work items: at most one per 64 keys of every request
@@ -543,12 +549,53 @@ int orca_engine_create(const orca_model_config *cfg, const orca_weights *w, void
             cudaMemset(E->next, 0, B * 4) != cudaSuccess)
             rc = ORCA_ERR_CUDA;
     }
+    if (rc == ORCA_OK && E->has_weights && E->bf && c.pack_weights) {
+        // one engine-owned buffer with every matrix repacked tile-contiguous
+        const int Hh = c.hidden, Ff = c.ffn;
+        const size_t per_layer = packed_weight_elems(3 * Hh, Hh) + packed_weight_elems(Hh, Hh) +
+                                 packed_weight_elems(Ff, Hh) + packed_weight_elems(Hh, Ff);
+        const size_t total = per_layer * c.n_layers + packed_weight_elems(c.vocab, Hh);
+        rc = dev_alloc(&E->packed_buf, total * 2);
+        bf16 *p = (bf16 *)E->packed_buf;
+        auto pack = [&](const void *src, int n, int k) -> const void * {
+            if (rc != ORCA_OK) return src;
+            if (pack_weight_bf16((const bf16 *)src, n, k, p, E->st) != cudaSuccess) rc = ORCA_ERR_CUDA;
+            const void *dst = p;
+            p += packed_weight_elems(n, k);
+            return dst;
+        };
+        for (int l = 0; l < c.n_layers && rc == ORCA_OK; ++l) {
+            orca_layer_weights &L = E->layers[l];
+            L.w_qkv = pack(L.w_qkv, 3 * Hh, Hh);
+            L.w_o = pack(L.w_o, Hh, Hh);
+            L.w_1 = pack(L.w_1, Ff, Hh);
+            L.w_2 = pack(L.w_2, Hh, Ff);
+        }
+        E->lm_head = pack(E->tok_emb, c.vocab, Hh);
+        if (rc == ORCA_OK && cudaStreamSynchronize(E->st) != cudaSuccess) rc = ORCA_ERR_CUDA;
+        E->packed = rc == ORCA_OK;
+    }
     if (rc != ORCA_OK) {
         cudaGetLastError();
         delete E;
         return rc;
     }
     *out = E;
+    return ORCA_OK;
+}
+
+int64_t orca_packed_weight_elems(int32_t n_out, int32_t k) {
+    if (n_out < 1 || k < 64 || k % 64) return ORCA_ERR_INVALID;
+    return (int64_t)packed_weight_elems(n_out, k);
+}
+
+int orca_pack_weight(orca_engine *E, const void *w, int32_t n_out, int32_t k, void *out) {
+    if (!E || !w || !out || n_out < 1 || k < 64 || k % 64) return ORCA_ERR_INVALID;
+    if (pack_weight_bf16((const bf16 *)w, n_out, k, (bf16 *)out, E->st) != cudaSuccess) {
+        cudaGetLastError();
+        return ORCA_ERR_CUDA;
+    }
+    E->launches++;
     return ORCA_OK;
 }
 
@@ -794,9 +841,9 @@ int orca_op_attention(orca_engine *E, int32_t dtype, const void *qkv, const void
     return ORCA_OK;
 }
 
-int orca_op_linear(orca_engine *E, int32_t dtype, const void *x, const void *w, int32_t m, int32_t n, int32_t k,
-                   const float *bias, int32_t gelu, const float *resid, float *out_f32, void *out_bf16,
-                   int32_t ld_out) {
+int orca_op_linear(orca_engine *E, int32_t dtype, const void *x, const void *w, int32_t w_packed, int32_t m,
+                   int32_t n, int32_t k, const float *bias, int32_t gelu, const float *resid, float *out_f32,
+                   void *out_bf16, int32_t ld_out) {
     if (!E || !x || !w || m < 0 || n < 1 || k < 1 || ld_out < n) return ORCA_ERR_INVALID;
     if ((out_f32 != nullptr) == (out_bf16 != nullptr) || (resid && !out_f32)) return ORCA_ERR_INVALID;
     Epilogue e;
@@ -809,9 +856,9 @@ int orca_op_linear(orca_engine *E, int32_t dtype, const void *x, const void *w, 
     cudaError_t ce;
     if (dtype == ORCA_DTYPE_BF16) {
         if (k % 64) return ORCA_ERR_INVALID;
-        ce = gemm_tc_bf16((const bf16 *)x, m, (const bf16 *)w, m, n, k, e, E->gs, E->st);
+        ce = gemm_tc_bf16((const bf16 *)x, m, (const bf16 *)w, w_packed != 0, m, n, k, e, E->gs, E->st);
     } else if (dtype == ORCA_DTYPE_FP32) {
-        if (out_bf16) return ORCA_ERR_INVALID;
+        if (out_bf16 || w_packed) return ORCA_ERR_INVALID;
         ce = gemm_simt_f32((const float *)x, (const float *)w, m, n, k, e, E->st);
     } else {
         return ORCA_ERR_INVALID;

@@ -20,13 +20,15 @@
 // mbarriers decouples loads from MMAs; tcgen05.commit releases a stage when the
 // MMAs reading it are done.
 //
-// Small sum L (decode) gives few output tiles, so K is split across the CTAs
-// of a thread-block cluster (split-K, up to 8 ways).  Each CTA stages its fp32
-// accumulator tile in its own shared memory; after a cluster barrier every CTA
-// reduces a slice of the tile's token rows by reading all partial tiles over
-// distributed shared memory, in split order (deterministic), and runs the
-// epilogue for that slice.  No global workspace, no atomics, no CTA waits on a
-// flag written by another.
+// Small sum L (decode) gives few output tiles.  When the caller can complete
+// a split-K sum itself (the residual projections: the next LayerNorm reads the
+// row anyway), K is split over up to 8 CTAs per tile, each writing its fp32
+// partial tile to a slab; no CTA waits on another.  Otherwise one CTA per tile
+// with a deep stage ring, one CTA per SM when the tiles fit in one wave.
+//
+// Weights can be pre-packed (pack_weight_bf16) so each 128 x 64 stage tile is
+// one contiguous, already swizzled 16 KiB block read by a single bulk copy:
+// sequential DRAM streaming instead of 128 rows of 128 bytes each.
 //
 // Epilogue: + bias, exact GeLU, + residual (fp32), store fp32 or bf16 rows
 // [token, feature] with 16-byte (fp32) or 8-byte (bf16) stores along the
@@ -51,8 +53,7 @@ constexpr int BK = 64;
 constexpr int kThreads = 192;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxStages = 8;
-constexpr int kMaxSplits = 8;         // split-K ways (partial slabs); also the DSMEM unroll bound
-constexpr int kMaxClusterSplits = 2;  // split-K ways reduced inside a cluster
+constexpr int kMaxSplits = 8;  // split-K ways (partial slabs)
 constexpr int kStageA = BM * BK * 2;  // 16 KiB
 constexpr int kGroup = 16;            // feature tiles per raster group
 constexpr int kRows = 4;              // epilogue rows per warp in flight
@@ -67,10 +68,11 @@ struct TcArgs {
     uint32_t idesc, tmem_cols;
     Epilogue e;
     int vec_out;  // output / residual rows allow 16-byte (fp32) or 8-byte (bf16) vector access
-    int mode;     // kDirect, kCluster (split-K reduced over DSMEM) or kPartial (split-K slabs to e.part)
+    int mode;     // kDirect, or kPartial (split-K slabs to e.part)
+    const bf16 *w_packed;  // weights in the tile-contiguous layout of pack_weight_bf16, or null (tensor map)
     unsigned *err;
 };
-enum { kDirect = 0, kCluster = 1, kPartial = 2 };
+enum { kDirect = 0, kPartial = 2 };
 
 __device__ __forceinline__ void tile_coords(int lin, const TcArgs &a, int &ft, int &tt) {
     const int per_group = kGroup * a.n_tok_tiles;
@@ -96,31 +98,6 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
     return r != 0;
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// Hardware barrier over every thread of every CTA of the cluster (all CTAs of
-// a cluster are co-resident by construction, so it cannot wait on a CTA that
-// is not running).
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t dsmem_map(uint32_t saddr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ float4 dsmem_ld4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
 __device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -138,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = a.splits;
-    const int split = a.mode == kCluster ? (int)cluster_rank() : (int)(blockIdx.x % S);
+    const int split = (int)(blockIdx.x % S);
     int ft, tt;
     tile_coords(blockIdx.x / S, a, ft, tt);
     const int kb0 = split * a.kb_per_split;
@@ -175,14 +152,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The weights do not depend on earlier kernels: fill the first stages
             // with weight slices before waiting for the previous kernel, then
             // add the activation slices.
+            // packed weights: tile (ft, kb) is one contiguous 16 KiB block, already in
+            // the swizzled shared-memory image, so one bulk copy moves it
+            const bf16 *wp = a.w_packed ? a.w_packed + (size_t)ft * a.num_kb * (BM * BK) : nullptr;
+            auto load_w = [&](int i, int s) {
+                uint8_t *sa = smem + (size_t)s * stage_bytes;
+                if (wp)
+                    bulk_load(sa, wp + (size_t)(kb0 + i) * (BM * BK), kStageA, &full[s], pol_w);
+                else if (stream_w)
+                    tma_load_2d_hint(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM, pol_w);
+                else
+                    tma_load_2d(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM);
+            };
             const int pre = min(nkb, a.stages);
             for (int i = 0; i < pre; ++i) {
                 mbar_arrive_expect_tx(&full[i], (uint32_t)stage_bytes);
-                uint8_t *sa = smem + (size_t)i * stage_bytes;
-                if (stream_w)
-                    tma_load_2d_hint(sa, &tmw, &full[i], (kb0 + i) * BK, ft * BM, pol_w);
-                else
-                    tma_load_2d(sa, &tmw, &full[i], (kb0 + i) * BK, ft * BM);
+                load_w(i, i);
             }
             pdl_wait();
             for (int i = 0; i < pre; ++i)
@@ -197,12 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
-                uint8_t *sa = smem + (size_t)s * stage_bytes;
-                if (stream_w)
-                    tma_load_2d_hint(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM, pol_w);
-                else
-                    tma_load_2d(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM);
-                tma_load_2d(sa + kStageA, &tmx, &full[s], (kb0 + i) * BK, t_base);
+                load_w(i, s);
+                tma_load_2d(smem + (size_t)s * stage_bytes + kStageA, &tmx, &full[s], (kb0 + i) * BK, t_base);
                 ++issued;
             }
             if (!ok) {
@@ -264,10 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncwarp();
-    if (a.mode == kCluster)
-        cluster_sync_all();
-    else
-        __syncthreads();
+    __syncthreads();
 
     // --------- epilogue phase 2: reduce the split partials, bias / GeLU / residual, store ---------
     if (flags[0] == 0 && a.mode == kPartial) {
@@ -290,9 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (f0 + 2 < a.n_out) bias.z = e.bias[f0 + 2];
             if (f0 + 3 < a.n_out) bias.w = e.bias[f0 + 3];
         }
-        const int SC = a.mode == kCluster ? S : 1;  // CTAs sharing this tile's epilogue
-        const int rs = (t_lim + SC - 1) / SC;
-        const int r0 = (SC > 1 ? split : 0) * rs, r1 = min(t_lim, r0 + rs);
+        const int r0 = 0, r1 = t_lim;
         // K/V append: output features >= kv_h go to the pool at the row's slot
         bf16 *kv_dst = nullptr;
         if (e.kv_pool && f0 >= e.kv_h && f0 < a.n_out) {
@@ -302,7 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int head = c / e.kv_hd;
             kv_dst = e.kv_pool + ((size_t)(which * e.kv_nh + head) * e.kv_slots) * e.kv_hd + (c - head * e.kv_hd);
         }
-        const uint32_t cbase = smem_u32(stage_c) + 16u * lane;
         for (int t0 = r0 + warp * kRows; t0 < r1; t0 += kWarps * kRows) {
             float4 acc[kRows];
             float4 res[kRows];
@@ -312,19 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                 res[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (t < r1) {
-                    if (SC == 1) {
-                        acc[u] = *reinterpret_cast<const float4 *>(stage_c + t * BM + 4 * lane);
-                    } else {
-                        // issue every peer's load before the first add (fixed split order for the sum)
-                        const uint32_t local = cbase + (uint32_t)(t * BM * 4);
-                        float4 v[kMaxClusterSplits];
-#pragma unroll
-                        for (int s = 0; s < kMaxClusterSplits; ++s)
-                            if (s < S) v[s] = dsmem_ld4(dsmem_map(local, (uint32_t)s));
-#pragma unroll
-                        for (int s = 0; s < kMaxClusterSplits; ++s)
-                            if (s < S) acc[u] = add4(acc[u], v[s]);
-                    }
+                    acc[u] = *reinterpret_cast<const float4 *>(stage_c + t * BM + 4 * lane);
                     if (e.resid && full4)
                         res[u] = *reinterpret_cast<const float4 *>(e.resid + (size_t)(t_base + t) * e.ld_out + f0);
                 }
@@ -371,14 +334,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncwarp();
-    if (a.mode == kCluster)
-        cluster_sync_all();  // peers may still be reading this CTA's tile
-    else
-        __syncthreads();
+    __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, a.tmem_cols);
+    }
+}
+
+// Pack w [n_out, k] into tiles of 128 rows x 64 columns, tile (ft, kb) at
+// element offset (ft * (k / 64) + kb) * 8192, each tile laid out exactly as
+// the 128-byte-swizzled K-major shared-memory image (row r at r * 128 bytes,
+// 16-byte chunk c at position c ^ (r % 8)); rows past n_out are zero.
+__global__ void __launch_bounds__(256) pack_weight_kernel(const bf16 *w, int n_out, int k, bf16 *out) {
+    pdl_trigger();
+    pdl_wait();
+    const int num_kb = k / BK;
+    const int ft = blockIdx.x / num_kb, kb = blockIdx.x % num_kb;
+    uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)blockIdx.x * (BM * BK));
+    for (int idx = threadIdx.x; idx < BM * 8; idx += 256) {
+        const int r = idx >> 3, c = idx & 7;
+        const int row = ft * BM + r;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < n_out) v = *reinterpret_cast<const uint4 *>(w + (size_t)row * k + kb * BK + c * 8);
+        dst[r * 8 + (c ^ (r & 7))] = v;
     }
 }
 
@@ -437,33 +416,33 @@ TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool al
     t.n_feat_tiles = ceil_div(n_out, BM);
     t.tmem_cols = 32;
     while ((int)t.tmem_cols < t.bn) t.tmem_cols *= 2;
+    const int num_kb = k / BK;
+    const int tiles = t.n_tok_tiles * t.n_feat_tiles;
+    // split-K only into partial slabs the caller completes, and only up to one CTA per SM
+    int splits = 1;
+    if (allow_partial && n_out % 4 == 0 && 2 * tiles <= s.num_sms) {
+        splits = std::max(1, std::min({kMaxSplits, s.num_sms / tiles, num_kb / 4}));
+        if (override_splits() > 0) splits = std::min({override_splits(), kMaxSplits, num_kb});
+        while (splits > 1 && (size_t)splits * m_tok * n_out > part_cap) --splits;
+    }
+    t.kb_per_split = ceil_div(num_kb, splits);
+    t.splits = ceil_div(num_kb, t.kb_per_split);
+    // one CTA per SM with a deep ring when everything runs in one wave, else two
     const int stage_bytes = kStageA + t.bn * BK * 2;
     const size_t max_stages_1cta = (kSmemMaxCta - kSmemExtra) / stage_bytes;
-    int ctas_per_sm = t.bn <= 128 ? 2 : 1;
+    const int ctas_per_sm = (tiles * t.splits > s.num_sms && t.bn <= 128) ? 2 : 1;
     const size_t budget = std::min(kSmemMaxCta, kSmemPerSm / ctas_per_sm - kSmemReserve) - kSmemExtra;
     t.stages = std::min<int>(kMaxStages, (int)(budget / stage_bytes));
     if (override_stages() > 0) t.stages = std::min<int>(std::min(override_stages(), kMaxStages), (int)max_stages_1cta);
     // the ring must also hold the staged fp32 accumulator tile (bn x 512 B) after the mainloop
     while ((size_t)t.stages * stage_bytes < (size_t)t.bn * BM * 4 && t.stages < (int)max_stages_1cta) ++t.stages;
-    if ((size_t)t.stages * stage_bytes + kSmemExtra > kSmemPerSm / 2 - kSmemReserve) ctas_per_sm = 1;
     t.smem = (size_t)t.stages * stage_bytes + kSmemExtra;
-    const int num_kb = k / BK;
-    const int tiles = t.n_tok_tiles * t.n_feat_tiles;
-    const int capacity = s.num_sms * ctas_per_sm;
-    int splits = 1;
-    if (tiles < capacity) splits = std::max(1, std::min({kMaxSplits, capacity / tiles, num_kb / 4}));
-    if (override_splits() > 0) splits = std::min({override_splits(), kMaxSplits, num_kb});
-    if (allow_partial && n_out % 4 == 0) {
-        while (splits > 1 && (size_t)splits * m_tok * n_out > part_cap) --splits;
-    } else {
-        splits = std::min(splits, kMaxClusterSplits);  // clusters beyond a pair schedule poorly
-    }
-    t.kb_per_split = ceil_div(num_kb, splits);
-    t.splits = ceil_div(num_kb, t.kb_per_split);
     return t;
 }
 
-cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok, int n_out, int k,
+size_t packed_weight_elems(int n_out, int k) { return (size_t)ceil_div(n_out, BM) * BM * (size_t)k; }
+
+cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_packed, int m_tok, int n_out, int k,
                          const Epilogue &e, const GemmScratch &s, cudaStream_t st, int *n_partials) {
     if (n_partials) *n_partials = 0;
     if (m_tok <= 0) return cudaSuccess;
@@ -480,7 +459,9 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok
         attr_done = true;
     }
     CUtensorMap mw, mx;
-    if (!make_map(&mw, w, n_out, k, BM) || !make_map(&mx, x, x_rows_cap, k, t.bn)) return cudaErrorInvalidValue;
+    if (w_packed && (reinterpret_cast<uintptr_t>(w) & 15)) return cudaErrorInvalidValue;
+    if (!make_map(&mw, w, w_packed ? BM : n_out, k, BM) || !make_map(&mx, x, x_rows_cap, k, t.bn))
+        return cudaErrorInvalidValue;  // (the weight map is unused when the weights are packed)
     TcArgs a;
     a.m_tok = m_tok;
     a.n_out = n_out;
@@ -499,7 +480,8 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok
                 !(reinterpret_cast<uintptr_t>(e.out_f32 ? (const void *)e.out_f32 : (const void *)e.out_bf16) & align_mask) &&
                 !(reinterpret_cast<uintptr_t>(e.resid) & 15);
     if (e.kv_pool && !a.vec_out) return cudaErrorInvalidValue;
-    a.mode = t.splits == 1 ? kDirect : (allow_partial ? kPartial : kCluster);
+    a.mode = t.splits == 1 ? kDirect : kPartial;
+    a.w_packed = w_packed ? w : nullptr;
     a.err = s.err;
     if (a.mode == kPartial && n_partials) *n_partials = t.splits;
     cudaLaunchConfig_t cfg = {};
@@ -507,16 +489,17 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = t.smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = (unsigned)t.splits;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = a.mode == kCluster ? 2 : 1;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, mw, mx, a);
+}
+
+cudaError_t pack_weight_bf16(const bf16 *w, int n_out, int k, bf16 *out, cudaStream_t st) {
+    if (k % BK != 0 || k <= 0 || n_out <= 0) return cudaErrorInvalidValue;
+    return launch_pdl(pack_weight_kernel, dim3(ceil_div(n_out, BM) * (k / BK)), dim3(256), 0, st, w, n_out, k, out);
 }
 
 }  // namespace orca

@@ -45,8 +45,12 @@ struct GemmScratch {
 // x: [x_rows_cap, k] row-major (rows >= m_tok are never stored), w: [n_out, k].
 // Returns in *n_partials the number of partial slabs written (0: the full
 // epilogue was applied).
-cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, int m_tok, int n_out, int k,
+// w_packed: w is in the layout written by pack_weight_bf16.
+cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_packed, int m_tok, int n_out, int k,
                          const Epilogue &e, const GemmScratch &s, cudaStream_t st, int *n_partials = nullptr);
+// Tile-contiguous, pre-swizzled copy of a [n_out, k] bf16 weight (k % 64 == 0).
+size_t packed_weight_elems(int n_out, int k);
+cudaError_t pack_weight_bf16(const bf16 *w, int n_out, int k, bf16 *out, cudaStream_t st);
 // Shape the tcgen05 GEMM would use (for scratch sizing and accounting).
 struct TcShape {
     int bn, n_tok_tiles, n_feat_tiles, splits, kb_per_split, stages, tmem_cols;

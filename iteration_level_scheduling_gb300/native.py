@@ -29,7 +29,8 @@ EXPORTS = [
     "orca_strerror", "orca_engine_create", "orca_engine_destroy", "orca_kv_alloc", "orca_kv_free",
     "orca_kv_layout_get", "orca_run_iteration", "orca_plan_words", "orca_plan_build", "orca_run_planned",
     "orca_engine_sync", "orca_get_last_hidden", "orca_get_last_logits", "orca_engine_stats_get",
-    "orca_engine_timing", "orca_engine_timing_read", "orca_op_linear", "orca_op_attention",
+    "orca_engine_timing", "orca_engine_timing_read", "orca_op_linear", "orca_op_attention", "orca_packed_weight_elems",
+    "orca_pack_weight",
     "orca_attention_decode_noalloc", "orca_sched_create", "orca_sched_destroy",
     "orca_sched_submit", "orca_sched_set_token_feedback", "orca_sched_next", "orca_sched_complete", "orca_sched_stats_get", "orca_sched_request_get",
     "orca_sched_request_tokens", "orca_sched_run",
@@ -45,7 +46,7 @@ class OrcaError(RuntimeError):
 class ModelConfig(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("hidden", C.c_int32), ("n_heads", C.c_int32), ("ffn", C.c_int32),
                 ("vocab", C.c_int32), ("max_pos", C.c_int32), ("dtype", C.c_int32), ("max_tokens", C.c_int32),
-                ("max_batch", C.c_int32), ("kv_slots", C.c_int64)]
+                ("max_batch", C.c_int32), ("kv_slots", C.c_int64), ("pack_weights", C.c_int32)]
 
 
 class LayerWeights(C.Structure):
@@ -111,8 +112,10 @@ _sig = {
     "orca_engine_stats_get": (C.c_int, [P, C.POINTER(EngineStats)]),
     "orca_engine_timing": (C.c_int, [P, C.c_int32]),
     "orca_engine_timing_read": (C.c_int, [P, C.POINTER(KernelTime), C.c_int32, C.POINTER(C.c_int32)]),
-    "orca_op_linear": (C.c_int, [P, C.c_int32, P, P, C.c_int32, C.c_int32, C.c_int32, P, C.c_int32, P, P, P,
-                                 C.c_int32]),
+    "orca_op_linear": (C.c_int, [P, C.c_int32, P, P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, P, C.c_int32, P, P,
+                                 P, C.c_int32]),
+    "orca_packed_weight_elems": (C.c_int64, [C.c_int32, C.c_int32]),
+    "orca_pack_weight": (C.c_int, [P, P, C.c_int32, C.c_int32, P]),
     "orca_op_attention": (C.c_int, [P, C.c_int32, P, P, C.c_int64, C.c_int32, C.c_int32, C.c_int32, P, P, P, P]),
     "orca_attention_decode_noalloc": (C.c_int, [C.c_int32, P, P, C.c_int64, C.c_int32, C.c_int32, C.c_int32, P, P,
                                                 P, P]),
@@ -182,8 +185,9 @@ class Engine:
     as ``orca_weights``; the engine borrows them (keep the tensors alive)."""
 
     def __init__(self, n_layers, hidden, n_heads, ffn, vocab, max_pos, dtype, max_tokens, max_batch, kv_slots,
-                 weights: Optional[dict] = None, stream: int = 0):
-        self.cfg = ModelConfig(n_layers, hidden, n_heads, ffn, vocab, max_pos, dtype, max_tokens, max_batch, kv_slots)
+                 weights: Optional[dict] = None, stream: int = 0, pack_weights: bool = True):
+        self.cfg = ModelConfig(n_layers, hidden, n_heads, ffn, vocab, max_pos, dtype, max_tokens, max_batch, kv_slots,
+                               int(pack_weights))
         self._h = P()
         wp = None
         if weights is not None:
@@ -264,11 +268,20 @@ class Engine:
                      flops=buf[i].flops) for i in range(n.value)]
 
     def op_linear(self, dtype: int, x: int, w: int, m: int, n: int, k: int, bias: int = 0, gelu: bool = False,
-                  resid: int = 0, out_f32: int = 0, out_bf16: int = 0, ld_out: int = 0, sync: bool = True):
-        check(lib.orca_op_linear(self._h, dtype, P(x), P(w), m, n, k, P(bias or None), int(gelu), P(resid or None),
-                                 P(out_f32 or None), P(out_bf16 or None), ld_out or n), "orca_op_linear")
+                  resid: int = 0, out_f32: int = 0, out_bf16: int = 0, ld_out: int = 0, sync: bool = True,
+                  w_packed: bool = False):
+        check(lib.orca_op_linear(self._h, dtype, P(x), P(w), int(w_packed), m, n, k, P(bias or None), int(gelu),
+                                 P(resid or None), P(out_f32 or None), P(out_bf16 or None), ld_out or n),
+              "orca_op_linear")
         if sync:
             self.sync()
+
+    @staticmethod
+    def packed_weight_elems(n_out: int, k: int) -> int:
+        return check(lib.orca_packed_weight_elems(n_out, k), "orca_packed_weight_elems")
+
+    def pack_weight(self, w: int, n_out: int, k: int, out: int) -> None:
+        check(lib.orca_pack_weight(self._h, P(w), n_out, k, P(out)), "orca_pack_weight")
 
     def op_attention(self, dtype: int, qkv: int, kv_layer: int, kv_slots: int, n_heads: int, head_dim: int,
                      n_input, ctx_len, kv_offset, out: int, sync: bool = True):

@@ -49,11 +49,13 @@ def upload_weights(w: dict, cfg: synth.ModelConfig):
     return keep, ptrs
 
 
-def make_engine(cfg: synth.ModelConfig, w: dict, max_tokens: int, max_batch: int, kv_slots: int):
+def make_engine(cfg: synth.ModelConfig, w: dict, max_tokens: int, max_batch: int, kv_slots: int,
+                pack_weights: bool = True):
     from iteration_level_scheduling_gb300 import native
     keep, ptrs = upload_weights(w, cfg)
     eng = native.Engine(cfg.n_layers, cfg.hidden, cfg.n_heads, cfg.ffn, cfg.vocab, cfg.max_pos, DTYPE[cfg.dtype],
-                        max_tokens, max_batch, kv_slots, ptrs, torch.cuda.current_stream().cuda_stream)
+                        max_tokens, max_batch, kv_slots, ptrs, torch.cuda.current_stream().cuda_stream,
+                        pack_weights=pack_weights)
     eng._keep = keep
     return eng
 

@@ -98,7 +98,7 @@ def test_tiny_fp32_trace_token_feedback():
     assert r["worst_l"] <= TOL_FP32 and r["agree"] == 1.0, r
 
 
-def run_one_batch(cfg, w, reqs, sample, seed_kv=0, max_tokens=None):
+def run_one_batch(cfg, w, reqs, sample, seed_kv=0, max_tokens=None, pack_weights=True):
     """Run one mixed iteration over all of `reqs` on the GPU; compare the
     requests whose ids are in `sample` with the oracle (requests are
     independent, so a sub-batch gives the same per-request result)."""
@@ -106,7 +106,7 @@ def run_one_batch(cfg, w, reqs, sample, seed_kv=0, max_tokens=None):
     B = len(reqs)
     rows = sum(len(r.prompt) for r in reqs)
     reserve = {r.rid: (r.ctx0 + len(r.prompt) + 8) for r in reqs}
-    eng = make_engine(cfg, w, max_tokens or rows, B, sum(reserve.values()))
+    eng = make_engine(cfg, w, max_tokens or rows, B, sum(reserve.values()), pack_weights=pack_weights)
     pool = kv_pool_tensor(eng)
     store = KVStore(cfg.n_layers, cfg.hidden)
     offs = {}
@@ -131,7 +131,8 @@ def run_one_batch(cfg, w, reqs, sample, seed_kv=0, max_tokens=None):
     return res
 
 
-def test_gpt2_medium_mixed_batch():
+@pytest.mark.parametrize("pack_weights", [True, False])
+def test_gpt2_medium_mixed_batch(pack_weights):
     """GPT-2-medium shape, bf16: prompts (128, 64, 256) + 29 increment requests with
     contexts U[1,1024] (sum L = 477); sampled requests against the oracle."""
     cfg = synth.GPT2_MEDIUM
@@ -141,7 +142,7 @@ def test_gpt2_medium_mixed_batch():
     longest = sorted((r for r in reqs if r.ctx0), key=lambda r: -r.ctx0)[:4]
     shortest = sorted((r for r in reqs if r.ctx0), key=lambda r: r.ctx0)[:2]
     sample = {0, 1, 2} | {r.rid for r in longest + shortest}
-    res = run_one_batch(cfg, w, reqs, sample)
+    res = run_one_batch(cfg, w, reqs, sample, pack_weights=pack_weights)
     assert res["h"] <= TOL_BF16 and res["l"] <= TOL_BF16, res
 
 

@@ -44,9 +44,17 @@ SHAPES = [
 ]
 
 
+def packed(eng, wd, n, k):
+    """The tile-contiguous copy of a bf16 weight the engine streams."""
+    buf = torch.zeros(eng.packed_weight_elems(n, k), dtype=torch.bfloat16, device="cuda")
+    eng.pack_weight(wd.data_ptr(), n, k, buf.data_ptr())
+    return buf
+
+
 @pytest.mark.parametrize("m,n,k", SHAPES)
 @pytest.mark.parametrize("mode", ["plain_bf16", "bias_gelu_bf16", "bias_resid_f32"])
-def test_linear_tc_bf16(eng, m, n, k, mode):
+@pytest.mark.parametrize("w_packed", [False, True])
+def test_linear_tc_bf16(eng, m, n, k, mode, w_packed):
     from iteration_level_scheduling_gb300 import native
     g = np.random.default_rng(m * 7919 + n * 31 + k)
     x = synth.bf16_round(g.standard_normal((m, k), dtype=np.float32))
@@ -55,20 +63,40 @@ def test_linear_tc_bf16(eng, m, n, k, mode):
     resid = g.standard_normal((m, n), dtype=np.float32)
     xd = torch.from_numpy(x).cuda().to(torch.bfloat16)
     wd = torch.from_numpy(w).cuda().to(torch.bfloat16)
+    if w_packed:
+        wd = packed(eng, wd, n, k)
     bd = torch.from_numpy(bias).cuda()
     if mode == "bias_resid_f32":
         out = torch.from_numpy(resid).cuda()
         eng.op_linear(native.DTYPE_BF16, xd.data_ptr(), wd.data_ptr(), m, n, k, bias=bd.data_ptr(),
-                      resid=out.data_ptr(), out_f32=out.data_ptr())
+                      resid=out.data_ptr(), out_f32=out.data_ptr(), w_packed=w_packed)
         ref = ref_linear(x, w, bias, False, resid)
         assert rel(out.cpu().numpy(), ref) < 1e-5
     else:
         out = torch.zeros((m, n), dtype=torch.bfloat16, device="cuda")
         act = mode == "bias_gelu_bf16"
         eng.op_linear(native.DTYPE_BF16, xd.data_ptr(), wd.data_ptr(), m, n, k,
-                      bias=bd.data_ptr() if act else 0, gelu=act, out_bf16=out.data_ptr())
+                      bias=bd.data_ptr() if act else 0, gelu=act, out_bf16=out.data_ptr(), w_packed=w_packed)
         ref = ref_linear(x, w, bias if act else None, act)
         assert rel(out.float().cpu().numpy(), ref) < 8e-3
+
+
+def test_pack_weight_layout(eng):
+    """The packed layout is the documented one: tile (ft, kb) at (ft * k/64 + kb) * 8192, row r of the
+    tile at r * 64 elements, 8-element chunk c at chunk position c ^ (r % 8), rows past n_out zero."""
+    n, k = 200, 192
+    w = torch.arange(n * k, dtype=torch.float32).reshape(n, k).remainder(251).to(torch.bfloat16).cuda()
+    p = packed(eng, w, n, k).view(torch.int16).cpu().numpy()
+    wn = w.view(torch.int16).cpu().numpy()
+    kbn = k // 64
+    for ft in range(2):
+        for kb in range(kbn):
+            tile = p[(ft * kbn + kb) * 8192:(ft * kbn + kb + 1) * 8192].reshape(128, 8, 8)
+            for r in range(128):
+                for c in range(8):
+                    row = ft * 128 + r
+                    expect = wn[row, kb * 64 + c * 8: kb * 64 + c * 8 + 8] if row < n else np.zeros(8, np.int16)
+                    assert (tile[r, c ^ (r % 8)] == expect).all()
 
 
 def test_linear_tc_lm_head_shape(eng):
@@ -80,8 +108,8 @@ def test_linear_tc_lm_head_shape(eng):
     w = synth.bf16_round(g.standard_normal((n, k), dtype=np.float32) * np.float32(0.02))
     out = torch.zeros((m, n), dtype=torch.float32, device="cuda")
     xd = torch.from_numpy(x).cuda().to(torch.bfloat16)
-    wd = torch.from_numpy(w).cuda().to(torch.bfloat16)
-    eng.op_linear(native.DTYPE_BF16, xd.data_ptr(), wd.data_ptr(), m, n, k, out_f32=out.data_ptr())
+    wd = packed(eng, torch.from_numpy(w).cuda().to(torch.bfloat16), n, k)
+    eng.op_linear(native.DTYPE_BF16, xd.data_ptr(), wd.data_ptr(), m, n, k, out_f32=out.data_ptr(), w_packed=True)
     ref = ref_linear(x, w)
     got = out.cpu().numpy()
     assert rel(got, ref) < 1e-5
