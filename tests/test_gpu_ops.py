@@ -71,7 +71,8 @@ def test_linear_tc_bf16(eng, m, n, k, mode, w_packed):
         eng.op_linear(native.DTYPE_BF16, xd.data_ptr(), wd.data_ptr(), m, n, k, bias=bd.data_ptr(),
                       resid=out.data_ptr(), out_f32=out.data_ptr(), w_packed=w_packed)
         ref = ref_linear(x, w, bias, False, resid)
-        assert rel(out.cpu().numpy(), ref) < 1e-5
+        # fp32 accumulation of k products: rounding error grows like sqrt(k)
+        assert rel(out.cpu().numpy(), ref) < 1e-5 * max(1.0, np.sqrt(k / 1024))
     else:
         out = torch.zeros((m, n), dtype=torch.bfloat16, device="cuda")
         act = mode == "bias_gelu_bf16"
