@@ -145,76 +145,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {
-            // with one token tile the weights are read exactly once: stream them past L2
-            const bool stream_w = a.n_tok_tiles == 1;
-            const uint64_t pol_w = l2_policy_evict_first();
-            // The weights do not depend on earlier kernels: fill the first stages
-            // with weight slices before waiting for the previous kernel, then
-            // add the activation slices.
-            // packed weights: tile (ft, kb) is one contiguous 16 KiB block, already in
-            // the swizzled shared-memory image, so one bulk copy moves it
-            const bf16 *wp = a.w_packed ? a.w_packed + (size_t)ft * a.num_kb * (BM * BK) : nullptr;
-            auto load_w = [&](int i, int s) {
-                uint8_t *sa = smem + (size_t)s * stage_bytes;
-                if (wp)
-                    bulk_load(sa, wp + (size_t)(kb0 + i) * (BM * BK), kStageA, &full[s], pol_w);
-                else if (stream_w)
-                    tma_load_2d_hint(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM, pol_w);
-                else
-                    tma_load_2d(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM);
-            };
-            const int pre = min(nkb, a.stages);
+        // The whole warp runs the loop (so addresses and coordinates stay warp-
+        // uniform) and one elected lane issues the copies.
+        const bool leader = elect_one();
+        // with one token tile the weights are read exactly once: stream them past L2
+        const bool stream_w = a.n_tok_tiles == 1;
+        const uint64_t pol_w = l2_policy_evict_first();
+        // packed weights: tile (ft, kb) is one contiguous 16 KiB block, already in
+        // the swizzled shared-memory image, so one bulk copy moves it
+        const bf16 *wp = a.w_packed ? a.w_packed + (size_t)ft * a.num_kb * (BM * BK) : nullptr;
+        auto load_w = [&](int i, int s) {
+            uint8_t *sa = smem + (size_t)s * stage_bytes;
+            if (wp)
+                bulk_load(sa, wp + (size_t)(kb0 + i) * (BM * BK), kStageA, &full[s], pol_w);
+            else if (stream_w)
+                tma_load_2d_hint(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM, pol_w);
+            else
+                tma_load_2d(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM);
+        };
+        // The weights do not depend on earlier kernels: fill the first stages
+        // with weight slices before waiting for the previous kernel, then add
+        // the activation slices.
+        const int pre = min(nkb, a.stages);
+        if (leader)
             for (int i = 0; i < pre; ++i) {
                 mbar_arrive_expect_tx(&full[i], (uint32_t)stage_bytes);
                 load_w(i, i);
             }
-            pdl_wait();
+        pdl_wait();
+        if (leader)
             for (int i = 0; i < pre; ++i)
                 tma_load_2d(smem + (size_t)i * stage_bytes + kStageA, &tmx, &full[i], (kb0 + i) * BK, t_base);
-            int issued = pre;
-            bool ok = true;
-            for (int i = pre; i < nkb; ++i) {
-                const int s = i % a.stages;
-                const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
-                if (!mbar_wait_bounded(&empty[s], ph ^ 1u, a.err)) {
-                    ok = false;
-                    break;
-                }
+        __syncwarp();
+        int issued = pre;
+        bool ok = true;
+        for (int i = pre; i < nkb; ++i) {
+            const int s = i % a.stages;
+            const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], ph ^ 1u, a.err))) {
+                ok = false;
+                break;
+            }
+            if (leader) {
                 mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
                 load_w(i, s);
                 tma_load_2d(smem + (size_t)s * stage_bytes + kStageA, &tmx, &full[s], (kb0 + i) * BK, t_base);
-                ++issued;
             }
-            if (!ok) {
-                flags[0] = 1;
-                // let the copies already in flight land before the CTA exits
-                for (int j = max(0, issued - a.stages); j < issued; ++j)
-                    mbar_wait_bounded(&full[j % a.stages], (uint32_t)(j / a.stages) & 1u, a.err);
-            }
-        } else {
-            pdl_wait();
+            __syncwarp();
+            ++issued;
+        }
+        if (!ok && leader) {
+            flags[0] = 1;
+            // let the copies already in flight land before the CTA exits
+            for (int j = max(0, issued - a.stages); j < issued; ++j)
+                mbar_wait_bounded(&full[j % a.stages], (uint32_t)(j / a.stages) & 1u, a.err);
         }
     } else if (warp == 1) {
+        // whole warp in the loop, one elected lane issues the MMAs and commits
         pdl_wait();
-        if (lane == 0) {
-            bool ok = true;
-            for (int i = 0; i < nkb; ++i) {
-                const int s = i % a.stages;
-                const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
-                if (!mbar_wait_bounded(&full[s], ph, a.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-                const uint64_t ad = smem_desc_k128(sa), bd = smem_desc_k128(sa + kStageA);
+        const bool leader = elect_one();
+        bool ok = true;
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % a.stages;
+            const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], ph, a.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+            const uint64_t ad = smem_desc_k128(sa), bd = smem_desc_k128(sa + kStageA);
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)  // 16 bf16 = 32 B per MMA: +2 in the >>4 address field
                     tc_mma_f16(tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), a.idesc,
                                (uint32_t)((i | kk) != 0));
                 tc_commit(&empty[s]);
             }
+            __syncwarp();
+        }
+        if (leader) {
             if (ok) {
                 tc_commit(done);
             } else {
