@@ -68,6 +68,33 @@ def parse():
     return p.parse_args()
 
 
+def profiled_traffic_ratio():
+    """DRAM traffic / algorithmic bytes of the GEMM launches in the committed ncu
+    capture (profiles/gemm_tc_decode_gpt3_13b.md), or None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "gemm_tc_decode_gpt3_13b.md")) as f:
+            for line in f:
+                if line.startswith("traffic_over_algorithmic:"):
+                    return float(line.split(":", 1)[1])
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def reduce_replicas(elapsed, tokens, world, device):
+    """Replicas run independently; the job's time is the slowest rank's and its
+    work is every rank's tokens."""
+    if world <= 1:
+        return elapsed, tokens
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed, float(tokens)], dtype=torch.float64, device=device)
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return mx[0].item(), t[1].item()
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -364,13 +391,7 @@ def run_orca(args, rank, world, local_rank):
     elapsed_ms = evs[0].elapsed_time(evs[-1])
     tokens = sum(w["B"] for w in work[args.warmup:])
 
-    # aggregate over ranks (replicas): total tokens, max time
-    if world > 1:
-        t = torch.tensor([elapsed_ms, float(tokens)], device="cuda", dtype=torch.float64)
-        mx = t.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        elapsed_ms, tokens = mx[0].item(), t[1].item()
+    elapsed_ms, tokens = reduce_replicas(elapsed_ms, tokens, world, "cuda")
     value = tokens / (elapsed_ms / 1000.0)
 
     # per-iteration roofline (tensor peak: sustained, the kernels run inside a long step)
@@ -410,7 +431,12 @@ def run_orca(args, rank, world, local_rank):
     else:
         ach = dom["bytes"] / (dom["ms"] / 1000) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s"}
-    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "kernel": dom_name,
+    ratio = profiled_traffic_ratio() if dom_name.startswith("gemm_tc") else None
+    traffic = ratio * dom["bytes"] / dom["n"] if ratio else None
+    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": traffic, "kernel": dom_name,
+                 "traffic_source": ("DRAM bytes per launch: algorithmic bytes x the traffic/algorithmic ratio "
+                                    "of profiles/gemm_tc_decode_gpt3_13b.md (2-layer capture, same shapes)")
+                 if traffic else None,
                  "peak_source": peaks["src"], "launches_timed": dom["n"],
                  "algorithmic_bytes_per_launch": dom["bytes"] / dom["n"],
                  "algorithmic_flops_per_launch": dom["flops"] / dom["n"]})
@@ -451,12 +477,7 @@ def run_orca(args, rank, world, local_rank):
             step(True)
         torch.cuda.synchronize()
         e2e_s = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([e2e_s, float(e2e_tokens)], device="cuda", dtype=torch.float64)
-            mx = t.clone()
-            dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-            dist.all_reduce(t, op=dist.ReduceOp.SUM)
-            e2e_s, e2e_tokens = mx[0].item(), t[1].item()
+        e2e_s, e2e_tokens = reduce_replicas(e2e_s, e2e_tokens, world, "cuda")
         e2e = {"value": e2e_tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d / args.steps,
                "d2h_bytes_per_step": d2h / args.steps, "ms_per_step": 1000 * e2e_s / args.steps}
         s2.close()
