@@ -440,11 +440,7 @@ TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool al
     // one CTA per SM with a deep ring when everything runs in one wave, else two
     const int stage_bytes = kStageA + t.bn * BK * 2;
     const size_t max_stages_1cta = (kSmemMaxCta - kSmemExtra) / stage_bytes;
-    // Narrow token tiles keep to about half the shared memory, so that two CTAs fit on an
-    // SM: then the next GEMM's CTAs (programmatic dependent launch) start their
-    // prologue and weight prefetch while this one drains.  A 4-stage ring of such
-    // stages already keeps enough bytes in flight for HBM.
-    const int ctas_per_sm = t.bn <= 128 ? 2 : 1;
+    const int ctas_per_sm = (tiles * t.splits > s.num_sms && t.bn <= 128) ? 2 : 1;
     const size_t budget = std::min(kSmemMaxCta, kSmemPerSm / ctas_per_sm - kSmemReserve) - kSmemExtra;
     t.stages = std::min<int>(kMaxStages, (int)(budget / stage_bytes));
     if (override_stages() > 0) t.stages = std::min<int>(std::min(override_stages(), kMaxStages), (int)max_stages_1cta);

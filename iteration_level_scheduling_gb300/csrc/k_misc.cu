@@ -59,6 +59,26 @@ __global__ void __launch_bounds__(kRowThreads) embed_kernel(const int32_t *token
     }
 }
 
+constexpr int kLnThreads = 256;
+constexpr int kLnMaxVec = 8;  // H <= kLnThreads * 4 * kLnMaxVec = 8192
+
+__device__ __forceinline__ float block_sum(float v, float *red) {
+    v = warp_sum(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    float t = 0.f;
+    if (w == 0) {
+        t = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
+        t = warp_sum(t);
+        if (l == 0) red[32] = t;
+    }
+    __syncthreads();
+    t = red[32];
+    __syncthreads();
+    return t;
+}
+
 template <typename T>
 __device__ __forceinline__ void store_vec4(T *p, const float *v);
 template <>
@@ -74,79 +94,66 @@ __device__ __forceinline__ void store_vec4<bf16>(bf16 *p, const float *v) {
     *reinterpret_cast<uint2 *>(p) = u;
 }
 
-// LayerNorm with biased variance, eps 1e-5, statistics in fp32 from registers.
-// One CTA of 4 warps per row; every load of the row (and, when completing a
-// split-K projection, of its partial rows) is issued before the first use,
-// and each reduction is warp shuffles plus one block barrier.
-constexpr int kLnThreads = 128;
-constexpr int kLnMaxH = 8192;
-constexpr int kLnChunks = kLnMaxH / (4 * kLnThreads);  // float4 per thread
-
-__device__ __forceinline__ float ln_block_sum(float v, float *red, int slot) {
-    v = warp_sum(v);
-    if ((threadIdx.x & 31) == 0) red[slot * 4 + (threadIdx.x >> 5)] = v;
-    __syncthreads();
-    return red[slot * 4 + 0] + red[slot * 4 + 1] + red[slot * 4 + 2] + red[slot * 4 + 3];  // fixed order
-}
-
+// LayerNorm with biased variance, eps 1e-5, statistics in fp32 from registers
+// (two passes over the row held in registers).
 template <typename T>
 __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(float *x, const int32_t *row_map, const float *g,
                                                                const float *b, T *y, float *y32, int H,
                                                                const float *part, int n_part, int part_rows,
                                                                const float *add_bias) {
-    __shared__ float red[8];
+    __shared__ float red[33];
     pdl_trigger();
     pdl_wait();
     const int r = blockIdx.x;
     const int src = row_map ? row_map[r] : r;
     float *xr = x + (size_t)src * H;
-    const int nc = H / 4;  // float4 chunks of the row; thread t handles chunks t, t + 128, ...
-    float4 v[kLnChunks];
-#pragma unroll
-    for (int i = 0; i < kLnChunks; ++i)
-        if (i * kLnThreads + (int)threadIdx.x < nc)
-            v[i] = *reinterpret_cast<const float4 *>(xr + (i * kLnThreads + threadIdx.x) * 4);
-    if (n_part > 0) {
-        // complete the residual row: x + (bias + the split-K partials, in split order)
-#pragma unroll
-        for (int i = 0; i < kLnChunks; ++i) {
-            const int c = i * kLnThreads + threadIdx.x;
-            if (c >= nc) break;
-            float4 acc = add_bias ? *reinterpret_cast<const float4 *>(add_bias + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
-            float4 pv[8];
-#pragma unroll
-            for (int sp = 0; sp < 8; ++sp)
-                if (sp < n_part) pv[sp] = *reinterpret_cast<const float4 *>(part + ((size_t)sp * part_rows + src) * H + 4 * c);
-#pragma unroll
-            for (int sp = 0; sp < 8; ++sp)
-                if (sp < n_part) acc.x += pv[sp].x, acc.y += pv[sp].y, acc.z += pv[sp].z, acc.w += pv[sp].w;
-            v[i].x += acc.x, v[i].y += acc.y, v[i].z += acc.z, v[i].w += acc.w;
-            *reinterpret_cast<float4 *>(xr + 4 * c) = v[i];
-        }
-    }
+    float v[kLnMaxVec][4];
     float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < kLnChunks; ++i)
-        if (i * kLnThreads + (int)threadIdx.x < nc) s += v[i].x + v[i].y + v[i].z + v[i].w;
-    const float mean = ln_block_sum(s, red, 0) / (float)H;
+    for (int i = 0; i < kLnMaxVec; ++i) {
+        int e = (threadIdx.x + i * kLnThreads) * 4;
+        if (e < H) {
+            float4 q = *reinterpret_cast<const float4 *>(xr + e);
+            if (n_part > 0) {
+                // complete the residual row: x + bias + the split-K partials, in split order
+                float4 acc = add_bias ? *reinterpret_cast<const float4 *>(add_bias + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int sp = 0; sp < n_part; ++sp) {
+                    const float4 pv = *reinterpret_cast<const float4 *>(part + ((size_t)sp * part_rows + src) * H + e);
+                    acc.x += pv.x, acc.y += pv.y, acc.z += pv.z, acc.w += pv.w;
+                }
+                q.x += acc.x, q.y += acc.y, q.z += acc.z, q.w += acc.w;
+                *reinterpret_cast<float4 *>(xr + e) = q;
+            }
+            v[i][0] = q.x, v[i][1] = q.y, v[i][2] = q.z, v[i][3] = q.w;
+            s += q.x + q.y + q.z + q.w;
+        }
+    }
+    const float mean = block_sum(s, red) / (float)H;
     float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < kLnChunks; ++i)
-        if (i * kLnThreads + (int)threadIdx.x < nc) {
-            const float a0 = v[i].x - mean, a1 = v[i].y - mean, a2 = v[i].z - mean, a3 = v[i].w - mean;
-            ss += a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
-        }
-    const float rstd = rsqrtf(ln_block_sum(ss, red, 1) / (float)H + 1e-5f);
+    for (int i = 0; i < kLnMaxVec; ++i) {
+        int e = (threadIdx.x + i * kLnThreads) * 4;
+        if (e < H) {
 #pragma unroll
-    for (int i = 0; i < kLnChunks; ++i) {
-        const int c = i * kLnThreads + threadIdx.x;
-        if (c >= nc) break;
-        const float4 gg = *reinterpret_cast<const float4 *>(g + 4 * c);
-        const float4 bb = *reinterpret_cast<const float4 *>(b + 4 * c);
-        float o[4] = {(v[i].x - mean) * rstd * gg.x + bb.x, (v[i].y - mean) * rstd * gg.y + bb.y,
-                      (v[i].z - mean) * rstd * gg.z + bb.z, (v[i].w - mean) * rstd * gg.w + bb.w};
-        store_vec4<T>(y + (size_t)r * H + 4 * c, o);
-        if (y32) store16(y32 + (size_t)r * H + 4 * c, o);
+            for (int j = 0; j < 4; ++j) {
+                float d = v[i][j] - mean;
+                ss += d * d;
+            }
+        }
+    }
+    const float var = block_sum(ss, red) / (float)H;
+    const float rstd = rsqrtf(var + 1e-5f);
+#pragma unroll
+    for (int i = 0; i < kLnMaxVec; ++i) {
+        int e = (threadIdx.x + i * kLnThreads) * 4;
+        if (e < H) {
+            float4 gg = *reinterpret_cast<const float4 *>(g + e);
+            float4 bb = *reinterpret_cast<const float4 *>(b + e);
+            float o[4] = {(v[i][0] - mean) * rstd * gg.x + bb.x, (v[i][1] - mean) * rstd * gg.y + bb.y,
+                          (v[i][2] - mean) * rstd * gg.z + bb.z, (v[i][3] - mean) * rstd * gg.w + bb.w};
+            store_vec4<T>(y + (size_t)r * H + e, o);
+            if (y32) store16(y32 + (size_t)r * H + e, o);
+        }
     }
 }
 
@@ -224,7 +231,7 @@ template <typename T>
 cudaError_t layernorm(float *x, const int32_t *row_map, const float *g, const float *b, T *y, float *y32, int n_rows,
                       int H, cudaStream_t st, const float *part, int n_part, int part_rows, const float *add_bias) {
     if (n_rows <= 0) return cudaSuccess;
-    if (H % 4 != 0 || H > kLnMaxH || n_part > 8) return cudaErrorInvalidValue;
+    if (H % 4 != 0 || H > kLnThreads * 4 * kLnMaxVec) return cudaErrorInvalidValue;
     return launch_pdl(layernorm_kernel<T>, dim3(n_rows), dim3(kLnThreads), 0, st, x, row_map, g, b, y, y32, H, part,
                       n_part, part_rows, add_bias);
 }
