@@ -115,12 +115,16 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(float *x, const i
         if (e < H) {
             float4 q = *reinterpret_cast<const float4 *>(xr + e);
             if (n_part > 0) {
-                // complete the residual row: x + bias + the split-K partials, in split order
+                // complete the residual row: x + (bias + the split-K partials, in split
+                // order); all partial loads are issued before the first add
                 float4 acc = add_bias ? *reinterpret_cast<const float4 *>(add_bias + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int sp = 0; sp < n_part; ++sp) {
-                    const float4 pv = *reinterpret_cast<const float4 *>(part + ((size_t)sp * part_rows + src) * H + e);
-                    acc.x += pv.x, acc.y += pv.y, acc.z += pv.z, acc.w += pv.w;
-                }
+                float4 pv[8];
+#pragma unroll
+                for (int sp = 0; sp < 8; ++sp)
+                    if (sp < n_part) pv[sp] = *reinterpret_cast<const float4 *>(part + ((size_t)sp * part_rows + src) * H + e);
+#pragma unroll
+                for (int sp = 0; sp < 8; ++sp)
+                    if (sp < n_part) acc.x += pv[sp].x, acc.y += pv[sp].y, acc.z += pv[sp].z, acc.w += pv[sp].w;
                 q.x += acc.x, q.y += acc.y, q.z += acc.z, q.w += acc.w;
                 *reinterpret_cast<float4 *>(xr + e) = q;
             }
@@ -231,7 +235,7 @@ template <typename T>
 cudaError_t layernorm(float *x, const int32_t *row_map, const float *g, const float *b, T *y, float *y32, int n_rows,
                       int H, cudaStream_t st, const float *part, int n_part, int part_rows, const float *add_bias) {
     if (n_rows <= 0) return cudaSuccess;
-    if (H % 4 != 0 || H > kLnThreads * 4 * kLnMaxVec) return cudaErrorInvalidValue;
+    if (H % 4 != 0 || H > kLnThreads * 4 * kLnMaxVec || n_part > 8) return cudaErrorInvalidValue;
     return launch_pdl(layernorm_kernel<T>, dim3(n_rows), dim3(kLnThreads), 0, st, x, row_map, g, b, y, y32, H, part,
                       n_part, part_rows, add_bias);
 }
