@@ -25,6 +25,7 @@
 //           and attends causally over keys 0..pos of its request.
 // Scores use exp2 with log2(e)/sqrt(head_dim) folded into q; the softmax is
 // the online (running max / running sum) form, exact up to rounding.
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -128,12 +129,17 @@ __device__ __forceinline__ void merge_groups(float &m, float &l, float *o) {
 
 // Decode: the K and V rows of one (request, head, chunk) are contiguous in the
 // pool, so a producer warp streams them into a ring of shared-memory stages
-// with bulk asynchronous copies (kDecTok tokens of K and of V per stage,
+// with bulk asynchronous copies (kTok tokens of K and of V per stage,
 // completing on an mbarrier); four consumer warps score and accumulate from
 // shared memory and release each stage through a second mbarrier.
+// Persistent: a grid of a few CTAs per SM walks the (work item, head) list --
+// work items sorted by length, longest first -- CTA b taking entries b,
+// b + grid, ...  The producer runs ahead across item boundaries, so the ring
+// never drains between items, and the consumers prefetch the next item's q.
 constexpr int kDecStages = 4;
 constexpr int kDecConsumers = 4;
 constexpr int kDecThreads = 32 * (kDecConsumers + 1);
+constexpr int kDecCtasPerSm = 3;
 
 // Tokens per stage: at least 32, and at least one warp-wide step per consumer.
 template <typename T, int D>
@@ -151,6 +157,21 @@ struct DecodeSmem {
     int last, abort;
 };
 
+// Barrier over the 128 consumer threads only (the producer warp never joins).
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool consumers_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const AttnArgs<T> a) {
     constexpr int VEC = Elem<T>::kPer16;
@@ -162,17 +183,19 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const AttnArgs
     static_assert(PER_WARP % TPW == 0, "stage split");
     extern __shared__ __align__(128) uint8_t dyn_smem[];
     DecodeSmem<T, D> &sm = *reinterpret_cast<DecodeSmem<T, D> *>(dyn_smem);
-
     pdl_trigger();
     pdl_wait();
-    const int w_idx = blockIdx.x, h = blockIdx.y;
-    const int i = a.p.dec_work[2 * w_idx], c = a.p.dec_work[2 * w_idx + 1];
-    const int row = a.p.req_off[i];
-    const int n_keys = a.p.req_ctx[i] + 1;
-    const int t0 = c * a.p.chunk, t1 = min(n_keys, t0 + a.p.chunk);
-    const int n_it = (t1 - t0 + kDecTok - 1) / kDecTok;
-    const size_t head_base = ((size_t)h * a.kv_slots + a.p.req_kvoff[i]) * D;
+
+    const int total = a.p.n_dec_work * a.n_heads;
+    const int G = gridDim.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // entry q of the list -> (request i, chunk c, head h)
+    auto item = [&](int q, int &i, int &c, int &h) {
+        const int w = a.p.dec_order[q / a.n_heads];
+        h = q % a.n_heads;
+        i = a.p.dec_work[2 * w];
+        c = a.p.dec_work[2 * w + 1];
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kDecStages; ++s) {
@@ -186,49 +209,78 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const AttnArgs
 
     if (warp == kDecConsumers) {
         // ------------------------------ producer ------------------------------
-        if (lane == 0) {
+        if (elect_one()) {
             const uint64_t pol = l2_policy_evict_first();  // every cached row is read once per iteration
-            int issued = 0;
-            for (int it = 0; it < n_it; ++it) {
-                const int s = it % kDecStages;
-                const uint32_t ph = (uint32_t)(it / kDecStages) & 1u;
-                if (!mbar_wait_bounded(&sm.empty[s], ph ^ 1u, a.err)) {
-                    sm.abort = 1;
-                    break;
+            uint32_t g = 0, issued = 0;
+            bool ok = true;
+            for (int q = blockIdx.x; q < total && ok; q += G) {
+                int i, c, h;
+                item(q, i, c, h);
+                const int n_keys = a.p.req_ctx[i] + 1;
+                const int t0 = c * a.p.chunk, t1 = min(n_keys, t0 + a.p.chunk);
+                const size_t head_base = ((size_t)h * a.kv_slots + a.p.req_kvoff[i]) * D;
+                for (int t = t0; t < t1; t += kDecTok, ++g) {
+                    const int s = g % kDecStages;
+                    const uint32_t ph = (g / kDecStages) & 1u;
+                    if (!mbar_wait_bounded(&sm.empty[s], ph ^ 1u, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bytes = (uint32_t)(min(kDecTok, t1 - t) * D * sizeof(T));
+                    mbar_arrive_expect_tx(&sm.full[s], 2 * bytes);
+                    bulk_load(&sm.kv[s][0][0][0], a.kpool + head_base + (size_t)t * D, bytes, &sm.full[s], pol);
+                    bulk_load(&sm.kv[s][1][0][0], a.vpool + head_base + (size_t)t * D, bytes, &sm.full[s], pol);
+                    ++issued;
                 }
-                const int t = t0 + it * kDecTok;
-                const uint32_t bytes = (uint32_t)(min(kDecTok, t1 - t) * D * sizeof(T));
-                mbar_arrive_expect_tx(&sm.full[s], 2 * bytes);
-                bulk_load(&sm.kv[s][0][0][0], a.kpool + head_base + (size_t)t * D, bytes, &sm.full[s], pol);
-                bulk_load(&sm.kv[s][1][0][0], a.vpool + head_base + (size_t)t * D, bytes, &sm.full[s], pol);
-                ++issued;
             }
-            if (sm.abort)  // let the copies in flight land before the CTA exits
-                for (int j = max(0, issued - kDecStages); j < issued; ++j)
-                    mbar_wait_bounded(&sm.full[j % kDecStages], (uint32_t)(j / kDecStages) & 1u, a.err);
+            if (!ok) {  // let the copies in flight land before the CTA exits
+                sm.abort = 1;
+                for (uint32_t j = issued > kDecStages ? issued - kDecStages : 0; j < issued; ++j)
+                    mbar_wait_bounded(&sm.full[j % kDecStages], (j / kDecStages) & 1u, a.err);
+            }
         }
-    } else {
-        // ------------------------------ consumers -----------------------------
-        const int g = lane / LPT, sub = lane % LPT;
-        float q[VEC];
-        load16(a.qkv + (size_t)row * 3 * a.H + h * D + sub * VEC, q);
+        return;
+    }
+
+    // -------------------------------- consumers --------------------------------
+    const int g_lane = lane / LPT, sub = lane % LPT;
+    uint32_t g = 0;
+    float qn[VEC];
+    if (blockIdx.x < total) {
+        int i, c, h;
+        item(blockIdx.x, i, c, h);
+        load16(a.qkv + (size_t)a.p.req_off[i] * 3 * a.H + h * D + sub * VEC, qn);
+    }
+    for (int q = blockIdx.x; q < total; q += G) {
+        int i, c, h;
+        item(q, i, c, h);
+        const int row = a.p.req_off[i];
+        const int n_keys = a.p.req_ctx[i] + 1;
+        const int t0 = c * a.p.chunk, t1 = min(n_keys, t0 + a.p.chunk);
+        float qv[VEC];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) q[e] *= a.scale_log2;
+        for (int e = 0; e < VEC; ++e) qv[e] = qn[e] * a.scale_log2;
+        if (q + G < total) {  // the next item's q, in flight during this item
+            int i2, c2, h2;
+            item(q + G, i2, c2, h2);
+            load16(a.qkv + (size_t)a.p.req_off[i2] * 3 * a.H + h2 * D + sub * VEC, qn);
+        }
         float m = kNegBig, l = 0.f, o[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) o[e] = 0.f;
-        for (int it = 0; it < n_it; ++it) {
-            const int s = it % kDecStages;
-            const uint32_t ph = (uint32_t)(it / kDecStages) & 1u;
+        bool ok = true;
+        for (int t = t0; t < t1; t += kDecTok, ++g) {
+            const int s = g % kDecStages;
+            const uint32_t ph = (g / kDecStages) & 1u;
             if (!mbar_wait_bounded(&sm.full[s], ph, a.err)) {
-                sm.abort = 1;
+                ok = false;
                 break;
             }
-            const int ntok = min(kDecTok, t1 - (t0 + it * kDecTok));
+            const int ntok = min(kDecTok, t1 - t);
             float sc[STEPS], vv[STEPS][VEC];
 #pragma unroll
             for (int st = 0; st < STEPS; ++st) {
-                const int j = warp * PER_WARP + st * TPW + g;
+                const int j = warp * PER_WARP + st * TPW + g_lane;
                 const bool valid = j < ntok;
                 float kk[VEC];
                 if (valid) {
@@ -240,7 +292,7 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const AttnArgs
                 }
                 float acc = 0.f;
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) acc = fmaf(q[e], kk[e], acc);
+                for (int e = 0; e < VEC; ++e) acc = fmaf(qv[e], kk[e], acc);
 #pragma unroll
                 for (int off = LPT / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
                 sc[st] = valid ? acc : kNegBig;
@@ -263,61 +315,65 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const AttnArgs
             }
             m = mx;
         }
+        if (!consumers_all(ok && sm.abort == 0)) return;  // every consumer warp leaves together
         merge_groups<LPT, VEC>(m, l, o);
         if (lane < LPT) {
 #pragma unroll
             for (int e = 0; e < VEC; ++e) sm.o[warp][sub * VEC + e] = o[e];
         }
         if (lane == 0) sm.m[warp] = m, sm.l[warp] = l;
-    }
-    __syncthreads();
-    if (sm.abort) return;
+        consumers_sync();
 
-    const int nch = a.p.dec_nch[i];
-    float M = kNegBig, L = 0.f, O = 0.f;
-    const int d = threadIdx.x;
-    if (d < D) {
+        const int nch = a.p.dec_nch[i];
+        float M = kNegBig, L = 0.f, O = 0.f;
+        const int d = threadIdx.x;
+        if (d < D) {
 #pragma unroll
-        for (int w = 0; w < kDecConsumers; ++w) M = fmaxf(M, sm.m[w]);
+            for (int w = 0; w < kDecConsumers; ++w) M = fmaxf(M, sm.m[w]);
 #pragma unroll
-        for (int w = 0; w < kDecConsumers; ++w) {
-            const float cw = exp2f(sm.m[w] - M);
-            L += sm.l[w] * cw;
-            O += sm.o[w][d] * cw;
+            for (int w = 0; w < kDecConsumers; ++w) {
+                const float cw = exp2f(sm.m[w] - M);
+                L += sm.l[w] * cw;
+                O += sm.o[w][d] * cw;
+            }
         }
-    }
-    T *dst = a.out + (size_t)row * a.H + h * D;
-    if (nch == 1) {
-        if (d < D) dst[d] = Elem<T>::from_f(O / L);
-        return;
-    }
-    // several chunks: publish the partial, the last CTA of (request, head) merges
-    float *mine = a.part + ((size_t)w_idx * a.n_heads + h) * (D + 2);
-    if (d < D) mine[d] = O;
-    if (d == 0) mine[D] = M, mine[D + 1] = L;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int old = atomicAdd(&a.counters[i * a.n_heads + h], 1);
-        sm.last = (old == nch - 1);
-    }
-    __syncthreads();
-    if (!sm.last) return;
-    __threadfence();
-    if (d < D) {
-        const int wb = a.p.dec_wbegin[i];
-        float Mt = kNegBig;
-        for (int j = 0; j < nch; ++j) Mt = fmaxf(Mt, __ldcg(a.part + ((size_t)(wb + j) * a.n_heads + h) * (D + 2) + D));
-        float Lt = 0.f, Ot = 0.f;
-        for (int j = 0; j < nch; ++j) {
-            const float *pj = a.part + ((size_t)(wb + j) * a.n_heads + h) * (D + 2);
-            const float cw = exp2f(__ldcg(pj + D) - Mt);
-            Lt += __ldcg(pj + D + 1) * cw;
-            Ot += __ldcg(pj + d) * cw;
+        T *dst = a.out + (size_t)row * a.H + h * D;
+        if (nch == 1) {
+            if (d < D) dst[d] = Elem<T>::from_f(O / L);
+        } else {
+            // several chunks: publish the partial, the last CTA of (request, head) merges
+            const int w_idx = a.p.dec_wbegin[i] + c;
+            float *mine = a.part + ((size_t)w_idx * a.n_heads + h) * (D + 2);
+            if (d < D) mine[d] = O;
+            if (d == 0) mine[D] = M, mine[D + 1] = L;
+            __threadfence();
+            consumers_sync();
+            if (threadIdx.x == 0) {
+                const int old = atomicAdd(&a.counters[i * a.n_heads + h], 1);
+                sm.last = (old == nch - 1);
+            }
+            consumers_sync();
+            if (sm.last) {
+                __threadfence();
+                if (d < D) {
+                    const int wb = a.p.dec_wbegin[i];
+                    float Mt = kNegBig;
+                    for (int j = 0; j < nch; ++j)
+                        Mt = fmaxf(Mt, __ldcg(a.part + ((size_t)(wb + j) * a.n_heads + h) * (D + 2) + D));
+                    float Lt = 0.f, Ot = 0.f;
+                    for (int j = 0; j < nch; ++j) {
+                        const float *pj = a.part + ((size_t)(wb + j) * a.n_heads + h) * (D + 2);
+                        const float cw = exp2f(__ldcg(pj + D) - Mt);
+                        Lt += __ldcg(pj + D + 1) * cw;
+                        Ot += __ldcg(pj + d) * cw;
+                    }
+                    dst[d] = Elem<T>::from_f(Ot / Lt);
+                }
+                if (threadIdx.x == 0) a.counters[i * a.n_heads + h] = 0;
+            }
         }
-        dst[d] = Elem<T>::from_f(Ot / Lt);
+        consumers_sync();  // the merge buffers are reused by the next item
     }
-    if (threadIdx.x == 0) a.counters[i * a.n_heads + h] = 0;
 }
 
 template <typename T, int D>
@@ -585,8 +641,13 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        cudaError_t e = launch_pdl(attn_decode_kernel<T, D>, dim3(a.p.n_dec_work, a.n_heads), dim3(kDecThreads),
-                                   sizeof(DecodeSmem<T, D>), st, a);
+        int sms = 0, dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int total = a.p.n_dec_work * a.n_heads;
+        const int grid = std::max(1, std::min(total, kDecCtasPerSm * sms));
+        cudaError_t e = launch_pdl(attn_decode_kernel<T, D>, dim3(grid), dim3(kDecThreads), sizeof(DecodeSmem<T, D>),
+                                   st, a);
         if (e != cudaSuccess) return e;
     }
     if (prefill && a.p.n_pre_tiles > 0) {
@@ -614,6 +675,18 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
 }
 
 }  // namespace
+
+void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_ctx, int chunk, int32_t *order) {
+    // counting sort of the work items by keys in the chunk (1 .. chunk <= 512), longest first
+    int start[513 + 1] = {0};
+    auto keys = [&](int w) {
+        const int i = dec_work[2 * w], c = dec_work[2 * w + 1];
+        return std::min(chunk, req_ctx[i] + 1 - c * chunk);
+    };
+    for (int w = 0; w < n_work; ++w) ++start[chunk - keys(w) + 1];
+    for (int b = 1; b <= chunk; ++b) start[b] += start[b - 1];
+    for (int w = 0; w < n_work; ++w) order[start[chunk - keys(w)]++] = w;
+}
 
 template <typename T>
 cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *out, const AttnPlan &p, int H,
@@ -656,7 +729,7 @@ constexpr int kNaMaxReq = 256;
 constexpr int kNaMaxHeads = 128;
 constexpr size_t kNaPartFloats = size_t(1) << 22;                    // 16 MiB of partials
 constexpr size_t kNaCounterWords = size_t(kNaMaxReq) * kNaMaxHeads;  // 128 KiB
-constexpr size_t kNaPlanWords = 8 * kNaMaxReq + 2 * 8192;            // tables + up to 8192 work items
+constexpr size_t kNaPlanWords = 8 * kNaMaxReq + 3 * 8192;            // tables + up to 8192 work items
 constexpr size_t kNaScratchBytes = 4 * (kNaPartFloats + kNaCounterWords + kNaPlanWords);
 constexpr int kNaMaxDevices = 64;
 
@@ -717,12 +790,13 @@ extern "C" int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, con
     }
     int64_t n_work = 0;
     for (int i = 0; i < n_req; ++i) n_work += ((int64_t)ctx_len[i] + chunk) / chunk;
-    const size_t words = 6 * (size_t)n_req + 1 + 2 * (size_t)n_work;
+    const size_t words = 6 * (size_t)n_req + 1 + 3 * (size_t)n_work;
     if (words > kNaPlanWords || (size_t)n_work * n_heads * (head_dim + 2) > kNaPartFloats) return kLimit;
 
     // tables: req_off, req_ctx, req_kvoff, dec_wbegin, dec_nch, dec_work
     int32_t *req_off = g_na_plan, *req_ctx = req_off + n_req + 1, *req_kv = req_ctx + n_req;
     int32_t *dec_wb = req_kv + n_req, *dec_nch = dec_wb + n_req, *dec_work = dec_nch + n_req;
+    int32_t *dec_ord = dec_work + 2 * n_work;
     int w = 0;
     for (int i = 0; i < n_req; ++i) {
         const int nch = (int)(((int64_t)ctx_len[i] + chunk) / chunk);
@@ -734,6 +808,7 @@ extern "C" int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, con
         for (int c = 0; c < nch; ++c, ++w) dec_work[2 * w] = i, dec_work[2 * w + 1] = c;
     }
     req_off[n_req] = n_req;
+    decode_order(dec_work, (int)n_work, req_ctx, chunk, dec_ord);
 
     float *part = reinterpret_cast<float *>(nd.scratch);
     int32_t *counters = reinterpret_cast<int32_t *>(part + kNaPartFloats);
@@ -751,6 +826,7 @@ extern "C" int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, con
     ap.dec_wbegin = plan + (dec_wb - g_na_plan);
     ap.dec_nch = plan + (dec_nch - g_na_plan);
     ap.dec_work = plan + (dec_work - g_na_plan);
+    ap.dec_order = plan + (dec_ord - g_na_plan);
     ap.pre_tiles = nullptr;
     ap.n_dec_work = (int)n_work;
     ap.n_pre_tiles = 0;

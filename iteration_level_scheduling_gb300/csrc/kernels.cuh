@@ -87,6 +87,7 @@ cudaError_t kv_append(const T *qkv, const int32_t *row_slot, T *pool_layer, int6
 struct AttnPlan {
     const int32_t *req_off, *req_ctx, *req_kvoff;
     const int32_t *dec_work, *dec_wbegin, *dec_nch;  // decode split-K work items
+    const int32_t *dec_order;                        // work items, longest first
     const int32_t *pre_tiles;                        // prefill (request, first row) tiles
     int n_dec_work, n_pre_tiles, chunk;
 };
@@ -97,6 +98,10 @@ template <typename T>
 cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *out, const AttnPlan &p, int H,
                       int n_heads, float *part, int *counters, unsigned *err, cudaStream_t st, bool decode,
                       bool prefill);
+
+// Order of the decode work items (request, chunk) by number of keys, longest
+// first (stable), for the persistent decode kernel's load balance.
+void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_ctx, int chunk, int32_t *order);
 
 // next[b] = argmax_j logits[b, j] (lowest j on ties); also to out2 if non-null.
 cudaError_t argmax_rows(const float *logits, int n_rows, int V, int32_t *next, int32_t *out2, cudaStream_t st);
