@@ -15,9 +15,11 @@
 //
 // decode  : requests with one input row (increment phase).  Work item =
 //           (request, chunk of `chunk` keys) x head, its K/V rows streamed into
-//           shared memory by bulk asynchronous copies; a request whose keys
-//           span several chunks is merged by the last CTA to finish (per-
-//           (request, head) arrival counter; no CTA ever waits on another).
+//           shared memory by a producer warp; a request whose keys span
+//           several chunks is merged by the last CTA to finish (per-(request,
+//           head) arrival counter; no CTA ever waits on another).  bf16 with
+//           head_dim 64/128: TMA-loaded stages scored and accumulated on the
+//           tensor cores (below); otherwise bulk copies and SIMT dot products.
 // prefill : requests with several input rows (initiation phase, or any
 //           multi-row request).  Work item = (request, 64 query rows) x head.
 //           bf16 with head_dim 64/128: flash-attention tiles on the tensor
@@ -631,8 +633,351 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const AttnArgs<bf
     }
 }
 
+// ---------------------------------------------------------------------------
+// Decode on tensor cores (bf16, head_dim 64 or 128).  Same persistent layout
+// as the kernel above -- a producer warp streams stages of kMdTok tokens of
+// one (request chunk, head) into a ring, consumer warps drain it, the producer
+// runs ahead across item boundaries -- but the stages arrive by 3-D TMA boxes
+// of 64 dims x kMdTok tokens with 128-byte swizzling (so ldmatrix reads them
+// without bank conflicts), and each of the four consumer warps scores and
+// accumulates its 16 tokens of a stage on mma.sync m16n8k16.  With one query
+// per (request, head) the keys take the M dimension:
+//   S^T = K q^T    A = the warp's 16-token x 16-dim K tile (ldmatrix), B = q
+//   O^T += V^T p   A = a 16-dim x 16-token V^T tile (ldmatrix.trans), B = p
+// Every column of B holds the same vector, so every column of each 16 x 8
+// result holds the answer.  p enters the MMA rounded to bf16 and l sums those
+// rounded weights.  Rows past an item's end in its last stage are masked out
+// of the scores and zeroed in V (they may belong to another request).
+// ---------------------------------------------------------------------------
+constexpr int kMdTok = 64;
+constexpr int kMdConsumers = kMdTok / 16;
+constexpr int kMdProducerWarp = kMdConsumers, kMdMergerWarp = kMdConsumers + 1;
+constexpr int kMdThreads = 32 * (kMdConsumers + 2);
+constexpr int kMdCtasPerSm = 2;
+constexpr int kMdMerge = 4;  // item results queued for the merge warp
+
+template <int D>
+__host__ __device__ constexpr uint32_t md_stage_bytes() {
+    return 2u * D * kMdTok * 2u;  // K and V
+}
+template <int D>
+__host__ __device__ constexpr int md_stages() {
+    return (int)(98304u / md_stage_bytes<D>());  // 96 KiB of ring
+}
+template <int D>
+struct MdTail {  // after the ring
+    uint64_t full[md_stages<D>()], empty[md_stages<D>()];
+    uint64_t mfull[kMdMerge], mempty[kMdMerge];
+    float o[kMdMerge][kMdConsumers][D];  // each consumer warp's unnormalised output of an item
+    float m[kMdMerge][kMdConsumers], l[kMdMerge][kMdConsumers];
+    volatile int abort;
+};
+template <int D>
+__host__ __device__ constexpr size_t md_smem_bytes() {
+    return 1024 + md_stages<D>() * md_stage_bytes<D>() + sizeof(MdTail<D>);
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+__device__ __forceinline__ int atom_add_acq_rel(int *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm,
+                                                                     const AttnArgs<bf16> a) {
+    constexpr int NB = D / 64;  // 64-dim boxes per row
+    constexpr int KS = D / 16;  // k-steps of the scores
+    constexpr int MT = D / 16;  // 16-dim tiles of the output
+    constexpr int S = md_stages<D>();
+    constexpr uint32_t kBox = kMdTok * 128;
+    constexpr uint32_t kStage = md_stage_bytes<D>();
+    static_assert(D % 64 == 0 && S >= 2, "tile shape");
+    extern __shared__ uint8_t dyn_smem[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+    MdTail<D> &sm = *reinterpret_cast<MdTail<D> *>(ring + S * kStage);
+    pdl_trigger();
+
+    const int total = a.p.n_dec_work * a.n_heads;
+    const int G = gridDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto item = [&](int q, int &i, int &c, int &h) {
+        const int w = a.p.dec_order[q / a.n_heads];
+        h = q % a.n_heads;
+        i = a.p.dec_work[2 * w];
+        c = a.p.dec_work[2 * w + 1];
+    };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kMdConsumers);
+        }
+        for (int e = 0; e < kMdMerge; ++e) {
+            mbar_init(&sm.mfull[e], kMdConsumers);
+            mbar_init(&sm.mempty[e], 1);
+        }
+        sm.abort = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tm);
+    }
+    __syncthreads();
+    pdl_wait();  // this iteration's K/V rows are appended by the previous kernel
+
+    // Every wait is bounded; a role whose wait gives up raises the abort flag
+    // and leaves, and the others leave at their next wait or item.
+    if (warp == kMdProducerWarp) {
+        // ------------------------------ producer ------------------------------
+        if (elect_one()) {
+            const uint64_t pol = l2_policy_evict_first();  // every cached row is read once per iteration
+            uint32_t g = 0, issued = 0;
+            bool ok = true;
+            for (int q = blockIdx.x; q < total && ok; q += G) {
+                int i, c, h;
+                item(q, i, c, h);
+                const int t0 = c * a.p.chunk, t1 = min(a.p.req_ctx[i] + 1, t0 + a.p.chunk);
+                const int y0 = a.p.req_kvoff[i];
+                for (int t = t0; t < t1; t += kMdTok, ++g) {
+                    const int s = g % S;
+                    if (sm.abort || !mbar_wait_bounded(&sm.empty[s], ((g / S) & 1u) ^ 1u, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *dst = ring + s * kStage;
+                    mbar_arrive_expect_tx(&sm.full[s], kStage);
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        tma_load_3d_hint(dst + b * kBox, &tm, &sm.full[s], 64 * b, y0 + t, h, pol);
+                        tma_load_3d_hint(dst + (NB + b) * kBox, &tm, &sm.full[s], 64 * b, y0 + t, a.n_heads + h, pol);
+                    }
+                    ++issued;
+                }
+            }
+            if (!ok) {  // let the copies in flight land before the CTA exits
+                sm.abort = 1;
+                for (uint32_t j = issued > (uint32_t)S ? issued - S : 0; j < issued; ++j)
+                    mbar_wait_bounded(&sm.full[j % S], (j / S) & 1u, a.err);
+            }
+        }
+        return;
+    }
+
+    if (warp == kMdMergerWarp) {
+        // ---------------- merge: the consumer warps' states of each item ----------------
+        int k = 0;
+        for (int q = blockIdx.x; q < total; q += G, ++k) {
+            const int e = k % kMdMerge;
+            if (!__all_sync(0xffffffffu, !sm.abort && mbar_wait_bounded(&sm.mfull[e], (k / kMdMerge) & 1u, a.err))) {
+                sm.abort = 1;
+                return;
+            }
+            int i, c, h;
+            item(q, i, c, h);
+            float M = kNegBig;
+#pragma unroll
+            for (int w = 0; w < kMdConsumers; ++w) M = fmaxf(M, sm.m[e][w]);
+            float cw[kMdConsumers], L = 0.f;
+#pragma unroll
+            for (int w = 0; w < kMdConsumers; ++w) cw[w] = exp2f(sm.m[e][w] - M), L += sm.l[e][w] * cw[w];
+            float O[D / 32];
+#pragma unroll
+            for (int u = 0; u < D / 32; ++u) {
+                O[u] = 0.f;
+#pragma unroll
+                for (int w = 0; w < kMdConsumers; ++w) O[u] += sm.o[e][w][lane + 32 * u] * cw[w];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.mempty[e]);  // the entry is free again
+            const int nch = a.p.dec_nch[i];
+            bf16 *dst = a.out + (size_t)a.p.req_off[i] * a.H + h * D;
+            if (nch == 1) {
+                const float inv = 1.f / L;
+#pragma unroll
+                for (int u = 0; u < D / 32; ++u) dst[lane + 32 * u] = __float2bfloat16_rn(O[u] * inv);
+                continue;
+            }
+            // several chunks: publish the partial; the last to arrive merges them in chunk order
+            const int wb = a.p.dec_wbegin[i];
+            float *mine = a.part + ((size_t)(wb + c) * a.n_heads + h) * (D + 2);
+#pragma unroll
+            for (int u = 0; u < D / 32; ++u) mine[lane + 32 * u] = O[u];
+            if (lane == 0) mine[D] = M, mine[D + 1] = L;
+            __syncwarp();  // the warp's stores, then lane 0's release
+            int last = 0;
+            if (lane == 0) {
+                int *cnt = a.counters + i * a.n_heads + h;
+                last = atom_add_acq_rel(cnt, 1) == nch - 1;
+                if (last) *cnt = 0;
+            }
+            if (__shfl_sync(0xffffffffu, last, 0)) {
+                float Mt = kNegBig;
+                for (int j = 0; j < nch; ++j)
+                    Mt = fmaxf(Mt, __ldcg(a.part + ((size_t)(wb + j) * a.n_heads + h) * (D + 2) + D));
+                float Lt = 0.f, Ot[D / 32];
+#pragma unroll
+                for (int u = 0; u < D / 32; ++u) Ot[u] = 0.f;
+                for (int j = 0; j < nch; ++j) {
+                    const float *pj = a.part + ((size_t)(wb + j) * a.n_heads + h) * (D + 2);
+                    const float w = exp2f(__ldcg(pj + D) - Mt);
+                    Lt += __ldcg(pj + D + 1) * w;
+#pragma unroll
+                    for (int u = 0; u < D / 32; ++u) Ot[u] += __ldcg(pj + lane + 32 * u) * w;
+                }
+#pragma unroll
+                for (int u = 0; u < D / 32; ++u) dst[lane + 32 * u] = __float2bfloat16_rn(Ot[u] / Lt);
+            }
+        }
+        return;
+    }
+
+    // -------------------------------- consumers --------------------------------
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int j0 = 16 * warp;  // this warp's 16 tokens of every stage
+    // q as the B operand (any column): b0 = dims 16ks + 2t4, +1; b1 = dims 16ks + 8 + 2t4, +1
+    auto load_q = [&](int q, uint32_t (*qb)[2]) {
+        int i, c, h;
+        item(q, i, c, h);
+        const uint32_t *qp = reinterpret_cast<const uint32_t *>(a.qkv + (size_t)a.p.req_off[i] * 3 * a.H + h * D);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qp[8 * ks + t4], qb[ks][1] = qp[8 * ks + 4 + t4];
+    };
+    uint32_t qn[KS][2];
+    if (blockIdx.x < total) load_q(blockIdx.x, qn);
+    uint32_t g = 0;
+    int k = 0;
+    for (int q = blockIdx.x; q < total; q += G, ++k) {
+        int i, c, h;
+        item(q, i, c, h);
+        const int t0 = c * a.p.chunk, t1 = min(a.p.req_ctx[i] + 1, t0 + a.p.chunk);
+        uint32_t qb[KS][2];
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qn[ks][0], qb[ks][1] = qn[ks][1];
+        if (q + G < total) load_q(q + G, qn);  // the next item's q, in flight during this one
+        float m = kNegBig, l = 0.f, o[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        for (int t = t0; t < t1; t += kMdTok, ++g) {
+            const int s = g % S;
+            if (!__all_sync(0xffffffffu, !sm.abort && mbar_wait_bounded(&sm.full[s], (g / S) & 1u, a.err))) {
+                sm.abort = 1;  // (uniform: ldmatrix and mma below are warp-wide)
+                return;
+            }
+            const uint32_t kb = smem_u32(ring + s * kStage), vb = kb + NB * kBox;
+            const int ntok = min(kMdTok, t1 - t);
+            if (j0 < ntok) {
+                // S^T = K q^T for tokens j0 .. j0 + 15: lane (g8, t4) gets tokens j0 + g8 and j0 + g8 + 8
+                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+                {
+                    const int r = j0 + ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const int d = 16 * ks + (lane >> 4) * 8;
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(kb + (d >> 6) * kBox + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4), a0, a1, a2, a3);
+                        mma_bf16((ks & 1) ? c1 : c0, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                    }
+                }
+                const float s_lo = j0 + g8 < ntok ? (c0[0] + c1[0]) * a.scale_log2 : kNegBig;
+                const float s_hi = j0 + g8 + 8 < ntok ? (c0[2] + c1[2]) * a.scale_log2 : kNegBig;
+                float mx = fmaxf(s_lo, s_hi);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                if (mx > m) {  // warp-uniform
+                    const float corr = exp2f(m - mx);
+                    m = mx;
+                    l *= corr;
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+                        o[mt][0] *= corr, o[mt][1] *= corr, o[mt][2] *= corr, o[mt][3] *= corr;
+                }
+                const uint32_t pw = pack_bf16(exp2f(s_lo - m), exp2f(s_hi - m));  // {p(j0 + g8), p(j0 + g8 + 8)}
+                {
+                    const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&pw);
+                    l += __low2float(pr) + __high2float(pr);
+                }
+                if (ntok < j0 + 16) {  // rows past the item may hold anything: zero this warp's in V
+                    for (int idx = lane; idx < (j0 + 16 - ntok) * NB * 8; idx += 32) {
+                        const int rr = ntok + idx / (NB * 8), b = (idx / 8) % NB, ch = idx % 8;
+                        st_shared_zero16(vb + b * kBox + rr * 128 + ch * 16);
+                    }
+                    fence_proxy_async_smem();  // before the slot's next TMA write
+                    __syncwarp();
+                }
+                // O^T += V^T p; B = p as a column: b0 = p(2t4), p(2t4 + 1); b1 = p(2t4 + 8), p(2t4 + 9)
+                const uint32_t x0 = __shfl_sync(0xffffffffu, pw, 8 * t4);
+                const uint32_t x1 = __shfl_sync(0xffffffffu, pw, 8 * t4 + 4);
+                const uint32_t b0 = prmt(x0, x1, 0x5410), b1 = prmt(x0, x1, 0x7632);
+                const int r = j0 + (lane >> 4) * 8 + (lane & 7);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int d = 16 * mt + ((lane >> 3) & 1) * 8;
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(vb + (d >> 6) * kBox + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4), a0, a1, a2, a3);
+                    mma_bf16(o[mt], a0, a1, a2, a3, b0, b1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);  // this warp is done with slot s
+        }
+        // hand the item's state to the merge warp: l over the 8 token groups; lane (g8, t4) holds
+        // o[mt][0] = dim 16mt + g8 and o[mt][2] = dim 16mt + g8 + 8
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        const int e = k % kMdMerge;
+        if (k >= kMdMerge &&
+            !__all_sync(0xffffffffu, !sm.abort && mbar_wait_bounded(&sm.mempty[e], ((k / kMdMerge) - 1) & 1u, a.err))) {
+            sm.abort = 1;
+            return;
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+            if ((mt & 3) == t4) sm.o[e][warp][16 * mt + g8] = o[mt][0], sm.o[e][warp][16 * mt + g8 + 8] = o[mt][2];
+        if (lane == 0) sm.m[e][warp] = m, sm.l[e][warp] = l;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.mfull[e]);
+    }
+}
+
 template <typename T, int D>
 cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStream_t st) {
+    if constexpr (std::is_same<T, bf16>::value && D % 64 == 0)
+        if (decode && a.p.n_dec_work > 0) {
+            static bool attr = false;
+            if (!attr) {
+                cudaError_t e = cudaFuncSetAttribute(attn_decode_mma_kernel<D>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     (int)md_smem_bytes<D>());
+                if (e != cudaSuccess) return e;
+                attr = true;
+            }
+            // the layer's pool as [K|V][head] planes of [slot][D]
+            CUtensorMap tm;
+            const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.kv_slots, (uint64_t)2 * a.n_heads};
+            const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)a.kv_slots * D * 2};
+            const uint32_t box[3] = {64, kMdTok, 1};
+            if (a.kv_slots > INT32_MAX || (reinterpret_cast<uintptr_t>(a.kpool) & 15) ||
+                !encode_tensor_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.kpool, dims, strides, box,
+                                   CU_TENSOR_MAP_SWIZZLE_128B))
+                return cudaErrorInvalidValue;
+            int sms = 0, dev = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            const int total = a.p.n_dec_work * a.n_heads;
+            const int grid = std::max(1, std::min(total, kMdCtasPerSm * sms));
+            cudaError_t e = launch_pdl(attn_decode_mma_kernel<D>, dim3(grid), dim3(kMdThreads), md_smem_bytes<D>(), st,
+                                       tm, a);
+            if (e != cudaSuccess) return e;
+            decode = false;
+        }
     if (decode && a.p.n_dec_work > 0) {
         static bool attr = false;
         if (!attr) {
@@ -677,6 +1022,10 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
 }  // namespace
 
 void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_ctx, int chunk, int32_t *order) {
+    if (chunk < 1 || chunk > 512) {  // (the engine's chunks are 64 .. 512) keep the given order
+        for (int w = 0; w < n_work; ++w) order[w] = w;
+        return;
+    }
     // counting sort of the work items by keys in the chunk (1 .. chunk <= 512), longest first
     int start[513 + 1] = {0};
     auto keys = [&](int w) {

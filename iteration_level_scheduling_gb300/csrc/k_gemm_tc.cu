@@ -390,15 +390,11 @@ EncodeTiledFn encode_fn() {
 
 // 2-D bf16 map over a row-major [rows, k] matrix, box = 64 (k) x box_rows, 128B swizzle.
 bool make_map(CUtensorMap *m, const void *ptr, int rows, int k, int box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)k * 2};
-    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const uint64_t dims[2] = {(uint64_t)k, (uint64_t)rows};
+    const uint64_t strides[1] = {(uint64_t)k * 2};
+    const uint32_t box[2] = {(uint32_t)BK, (uint32_t)box_rows};
+    return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -418,6 +414,22 @@ int override_stages() {
 }
 
 }  // namespace
+
+bool encode_tensor_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t rank, const void *base, const uint64_t *dims,
+                       const uint64_t *strides, const uint32_t *box, CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t bx[5], estr[5];
+    for (uint32_t r = 0; r < rank; ++r) {
+        d[r] = dims[r];
+        bx[r] = box[r];
+        estr[r] = 1;
+        if (r + 1 < rank) st[r] = strides[r];
+    }
+    return fn(m, dt, rank, const_cast<void *>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool allow_partial, size_t part_cap) {
     TcShape t{};

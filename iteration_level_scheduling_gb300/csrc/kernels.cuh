@@ -1,6 +1,7 @@
 // Host-side launchers of the device kernels (internal to liborca).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -58,6 +59,11 @@ struct TcShape {
 };
 TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool allow_partial = false,
                       size_t part_cap = 0);
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point;
+// dims/strides/box innermost first (strides in bytes, rank - 1 of them).
+bool encode_tensor_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t rank, const void *base, const uint64_t *dims,
+                       const uint64_t *strides, const uint32_t *box, CUtensorMapSwizzle swizzle);
 
 // SIMT FFMA GEMM, fp32 operands.
 cudaError_t gemm_simt_f32(const float *x, const float *w, int m_tok, int n_out, int k, const Epilogue &e,

@@ -41,6 +41,7 @@ def rel(a, ref):
 SHAPES = [
     (1, 128, 64), (16, 256, 128), (5, 130, 64), (64, 384, 1024), (100, 200, 512), (64, 5120, 1024),
     (300, 640, 256), (477, 1024, 1024), (600, 1280, 320), (1000, 384, 128), (2048, 512, 64), (64, 128, 20480),
+    (16, 128, 64), (33, 15360, 128), (256, 2560, 5120),
 ]
 
 
