@@ -265,7 +265,7 @@ int orca_op_attention(orca_engine *eng, int32_t dtype, const void *qkv, const vo
  * the same split-K decode kernel as orca_op_attention for requests that have
  * exactly one input row each (increment phase), with the kernel's scratch
  * (plan tables, per-(request, head) arrival counters, split-K partials) in a
- * fixed device array of about 16.2 MiB inside this library.  Every GPU that loads the
+ * fixed device array of about 16.5 MiB inside this library.  Every GPU that loads the
  * library holds that array until the process exits.
  *   qkv [n_req, 3*hidden], kv_layer [K|V][n_heads][kv_slots][head_dim],
  *   out [n_req, hidden]: device pointers, owned by the caller.

@@ -59,6 +59,7 @@ enum : int {
     P_PREPAIRS_HI,  // sum over prefill rows of (pos + 1), split in two words
     P_PREPAIRS_LO,
     P_DECORDER,  // decode work items, longest first
+    P_DECITEM,   // their 8-word records (AttnPlan::dec_items)
 };
 
 struct KRec {
@@ -149,7 +150,7 @@ namespace {
 // Sizes of one plan; the same function drives both orca_plan_words and the build.
 struct Layout {
     int B, R, n_dec, n_pre, n_dec_work, n_pre_tiles, chunk;
-    int64_t off[P_DECORDER + 1];
+    int64_t off[P_DECITEM + 1];
 };
 
 int decode_chunk(const orca_engine *E, const orca_batch *b) {
@@ -210,6 +211,7 @@ int layout(const orca_engine *E, const orca_batch *b, Layout *lay) {
     put(P_DECNCH, B);
     put(P_DECWORK, 2 * (int64_t)work);
     put(P_DECORDER, work);
+    put(P_DECITEM, 8 * (int64_t)work);
     put(P_PRETILES, 2 * (int64_t)tiles);
     put(P_LASTROW, B);
     lay->off[P_TOTAL] = w;
@@ -274,6 +276,8 @@ int build(orca_engine *E, const orca_batch *b, int32_t *buf, int64_t cap) {
     }
     req_off[B] = r;
     decode_order(dec_work, lay.n_dec_work, req_ctx, lay.chunk, buf + lay.off[P_DECORDER]);
+    decode_items(buf + lay.off[P_DECORDER], dec_work, lay.n_dec_work, req_off, req_ctx, req_kv, dec_wb, dec_nch,
+                 lay.chunk, buf + lay.off[P_DECITEM]);
     buf[P_MAGIC] = kPlanMagic;
     buf[P_NREQ] = B;
     buf[P_NROWS] = lay.R;
@@ -289,6 +293,7 @@ int build(orca_engine *E, const orca_batch *b, int32_t *buf, int64_t cap) {
     buf[P_PREPAIRS_HI] = (int32_t)(pre_pairs >> 31);
     buf[P_PREPAIRS_LO] = (int32_t)(pre_pairs & 0x7FFFFFFF);
     buf[P_DECORDER] = (int32_t)lay.off[P_DECORDER];
+    buf[P_DECITEM] = (int32_t)lay.off[P_DECITEM];
     E->built_prev_n = B;
     return ORCA_OK;
 }
@@ -319,6 +324,7 @@ int run_plan(orca_engine *E, const int32_t *hp, const int32_t *dp, int32_t *dev_
     ap.dec_wbegin = dp + hp[P_DECWB];
     ap.dec_nch = dp + hp[P_DECNCH];
     ap.dec_order = dp + hp[P_DECORDER];
+    ap.dec_items = dp + hp[P_DECITEM];
     ap.pre_tiles = dp + hp[P_PRETILES];
     ap.n_dec_work = hp[P_NDECWORK];
     ap.n_pre_tiles = hp[P_NPRETILES];
@@ -522,7 +528,7 @@ int orca_engine_create(const orca_model_config *cfg, const orca_weights *w, void
     const size_t R = c.max_tokens, B = c.max_batch, H = c.hidden, F = c.ffn, es = E->es;
     // decode split-K work items: at most one per 64 keys of every request
     E->attn_part_work = (int64_t)B * ceil_div(c.max_pos, 64);
-    E->plan_cap = kHdr + 64 + 8 * (int64_t)B + 3 * (int64_t)R + 3 * E->attn_part_work + 2 * ((int64_t)R / 16 + B);
+    E->plan_cap = kHdr + 64 + 8 * (int64_t)B + 3 * (int64_t)R + 11 * E->attn_part_work + 2 * ((int64_t)R / 16 + B);
     E->gs.num_sms = E->num_sms;
     // up to 8 partial slabs of up to 512 rows (split-K is only chosen when the rows are few)
     E->part_cap = E->bf ? (size_t)8 * std::min<size_t>(R, 512) * H : 0;
@@ -814,6 +820,8 @@ int orca_op_attention(orca_engine *E, int32_t dtype, const void *qkv, const void
     }
     req_off[n_req] = r;
     decode_order(dec_work, lay.n_dec_work, req_ctx, lay.chunk, buf + lay.off[P_DECORDER]);
+    decode_items(buf + lay.off[P_DECORDER], dec_work, lay.n_dec_work, req_off, req_ctx, req_kv, dec_wb, dec_nch,
+                 lay.chunk, buf + lay.off[P_DECITEM]);
     if (cudaMemcpyAsync(E->d_plan, E->h_plan, (size_t)lay.off[P_TOTAL] * 4, cudaMemcpyHostToDevice, E->st) !=
         cudaSuccess) {
         cudaGetLastError();
@@ -828,6 +836,7 @@ int orca_op_attention(orca_engine *E, int32_t dtype, const void *qkv, const void
     ap.dec_wbegin = dp + lay.off[P_DECWB];
     ap.dec_nch = dp + lay.off[P_DECNCH];
     ap.dec_order = dp + lay.off[P_DECORDER];
+    ap.dec_items = dp + lay.off[P_DECITEM];
     ap.pre_tiles = dp + lay.off[P_PRETILES];
     ap.n_dec_work = lay.n_dec_work;
     ap.n_pre_tiles = lay.n_pre_tiles;

@@ -646,8 +646,10 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const AttnArgs<bf
 //   O^T += V^T p   A = a 16-dim x 16-token V^T tile (ldmatrix.trans), B = p
 // Every column of B holds the same vector, so every column of each 16 x 8
 // result holds the answer.  p enters the MMA rounded to bf16 and l sums those
-// rounded weights.  Rows past an item's end in its last stage are masked out
-// of the scores and zeroed in V (they may belong to another request).
+// rounded weights.  An item's last stage is loaded in boxes of 16 tokens (a
+// second tensor map), so at most 15 keys past its end are read; rows past the
+// end are masked out of the scores and zeroed in V (they may belong to
+// another request, or be stale).
 // ---------------------------------------------------------------------------
 constexpr int kMdTok = 64;
 constexpr int kMdConsumers = kMdTok / 16;
@@ -693,6 +695,7 @@ __device__ __forceinline__ int atom_add_acq_rel(int *p, int v) {
 
 template <int D>
 __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm,
+                                                                     const __grid_constant__ CUtensorMap tm16,
                                                                      const AttnArgs<bf16> a) {
     constexpr int NB = D / 64;  // 64-dim boxes per row
     constexpr int KS = D / 16;  // k-steps of the scores
@@ -709,12 +712,16 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
     const int total = a.p.n_dec_work * a.n_heads;
     const int G = gridDim.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    auto item = [&](int q, int &i, int &c, int &h) {
-        const int w = a.p.dec_order[q / a.n_heads];
-        h = q % a.n_heads;
-        i = a.p.dec_work[2 * w];
-        c = a.p.dec_work[2 * w + 1];
+    // entry q = (sorted work item q / n_heads, head q % n_heads): {kv slot of the first key,
+    // keys, first row, request} and {chunk, the request's chunks, its first work item, first key}
+    auto rec = [&](int q, int4 &r0, int4 &r1) {
+        const int4 *r = reinterpret_cast<const int4 *>(a.p.dec_items) + 2 * (q / a.n_heads);
+        r0 = r[0], r1 = r[1];
     };
+    // This CTA's k-th entry of the (longest-first) list: rounds of G entries,
+    // dealt forwards and backwards in turn so that every CTA's share of the
+    // large and the small items evens out.  Past the list once >= total.
+    auto nth = [&](int k) { return k * G + ((k & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x); };
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&sm.full[s], 1);
@@ -727,6 +734,7 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
         sm.abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tm);
+        prefetch_tmap(&tm16);
     }
     __syncthreads();
     pdl_wait();  // this iteration's K/V rows are appended by the previous kernel
@@ -739,23 +747,39 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
             const uint64_t pol = l2_policy_evict_first();  // every cached row is read once per iteration
             uint32_t g = 0, issued = 0;
             bool ok = true;
-            for (int q = blockIdx.x; q < total && ok; q += G) {
-                int i, c, h;
-                item(q, i, c, h);
-                const int t0 = c * a.p.chunk, t1 = min(a.p.req_ctx[i] + 1, t0 + a.p.chunk);
-                const int y0 = a.p.req_kvoff[i];
-                for (int t = t0; t < t1; t += kMdTok, ++g) {
+            int4 r0, r1, n0, n1;
+            if (nth(0) < total) rec(nth(0), n0, n1);
+            for (int k = 0, q = nth(0); q < total && ok; q = nth(++k)) {
+                r0 = n0;
+                if (nth(k + 1) < total) rec(nth(k + 1), n0, n1);  // the next record, in flight meanwhile
+                const int h = q % a.n_heads, y0 = r0.x, nk = r0.y;
+                for (int t = 0; t < nk; t += kMdTok, ++g) {
                     const int s = g % S;
                     if (sm.abort || !mbar_wait_bounded(&sm.empty[s], ((g / S) & 1u) ^ 1u, a.err)) {
                         ok = false;
                         break;
                     }
                     uint8_t *dst = ring + s * kStage;
-                    mbar_arrive_expect_tx(&sm.full[s], kStage);
+                    const int ntok = min(kMdTok, nk - t);
+                    if (ntok == kMdTok) {
+                        mbar_arrive_expect_tx(&sm.full[s], kStage);
 #pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        tma_load_3d_hint(dst + b * kBox, &tm, &sm.full[s], 64 * b, y0 + t, h, pol);
-                        tma_load_3d_hint(dst + (NB + b) * kBox, &tm, &sm.full[s], 64 * b, y0 + t, a.n_heads + h, pol);
+                        for (int b = 0; b < NB; ++b) {
+                            tma_load_3d_hint(dst + b * kBox, &tm, &sm.full[s], 64 * b, y0 + t, h, pol);
+                            tma_load_3d_hint(dst + (NB + b) * kBox, &tm, &sm.full[s], 64 * b, y0 + t, a.n_heads + h,
+                                             pol);
+                        }
+                    } else {  // 16-token boxes at 2 KiB (16-row) offsets keep the 128-byte swizzle phase
+                        const int nq = (ntok + 15) / 16;
+                        mbar_arrive_expect_tx(&sm.full[s], (uint32_t)nq * (kStage / 4));
+                        for (int j = 0; j < nq; ++j)
+#pragma unroll
+                            for (int b = 0; b < NB; ++b) {
+                                tma_load_3d_hint(dst + b * kBox + j * 2048, &tm16, &sm.full[s], 64 * b, y0 + t + 16 * j,
+                                                 h, pol);
+                                tma_load_3d_hint(dst + (NB + b) * kBox + j * 2048, &tm16, &sm.full[s], 64 * b,
+                                                 y0 + t + 16 * j, a.n_heads + h, pol);
+                            }
                     }
                     ++issued;
                 }
@@ -771,15 +795,15 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
 
     if (warp == kMdMergerWarp) {
         // ---------------- merge: the consumer warps' states of each item ----------------
-        int k = 0;
-        for (int q = blockIdx.x; q < total; q += G, ++k) {
+        for (int k = 0, q = nth(0); q < total; q = nth(++k)) {
             const int e = k % kMdMerge;
             if (!__all_sync(0xffffffffu, !sm.abort && mbar_wait_bounded(&sm.mfull[e], (k / kMdMerge) & 1u, a.err))) {
                 sm.abort = 1;
                 return;
             }
-            int i, c, h;
-            item(q, i, c, h);
+            int4 r0, r1;
+            rec(q, r0, r1);
+            const int h = q % a.n_heads, i = r0.w, c = r1.x;
             float M = kNegBig;
 #pragma unroll
             for (int w = 0; w < kMdConsumers; ++w) M = fmaxf(M, sm.m[e][w]);
@@ -795,8 +819,8 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.mempty[e]);  // the entry is free again
-            const int nch = a.p.dec_nch[i];
-            bf16 *dst = a.out + (size_t)a.p.req_off[i] * a.H + h * D;
+            const int nch = r1.y;
+            bf16 *dst = a.out + (size_t)r0.z * a.H + h * D;
             if (nch == 1) {
                 const float inv = 1.f / L;
 #pragma unroll
@@ -804,7 +828,7 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
                 continue;
             }
             // several chunks: publish the partial; the last to arrive merges them in chunk order
-            const int wb = a.p.dec_wbegin[i];
+            const int wb = r1.z;
             float *mine = a.part + ((size_t)(wb + c) * a.n_heads + h) * (D + 2);
 #pragma unroll
             for (int u = 0; u < D / 32; ++u) mine[lane + 32 * u] = O[u];
@@ -842,24 +866,24 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
     const int j0 = 16 * warp;  // this warp's 16 tokens of every stage
     // q as the B operand (any column): b0 = dims 16ks + 2t4, +1; b1 = dims 16ks + 8 + 2t4, +1
     auto load_q = [&](int q, uint32_t (*qb)[2]) {
-        int i, c, h;
-        item(q, i, c, h);
-        const uint32_t *qp = reinterpret_cast<const uint32_t *>(a.qkv + (size_t)a.p.req_off[i] * 3 * a.H + h * D);
+        int4 r0, r1;
+        rec(q, r0, r1);
+        const uint32_t *qp =
+            reinterpret_cast<const uint32_t *>(a.qkv + (size_t)r0.z * 3 * a.H + (q % a.n_heads) * D);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qp[8 * ks + t4], qb[ks][1] = qp[8 * ks + 4 + t4];
     };
     uint32_t qn[KS][2];
-    if (blockIdx.x < total) load_q(blockIdx.x, qn);
+    if (nth(0) < total) load_q(nth(0), qn);
     uint32_t g = 0;
-    int k = 0;
-    for (int q = blockIdx.x; q < total; q += G, ++k) {
-        int i, c, h;
-        item(q, i, c, h);
-        const int t0 = c * a.p.chunk, t1 = min(a.p.req_ctx[i] + 1, t0 + a.p.chunk);
+    for (int k = 0, q = nth(0); q < total; q = nth(++k)) {
+        int4 r0, r1;
+        rec(q, r0, r1);
+        const int t0 = 0, t1 = r0.y;  // keys of this item, from its first
         uint32_t qb[KS][2];
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qn[ks][0], qb[ks][1] = qn[ks][1];
-        if (q + G < total) load_q(q + G, qn);  // the next item's q, in flight during this one
+        if (nth(k + 1) < total) load_q(nth(k + 1), qn);  // the next item's q, in flight during this one
         float m = kNegBig, l = 0.f, o[MT][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -960,12 +984,14 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
                 attr = true;
             }
             // the layer's pool as [K|V][head] planes of [slot][D]
-            CUtensorMap tm;
+            CUtensorMap tm, tm16;
             const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.kv_slots, (uint64_t)2 * a.n_heads};
             const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)a.kv_slots * D * 2};
-            const uint32_t box[3] = {64, kMdTok, 1};
+            const uint32_t box[3] = {64, kMdTok, 1}, box16[3] = {64, 16, 1};
             if (a.kv_slots > INT32_MAX || (reinterpret_cast<uintptr_t>(a.kpool) & 15) ||
                 !encode_tensor_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.kpool, dims, strides, box,
+                                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+                !encode_tensor_map(&tm16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.kpool, dims, strides, box16,
                                    CU_TENSOR_MAP_SWIZZLE_128B))
                 return cudaErrorInvalidValue;
             int sms = 0, dev = 0;
@@ -974,7 +1000,7 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
             const int total = a.p.n_dec_work * a.n_heads;
             const int grid = std::max(1, std::min(total, kMdCtasPerSm * sms));
             cudaError_t e = launch_pdl(attn_decode_mma_kernel<D>, dim3(grid), dim3(kMdThreads), md_smem_bytes<D>(), st,
-                                       tm, a);
+                                       tm, tm16, a);
             if (e != cudaSuccess) return e;
             decode = false;
         }
@@ -1037,6 +1063,18 @@ void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_ctx, i
     for (int w = 0; w < n_work; ++w) order[start[chunk - keys(w)]++] = w;
 }
 
+void decode_items(const int32_t *order, const int32_t *dec_work, int n_work, const int32_t *req_off,
+                  const int32_t *req_ctx, const int32_t *req_kvoff, const int32_t *dec_wbegin, const int32_t *dec_nch,
+                  int chunk, int32_t *items) {
+    for (int k = 0; k < n_work; ++k) {
+        const int w = order[k], i = dec_work[2 * w], c = dec_work[2 * w + 1];
+        const int t0 = c * chunk, t1 = std::min(req_ctx[i] + 1, t0 + chunk);
+        int32_t *r = items + 8 * (size_t)k;
+        r[0] = req_kvoff[i] + t0, r[1] = t1 - t0, r[2] = req_off[i], r[3] = i;
+        r[4] = c, r[5] = dec_nch[i], r[6] = dec_wbegin[i], r[7] = t0;
+    }
+}
+
 template <typename T>
 cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *out, const AttnPlan &p, int H,
                       int n_heads, float *part, int *counters, unsigned *err, cudaStream_t st, bool decode,
@@ -1078,7 +1116,7 @@ constexpr int kNaMaxReq = 256;
 constexpr int kNaMaxHeads = 128;
 constexpr size_t kNaPartFloats = size_t(1) << 22;                    // 16 MiB of partials
 constexpr size_t kNaCounterWords = size_t(kNaMaxReq) * kNaMaxHeads;  // 128 KiB
-constexpr size_t kNaPlanWords = 8 * kNaMaxReq + 3 * 8192;            // tables + up to 8192 work items
+constexpr size_t kNaPlanWords = 8 * kNaMaxReq + 11 * 8192 + 16;      // tables + up to 8192 work items
 constexpr size_t kNaScratchBytes = 4 * (kNaPartFloats + kNaCounterWords + kNaPlanWords);
 constexpr int kNaMaxDevices = 64;
 
@@ -1139,7 +1177,8 @@ extern "C" int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, con
     }
     int64_t n_work = 0;
     for (int i = 0; i < n_req; ++i) n_work += ((int64_t)ctx_len[i] + chunk) / chunk;
-    const size_t words = 6 * (size_t)n_req + 1 + 3 * (size_t)n_work;
+    const size_t items_at = (6 * (size_t)n_req + 1 + 3 * (size_t)n_work + 3) & ~size_t(3);  // 16-byte aligned
+    const size_t words = items_at + 8 * (size_t)n_work;
     if (words > kNaPlanWords || (size_t)n_work * n_heads * (head_dim + 2) > kNaPartFloats) return kLimit;
 
     // tables: req_off, req_ctx, req_kvoff, dec_wbegin, dec_nch, dec_work
@@ -1158,6 +1197,7 @@ extern "C" int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, con
     }
     req_off[n_req] = n_req;
     decode_order(dec_work, (int)n_work, req_ctx, chunk, dec_ord);
+    decode_items(dec_ord, dec_work, (int)n_work, req_off, req_ctx, req_kv, dec_wb, dec_nch, chunk, g_na_plan + items_at);
 
     float *part = reinterpret_cast<float *>(nd.scratch);
     int32_t *counters = reinterpret_cast<int32_t *>(part + kNaPartFloats);
@@ -1176,6 +1216,7 @@ extern "C" int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, con
     ap.dec_nch = plan + (dec_nch - g_na_plan);
     ap.dec_work = plan + (dec_work - g_na_plan);
     ap.dec_order = plan + (dec_ord - g_na_plan);
+    ap.dec_items = plan + items_at;
     ap.pre_tiles = nullptr;
     ap.n_dec_work = (int)n_work;
     ap.n_pre_tiles = 0;

@@ -94,6 +94,9 @@ struct AttnPlan {
     const int32_t *req_off, *req_ctx, *req_kvoff;
     const int32_t *dec_work, *dec_wbegin, *dec_nch;  // decode split-K work items
     const int32_t *dec_order;                        // work items, longest first
+    // per entry of dec_order, 8 words (16-byte aligned): kv_offset + first key,
+    // keys, first row, request, chunk, the request's chunks, its first work item, first key
+    const int32_t *dec_items;
     const int32_t *pre_tiles;                        // prefill (request, first row) tiles
     int n_dec_work, n_pre_tiles, chunk;
 };
@@ -108,6 +111,10 @@ cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *ou
 // Order of the decode work items (request, chunk) by number of keys, longest
 // first (stable), for the persistent decode kernel's load balance.
 void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_ctx, int chunk, int32_t *order);
+// The 8-word records of AttnPlan::dec_items, in the order of `order`.
+void decode_items(const int32_t *order, const int32_t *dec_work, int n_work, const int32_t *req_off,
+                  const int32_t *req_ctx, const int32_t *req_kvoff, const int32_t *dec_wbegin, const int32_t *dec_nch,
+                  int chunk, int32_t *items);
 
 // next[b] = argmax_j logits[b, j] (lowest j on ties); also to out2 if non-null.
 cudaError_t argmax_rows(const float *logits, int n_rows, int V, int32_t *next, int32_t *out2, cudaStream_t st);
