@@ -653,8 +653,9 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const AttnArgs<bf
 // ---------------------------------------------------------------------------
 constexpr int kMdTok = 64;
 constexpr int kMdConsumers = kMdTok / 16;
+constexpr int kMdMergers = 2;  // merge warps, taking the items in turn
 constexpr int kMdProducerWarp = kMdConsumers, kMdMergerWarp = kMdConsumers + 1;
-constexpr int kMdThreads = 32 * (kMdConsumers + 2);
+constexpr int kMdThreads = 32 * (kMdConsumers + 1 + kMdMergers);
 constexpr int kMdCtasPerSm = 2;
 constexpr int kMdMerge = 4;  // item results queued for the merge warp
 
@@ -793,9 +794,10 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
         return;
     }
 
-    if (warp == kMdMergerWarp) {
+    if (warp >= kMdMergerWarp) {
         // ---------------- merge: the consumer warps' states of each item ----------------
-        for (int k = 0, q = nth(0); q < total; q = nth(++k)) {
+        const int mw = warp - kMdMergerWarp;  // items k = mw, mw + kMdMergers, ...
+        for (int k = mw, q = nth(mw); q < total; k += kMdMergers, q = nth(k)) {
             const int e = k % kMdMerge;
             if (!__all_sync(0xffffffffu, !sm.abort && mbar_wait_bounded(&sm.mfull[e], (k / kMdMerge) & 1u, a.err))) {
                 sm.abort = 1;
@@ -841,18 +843,30 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
                 if (last) *cnt = 0;
             }
             if (__shfl_sync(0xffffffffu, last, 0)) {
-                float Mt = kNegBig;
-                for (int j = 0; j < nch; ++j)
-                    Mt = fmaxf(Mt, __ldcg(a.part + ((size_t)(wb + j) * a.n_heads + h) * (D + 2) + D));
-                float Lt = 0.f, Ot[D / 32];
+                // chunks in order, up to 4 at a time with every load in flight before the first use
+                float Mt = kNegBig, Lt = 0.f, Ot[D / 32];
 #pragma unroll
                 for (int u = 0; u < D / 32; ++u) Ot[u] = 0.f;
-                for (int j = 0; j < nch; ++j) {
-                    const float *pj = a.part + ((size_t)(wb + j) * a.n_heads + h) * (D + 2);
-                    const float w = exp2f(__ldcg(pj + D) - Mt);
-                    Lt += __ldcg(pj + D + 1) * w;
+                for (int j0 = 0; j0 < nch; j0 += 4) {
+                    float pm[4], pl[4], po[4][D / 32];
 #pragma unroll
-                    for (int u = 0; u < D / 32; ++u) Ot[u] += __ldcg(pj + lane + 32 * u) * w;
+                    for (int jj = 0; jj < 4; ++jj)
+                        if (j0 + jj < nch) {
+                            const float *pj = a.part + ((size_t)(wb + j0 + jj) * a.n_heads + h) * (D + 2);
+                            pm[jj] = __ldcg(pj + D), pl[jj] = __ldcg(pj + D + 1);
+#pragma unroll
+                            for (int u = 0; u < D / 32; ++u) po[jj][u] = __ldcg(pj + lane + 32 * u);
+                        }
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        if (j0 + jj < nch) {  // online merge: rescale the running sums to the new maximum
+                            const float mn = fmaxf(Mt, pm[jj]);
+                            const float c_old = exp2f(Mt - mn), c_new = exp2f(pm[jj] - mn);
+                            Lt = Lt * c_old + pl[jj] * c_new;
+#pragma unroll
+                            for (int u = 0; u < D / 32; ++u) Ot[u] = Ot[u] * c_old + po[jj][u] * c_new;
+                            Mt = mn;
+                        }
                 }
 #pragma unroll
                 for (int u = 0; u < D / 32; ++u) dst[lane + 32 * u] = __float2bfloat16_rn(Ot[u] / Lt);
