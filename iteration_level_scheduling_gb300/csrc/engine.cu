@@ -457,6 +457,8 @@ int check_flag(orca_engine *E) {
     if (*E->h_err == 0) return ORCA_OK;
     *E->h_err = 0;
     cudaMemsetAsync(E->d_err, 0, sizeof(unsigned), E->st);
+    // a kernel that gave up may have left split-request arrival counters part-way
+    cudaMemsetAsync(E->attn_cnt, 0, (size_t)E->cfg.max_batch * E->cfg.n_heads * 4, E->st);
     cudaStreamSynchronize(E->st);
     return ORCA_ERR_DEVICE_FLAG;
 }
