@@ -59,8 +59,8 @@ __global__ void __launch_bounds__(kRowThreads) embed_kernel(const int32_t *token
     }
 }
 
-constexpr int kLnThreads = 256;
-constexpr int kLnMaxVec = 8;  // H <= kLnThreads * 4 * kLnMaxVec = 8192
+constexpr int kLnThreads = 1024;
+constexpr int kLnMaxVec = 2;  // H <= kLnThreads * 4 * kLnMaxVec = 8192
 
 __device__ __forceinline__ float block_sum(float v, float *red) {
     v = warp_sum(v);
@@ -107,29 +107,45 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(float *x, const i
     const int r = blockIdx.x;
     const int src = row_map ? row_map[r] : r;
     float *xr = x + (size_t)src * H;
+    // every load of the row (and of its split-K partials and bias) is issued
+    // before the first use
+    constexpr int kInline = 4;  // partial slabs loaded up front (the engine splits K at most 3 ways here)
+    float4 q[kLnMaxVec], bias[kLnMaxVec], pv[kLnMaxVec][kInline];
+#pragma unroll
+    for (int i = 0; i < kLnMaxVec; ++i) {
+        const int e = (threadIdx.x + i * kLnThreads) * 4;
+        if (e < H) {
+            q[i] = *reinterpret_cast<const float4 *>(xr + e);
+            if (n_part > 0) {
+                bias[i] = add_bias ? *reinterpret_cast<const float4 *>(add_bias + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int sp = 0; sp < kInline; ++sp)
+                    if (sp < n_part)
+                        pv[i][sp] = *reinterpret_cast<const float4 *>(part + ((size_t)sp * part_rows + src) * H + e);
+            }
+        }
+    }
     float v[kLnMaxVec][4];
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < kLnMaxVec; ++i) {
-        int e = (threadIdx.x + i * kLnThreads) * 4;
+        const int e = (threadIdx.x + i * kLnThreads) * 4;
         if (e < H) {
-            float4 q = *reinterpret_cast<const float4 *>(xr + e);
             if (n_part > 0) {
-                // complete the residual row: x + (bias + the split-K partials, in split
-                // order); all partial loads are issued before the first add
-                float4 acc = add_bias ? *reinterpret_cast<const float4 *>(add_bias + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-                float4 pv[8];
+                // complete the residual row: x + (bias + the split-K partials, in split order)
+                float4 acc = bias[i];
 #pragma unroll
-                for (int sp = 0; sp < 8; ++sp)
-                    if (sp < n_part) pv[sp] = *reinterpret_cast<const float4 *>(part + ((size_t)sp * part_rows + src) * H + e);
-#pragma unroll
-                for (int sp = 0; sp < 8; ++sp)
-                    if (sp < n_part) acc.x += pv[sp].x, acc.y += pv[sp].y, acc.z += pv[sp].z, acc.w += pv[sp].w;
-                q.x += acc.x, q.y += acc.y, q.z += acc.z, q.w += acc.w;
-                *reinterpret_cast<float4 *>(xr + e) = q;
+                for (int sp = 0; sp < kInline; ++sp)
+                    if (sp < n_part) acc.x += pv[i][sp].x, acc.y += pv[i][sp].y, acc.z += pv[i][sp].z, acc.w += pv[i][sp].w;
+                for (int sp = kInline; sp < n_part; ++sp) {
+                    const float4 p = *reinterpret_cast<const float4 *>(part + ((size_t)sp * part_rows + src) * H + e);
+                    acc.x += p.x, acc.y += p.y, acc.z += p.z, acc.w += p.w;
+                }
+                q[i].x += acc.x, q[i].y += acc.y, q[i].z += acc.z, q[i].w += acc.w;
+                *reinterpret_cast<float4 *>(xr + e) = q[i];
             }
-            v[i][0] = q.x, v[i][1] = q.y, v[i][2] = q.z, v[i][3] = q.w;
-            s += q.x + q.y + q.z + q.w;
+            v[i][0] = q[i].x, v[i][1] = q[i].y, v[i][2] = q[i].z, v[i][3] = q[i].w;
+            s += q[i].x + q[i].y + q[i].z + q[i].w;
         }
     }
     const float mean = block_sum(s, red) / (float)H;
