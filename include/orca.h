@@ -300,7 +300,15 @@ int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, const void *kv
  * iteration every selected request gets its token; a request is done after
  * out_len tokens and its K/V is freed at once.
  * mode 1 = request-level baseline: a batch is formed only when the previous
- * one has completely finished; its K/V is freed when it completes. */
+ * one has completely finished; its K/V is freed when it completes.
+ * chunked_prefill (mode 0 only): a request still in its prompt whose remaining
+ * prompt exceeds what is left of the iteration's max_tokens takes exactly what
+ * is left (>= 1 token) and admission stops there; its prompt runs in chunks
+ * over consecutive iterations, each with the tokens processed so far as
+ * context (phase 1, n_input > 1), and only the iteration that processes its
+ * last prompt token yields a token (the engine's output for an earlier chunk
+ * is ignored).  Prompts longer than max_tokens become admissible.  The pages
+ * describe no chunking (a later system's idea); this is the plainest reading. */
 typedef struct orca_sched_config {
     int32_t max_batch, max_tokens;
     int64_t kv_slots;      /* used only when no engine is attached */
@@ -308,6 +316,7 @@ typedef struct orca_sched_config {
     int32_t mode;          /* 0 iteration-level, 1 request-level */
     int32_t token_feedback;/* 1: increment inputs are emitted as references to
                               the previous iteration's outputs (see orca_batch) */
+    int32_t chunked_prefill; /* 0 or 1 (see above) */
 } orca_sched_config;
 
 typedef struct orca_sched orca_sched;
@@ -342,12 +351,22 @@ int orca_sched_next(orca_sched *s, orca_batch *out, int32_t *status);
  * requests. */
 int orca_sched_complete(orca_sched *s, const int32_t *next_tokens);
 
+/* Cancel a waiting or running request between iterations ([houmin] 3.1.1: a
+ * request that leaves the pool has its memory freed at once): it never runs
+ * again, its K/V reservation is freed immediately (also in request-level
+ * mode), its tokens so far stay readable (state 3), and a request-level batch
+ * whose remaining members are all done completes at once.
+ * Errors: NOT_FOUND (unknown id), INVALID (a batch is open, or the request is
+ * finished or already cancelled). */
+int orca_sched_cancel(orca_sched *s, int64_t id);
+
 typedef struct orca_sched_stats {
     int64_t clock;            /* iteration clock */
     int64_t iterations;       /* engine iterations issued */
     int64_t generated;        /* tokens generated */
     int64_t finished, waiting, running;
     int64_t kv_reserved;      /* tokens currently reserved */
+    int64_t cancelled;
 } orca_sched_stats;
 int orca_sched_stats_get(orca_sched *s, orca_sched_stats *out);
 
@@ -355,7 +374,7 @@ int orca_sched_stats_get(orca_sched *s, orca_sched_stats *out);
  * (-1 = not yet; a request entered with ctx0 > 0 is admitted at -1). */
 typedef struct orca_request_info {
     int64_t id, kv_offset;
-    int32_t state; /* 0 waiting, 1 running, 2 finished */
+    int32_t state; /* 0 waiting, 1 running, 2 finished, 3 cancelled */
     int32_t ctx_len, n_generated;
     int64_t admitted_at, finished_at;
 } orca_request_info;

@@ -17,6 +17,15 @@
 // producing the first; the clock counts iterations and a tick with nothing to
 // run does not call the engine.  Request-level mode (the baseline): a batch is
 // formed only when the previous batch has completely finished.
+//
+// Cancellation (houmin 3.1.1: a request that leaves the pool has its memory
+// freed at once): between iterations a waiting or running request can be
+// dropped; its reservation is freed immediately, it never runs again, and a
+// request-level batch whose other members are all done completes then.
+// Chunked prefill (optional, iteration-level only): in the FCFS scan a request
+// still in its prompt whose remaining prompt exceeds the budget left takes the
+// budget left as a chunk (>= 1 token) and the scan stops; only the iteration
+// that processes its last prompt token yields a token.
 #include <algorithm>
 #include <cstring>
 #include <memory>
@@ -29,7 +38,7 @@
 
 namespace {
 
-enum { W_WAITING = 0, W_RUNNING = 1, W_FINISHED = 2 };
+enum { W_WAITING = 0, W_RUNNING = 1, W_FINISHED = 2, W_CANCELLED = 3 };
 
 struct Request {
     int64_t id = 0;
@@ -45,8 +54,12 @@ struct Request {
     int64_t admitted_at = -1, finished_at = -1;
     int64_t last_iter = -1;  // engine iteration this request last ran in
     int32_t last_index = -1; // its index in that iteration's batch
+    int32_t chunk = 0;       // its input rows in the batch being formed
 
-    int32_t n_input() const { return ctx == 0 ? (int32_t)prompt.size() : 1; }
+    // prompt tokens remain to be processed (never for requests entered with ctx0 > 0)
+    bool in_prompt() const { return ctx0 == 0 && ctx < (int32_t)prompt.size(); }
+    // rows needed to finish the current phase in one iteration
+    int32_t n_input() const { return in_prompt() ? (int32_t)prompt.size() - ctx : 1; }
     bool done() const { return (int32_t)generated.size() >= out_len; }
 };
 
@@ -66,7 +79,7 @@ struct orca_sched {
     std::vector<Request *> current_batch;  // request-level mode only
     std::vector<Request *> batch;          // batch of the last orca_sched_next
     bool batch_open = false;
-    int64_t clock = 0, iterations = 0, generated = 0, finished = 0;
+    int64_t clock = 0, iterations = 0, generated = 0, finished = 0, cancelled = 0;
     int64_t feedback_since = 0;  // first iteration run with token feedback on
     // descriptor arrays handed out by orca_sched_next
     std::vector<int64_t> d_id, d_kv;
@@ -99,7 +112,12 @@ struct orca_sched {
         int64_t rows = 0;
         for (Request *r : cands) {
             int32_t n = r->n_input();
-            if ((int32_t)out.size() >= cfg.max_batch || rows + n > cfg.max_tokens) break;
+            if ((int32_t)out.size() >= cfg.max_batch) break;
+            if (rows + n > cfg.max_tokens) {
+                const int64_t left = cfg.max_tokens - rows;
+                if (!(cfg.chunked_prefill && r->in_prompt() && left >= 1)) break;
+                n = (int32_t)left;  // a chunk of the prompt; the budget is now used up
+            }
             if (r->state == W_WAITING) {
                 int64_t off = -1;
                 if (kv_alloc(r->id, reserve_size(*r), &off) != ORCA_OK) break;
@@ -107,9 +125,21 @@ struct orca_sched {
                 r->state = W_RUNNING;
                 r->admitted_at = clock;
             }
+            r->chunk = n;
             out.push_back(r);
             rows += n;
         }
+    }
+
+    // Request-level: the batch completes when every member is done or
+    // cancelled; the reservations still held are released then.
+    void close_request_batch() {
+        if (cfg.mode != 1 || current_batch.empty()) return;
+        for (Request *r : current_batch)
+            if (!r->done() && r->state != W_CANCELLED) return;
+        for (Request *r : current_batch)
+            if (r->state != W_CANCELLED) kv_free(r->id);
+        current_batch.clear();
     }
 };
 
@@ -127,7 +157,8 @@ extern "C" {
 
 int orca_sched_create(const orca_sched_config *cfg, orca_engine *eng, orca_sched **out) {
     if (!cfg || !out) return ORCA_ERR_INVALID;
-    if (cfg->max_batch <= 0 || cfg->max_tokens <= 0 || cfg->kv_reserve < 0 || (cfg->mode != 0 && cfg->mode != 1))
+    if (cfg->max_batch <= 0 || cfg->max_tokens <= 0 || cfg->kv_reserve < 0 || (cfg->mode != 0 && cfg->mode != 1) ||
+        (cfg->chunked_prefill != 0 && cfg->chunked_prefill != 1) || (cfg->chunked_prefill && cfg->mode != 0))
         return ORCA_ERR_INVALID;
     if (!eng && cfg->kv_slots <= 0) return ORCA_ERR_INVALID;
     orca_sched *s = new (std::nothrow) orca_sched();
@@ -165,7 +196,8 @@ int orca_sched_submit(orca_sched *s, int64_t id, double arrival, const int32_t *
     r->out_len = out_len;
     r->ctx0 = ctx0;
     int64_t need = ctx0 ? (int64_t)ctx0 + out_len : (int64_t)prompt_len + out_len - 1;
-    if (prompt_len > s->cfg.max_tokens || need > s->reserve_size(*r)) return ORCA_ERR_INVALID;
+    if ((prompt_len > s->cfg.max_tokens && !s->cfg.chunked_prefill) || need > s->reserve_size(*r))
+        return ORCA_ERR_INVALID;
     if (ctx0) {
         if (prompt_len != 1) return ORCA_ERR_INVALID;
         int64_t off = -1;
@@ -206,7 +238,7 @@ int orca_sched_next(orca_sched *s, orca_batch *out, int32_t *status) {
     for (Request *r : s->live) {
         if (r->arrival > k) break;  // live is sorted by arrival first
         if (s->cfg.mode == 1 && r->state != W_WAITING) continue;
-        cands.push_back(r);
+        cands.push_back(r);  // (live holds no finished or cancelled request)
     }
     if (s->cfg.mode == 0) {
         s->admit_prefix(cands, s->batch);
@@ -214,7 +246,10 @@ int orca_sched_next(orca_sched *s, orca_batch *out, int32_t *status) {
         if (s->current_batch.empty()) s->admit_prefix(cands, s->current_batch);
         s->batch.clear();
         for (Request *r : s->current_batch)
-            if (!r->done()) s->batch.push_back(r);
+            if (r->state == W_RUNNING && !r->done()) {
+                r->chunk = r->n_input();
+                s->batch.push_back(r);
+            }
     }
     if (s->batch.empty()) {
         s->clock++;
@@ -233,10 +268,10 @@ int orca_sched_next(orca_sched *s, orca_batch *out, int32_t *status) {
         s->d_id[i] = r->id;
         s->d_kv[i] = r->kv_off;
         s->d_phase[i] = r->ctx == 0 ? 0 : 1;
-        s->d_n[i] = r->n_input();
+        s->d_n[i] = r->chunk;
         s->d_ctx[i] = r->ctx;
-        if (r->ctx == 0) {
-            s->d_tok.insert(s->d_tok.end(), r->prompt.begin(), r->prompt.end());
+        if (r->in_prompt()) {
+            s->d_tok.insert(s->d_tok.end(), r->prompt.begin() + r->ctx, r->prompt.begin() + r->ctx + r->chunk);
         } else if (s->cfg.token_feedback && r->last_iter == s->iterations - 1 && r->last_iter >= s->feedback_since) {
             s->d_tok.push_back(-1 - r->last_index);
         } else {
@@ -259,11 +294,12 @@ int orca_sched_complete(orca_sched *s, const int32_t *next_tokens) {
     if (!s || !next_tokens || !s->batch_open) return ORCA_ERR_INVALID;
     for (size_t i = 0; i < s->batch.size(); ++i) {
         Request *r = s->batch[i];
-        r->ctx += r->n_input();
-        r->generated.push_back(next_tokens[i]);
-        r->pending = next_tokens[i];
+        r->ctx += r->chunk;
         r->last_iter = s->iterations;
         r->last_index = (int32_t)i;
+        if (r->in_prompt()) continue;  // a prompt chunk before the last: its output is not a token
+        r->generated.push_back(next_tokens[i]);
+        r->pending = next_tokens[i];
         s->generated++;
         if (r->done()) {
             r->state = W_FINISHED;
@@ -272,19 +308,27 @@ int orca_sched_complete(orca_sched *s, const int32_t *next_tokens) {
             if (s->cfg.mode == 0) s->kv_free(r->id);
         }
     }
-    if (s->cfg.mode == 1) {
-        bool all_done = true;
-        for (Request *r : s->current_batch) all_done = all_done && r->done();
-        if (all_done) {
-            for (Request *r : s->current_batch) s->kv_free(r->id);
-            s->current_batch.clear();
-        }
-    }
+    s->close_request_batch();
     s->live.erase(std::remove_if(s->live.begin(), s->live.end(), [](Request *r) { return r->state == W_FINISHED; }),
                   s->live.end());
     s->batch_open = false;
     s->iterations++;
     s->clock++;
+    return ORCA_OK;
+}
+
+int orca_sched_cancel(orca_sched *s, int64_t id) {
+    if (!s) return ORCA_ERR_INVALID;
+    if (s->batch_open) return ORCA_ERR_INVALID;  // only between iterations
+    auto it = s->by_id.find(id);
+    if (it == s->by_id.end()) return ORCA_ERR_NOT_FOUND;
+    Request *r = it->second.get();
+    if (r->state != W_WAITING && r->state != W_RUNNING) return ORCA_ERR_INVALID;
+    if (r->kv_off >= 0) s->kv_free(r->id);
+    r->state = W_CANCELLED;
+    s->cancelled++;
+    s->live.erase(std::remove(s->live.begin(), s->live.end(), r), s->live.end());
+    s->close_request_batch();
     return ORCA_OK;
 }
 
@@ -294,6 +338,7 @@ int orca_sched_stats_get(orca_sched *s, orca_sched_stats *out) {
     out->iterations = s->iterations;
     out->generated = s->generated;
     out->finished = s->finished;
+    out->cancelled = s->cancelled;
     int64_t waiting = 0, running = 0;
     for (Request *r : s->live) (r->state == W_WAITING ? waiting : running)++;
     out->waiting = waiting;

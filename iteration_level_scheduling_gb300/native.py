@@ -32,7 +32,8 @@ EXPORTS = [
     "orca_engine_timing", "orca_engine_timing_read", "orca_op_linear", "orca_op_attention", "orca_packed_weight_elems",
     "orca_pack_weight",
     "orca_attention_decode_noalloc", "orca_sched_create", "orca_sched_destroy",
-    "orca_sched_submit", "orca_sched_set_token_feedback", "orca_sched_next", "orca_sched_complete", "orca_sched_stats_get", "orca_sched_request_get",
+    "orca_sched_submit", "orca_sched_set_token_feedback", "orca_sched_next", "orca_sched_complete", "orca_sched_cancel",
+    "orca_sched_stats_get", "orca_sched_request_get",
     "orca_sched_request_tokens", "orca_sched_run",
 ]
 
@@ -81,12 +82,13 @@ class KernelTime(C.Structure):
 
 class SchedConfig(C.Structure):
     _fields_ = [("max_batch", C.c_int32), ("max_tokens", C.c_int32), ("kv_slots", C.c_int64),
-                ("kv_reserve", C.c_int32), ("mode", C.c_int32), ("token_feedback", C.c_int32)]
+                ("kv_reserve", C.c_int32), ("mode", C.c_int32), ("token_feedback", C.c_int32),
+                ("chunked_prefill", C.c_int32)]
 
 
 class SchedStats(C.Structure):
     _fields_ = [("clock", C.c_int64), ("iterations", C.c_int64), ("generated", C.c_int64), ("finished", C.c_int64),
-                ("waiting", C.c_int64), ("running", C.c_int64), ("kv_reserved", C.c_int64)]
+                ("waiting", C.c_int64), ("running", C.c_int64), ("kv_reserved", C.c_int64), ("cancelled", C.c_int64)]
 
 
 class RequestInfo(C.Structure):
@@ -126,6 +128,7 @@ _sig = {
     "orca_sched_set_token_feedback": (C.c_int, [P, C.c_int32]),
     "orca_sched_next": (C.c_int, [P, C.POINTER(Batch), C.POINTER(C.c_int32)]),
     "orca_sched_complete": (C.c_int, [P, P]),
+    "orca_sched_cancel": (C.c_int, [P, C.c_int64]),
     "orca_sched_stats_get": (C.c_int, [P, C.POINTER(SchedStats)]),
     "orca_sched_request_get": (C.c_int, [P, C.c_int64, C.POINTER(RequestInfo)]),
     "orca_sched_request_tokens": (C.c_int, [P, C.c_int64, P, C.c_int32, C.POINTER(C.c_int32)]),
@@ -309,8 +312,9 @@ class Scheduler:
     ``engine=None`` it keeps its own host-side K/V pool and needs no GPU."""
 
     def __init__(self, max_batch: int, max_tokens: int, kv_slots: int = 0, kv_reserve: int = 0, mode: int = 0,
-                 token_feedback: bool = False, engine: Optional[Engine] = None):
-        self.cfg = SchedConfig(max_batch, max_tokens, kv_slots, kv_reserve, mode, int(token_feedback))
+                 token_feedback: bool = False, engine: Optional[Engine] = None, chunked_prefill: bool = False):
+        self.cfg = SchedConfig(max_batch, max_tokens, kv_slots, kv_reserve, mode, int(token_feedback),
+                               int(chunked_prefill))
         self._h = P()
         self.engine = engine
         check(lib.orca_sched_create(C.byref(self.cfg), engine.handle if engine else None, C.byref(self._h)),
@@ -358,6 +362,9 @@ class Scheduler:
     def complete(self, next_tokens) -> None:
         t = _i32(next_tokens)
         check(lib.orca_sched_complete(self._h, _ptr(t)), "orca_sched_complete")
+
+    def cancel(self, rid: int) -> None:
+        check(lib.orca_sched_cancel(self._h, rid), "orca_sched_cancel")
 
     def stats(self) -> SchedStats:
         s = SchedStats()

@@ -35,6 +35,23 @@ a batch is formed (same FCFS prefix rule) only when the previous batch has
 completely finished, and runs until its longest member is done.  Members that
 finish early stop being executed (their slots idle); K/V of the whole batch is
 released when it completes.
+
+Cancellation ([houmin] 3.1.1: a request that is done leaves the pool and its
+memory is freed at once; the same applies to a request the client drops).
+Between iterations a request may be cancelled: it leaves the pool, never runs
+again, and its K/V reservation is freed immediately, in either mode.  Its
+tokens so far stay readable.  A request-level batch whose remaining members
+are all done or cancelled completes at that moment.
+
+Chunked prefill (optional, iteration-level only; a later system's idea that
+the pages mention as a contrast: a prompt larger than what is left of an
+iteration's token budget is split).  Reading taken: in the FCFS scan, a
+request still in its prompt whose remaining prompt exceeds the budget left
+takes exactly that budget as a chunk (at least one token) and the scan stops
+there; its chunks run in consecutive selections, each with the tokens
+processed so far as context; only the iteration that processes the last
+prompt token yields a generated token (the engine's output for an earlier
+chunk is ignored).  Prompts longer than max_tokens become admissible.
 """
 
 from __future__ import annotations
@@ -60,16 +77,23 @@ class Req:
     state: str = "waiting"  # waiting | running | finished
     admitted_at: Optional[int] = None
     finished_at: Optional[int] = None
+    chunk: int = 0  # input rows of the request in the batch being formed
 
     @property
     def done(self) -> bool:
         return len(self.generated) >= self.out_len
 
+    @property
+    def in_prompt(self) -> bool:
+        """Prompt tokens not yet processed remain (never for ctx0 > 0 requests)."""
+        return self.ctx0 == 0 and self.ctx < len(self.prompt)
+
     def n_input(self) -> int:
-        return len(self.prompt) if self.ctx == 0 else 1
+        """Rows the request needs to finish its current phase in one iteration."""
+        return len(self.prompt) - self.ctx if self.in_prompt else 1
 
     def input_tokens(self) -> List[int]:
-        return list(self.prompt) if self.ctx == 0 else [self.pending]
+        return list(self.prompt[self.ctx:self.ctx + self.chunk]) if self.in_prompt else [self.pending]
 
 
 @dataclasses.dataclass
@@ -96,10 +120,14 @@ class Iteration:
 
 class Scheduler:
     def __init__(self, max_batch: int, max_tokens: int, kv_slots: int, kv_reserve: int = 0,
-                 mode: str = "iteration"):
+                 mode: str = "iteration", chunked_prefill: bool = False):
         if mode not in ("iteration", "request"):
             raise ValueError(mode)
+        if chunked_prefill and mode != "iteration":
+            raise ValueError("chunked prefill is an iteration-level option")
         self.max_batch, self.max_tokens, self.kv_reserve, self.mode = max_batch, max_tokens, kv_reserve, mode
+        self.chunked_prefill = chunked_prefill
+        self.cancelled_total = 0
         self.pool = KVPool(kv_slots)
         self.reqs: List[Req] = []
         self.k = 0
@@ -118,7 +146,8 @@ class Scheduler:
         if out_len < 1 or len(r.prompt) < 1:
             raise ValueError("empty request")
         need = (ctx0 + out_len) if ctx0 else (len(r.prompt) + out_len - 1)
-        if len(r.prompt) > self.max_tokens or need > self.reserve_size(r):
+        too_long = len(r.prompt) > self.max_tokens and not self.chunked_prefill
+        if too_long or need > self.reserve_size(r):
             raise ValueError("request does not fit its reservation or the token budget")
         if ctx0:
             # already in the increment phase: its context is cached, so its
@@ -133,7 +162,7 @@ class Scheduler:
         return r
 
     def _ordered(self, k: int) -> List[Req]:
-        c = [r for r in self.reqs if r.state != "finished" and r.arrival <= k]
+        c = [r for r in self.reqs if r.state in ("waiting", "running") and r.arrival <= k]
         c.sort(key=lambda r: (r.arrival, r.rid))
         return c
 
@@ -141,13 +170,19 @@ class Scheduler:
         batch, rows = [], 0
         for r in cands:
             n = r.n_input()
-            if len(batch) >= self.max_batch or rows + n > self.max_tokens:
+            if len(batch) >= self.max_batch:
                 break
+            if rows + n > self.max_tokens:
+                left = self.max_tokens - rows
+                if not (self.chunked_prefill and r.in_prompt and left >= 1):
+                    break
+                n = left  # a chunk of the prompt; the budget is now used up
             if r.state == "waiting":
                 off = self.pool.alloc(r.rid, self.reserve_size(r))
                 if off is None:
                     break
                 r.kv_off, r.state, r.admitted_at = off, "running", k
+            r.chunk = n
             batch.append(r)
             rows += n
         return batch
@@ -159,19 +194,24 @@ class Scheduler:
             return self._admit_prefix(self._ordered(k), k)
         if not self.current_batch:
             self.current_batch = self._admit_prefix([r for r in self._ordered(k) if r.state == "waiting"], k)
-        return [r for r in self.current_batch if not r.done]
+        batch = [r for r in self.current_batch if r.state == "running" and not r.done]
+        for r in batch:
+            r.chunk = r.n_input()
+        return batch
 
     def describe(self, batch: List[Req]) -> Iteration:
         toks = []
         for r in batch:
             toks += r.input_tokens()
         return Iteration(self.k, [r.rid for r in batch], [0 if r.ctx == 0 else 1 for r in batch],
-                         [r.n_input() for r in batch], [r.ctx for r in batch], [r.kv_off for r in batch], toks)
+                         [r.chunk for r in batch], [r.ctx for r in batch], [r.kv_off for r in batch], toks)
 
     def complete(self, batch: List[Req], next_tokens: Sequence[int]) -> None:
         """Engine returned: append tokens, advance contexts, retire finished requests."""
         for r, t in zip(batch, next_tokens):
-            r.ctx += r.n_input()
+            r.ctx += r.chunk
+            if r.in_prompt:
+                continue  # a prompt chunk before the last: its output is not a token
             r.generated.append(int(t))
             r.pending = int(t)
             self.generated_total += 1
@@ -179,35 +219,65 @@ class Scheduler:
                 r.state, r.finished_at = "finished", self.k
                 if self.mode == "iteration":
                     self.pool.free(r.rid)
-        if self.mode == "request" and all(r.done for r in self.current_batch):
-            for r in self.current_batch:
-                self.pool.free(r.rid)
-            self.current_batch = []
+        self._close_request_batch()
         self.iterations += 1
         self.k += 1
+
+    def _close_request_batch(self) -> None:
+        """Request-level: the batch completes when every member is done or
+        cancelled; the reservations still held are released then."""
+        if self.mode == "request" and self.current_batch and all(
+                r.done or r.state == "cancelled" for r in self.current_batch):
+            for r in self.current_batch:
+                if r.state != "cancelled":
+                    self.pool.free(r.rid)
+            self.current_batch = []
+
+    def cancel(self, rid: int) -> None:
+        """Drop a waiting or running request between iterations; its K/V is
+        freed at once."""
+        r = next((q for q in self.reqs if q.rid == rid), None)
+        if r is None:
+            raise KeyError(rid)
+        if r.state not in ("waiting", "running") or (self.mode == "request" and r.done):
+            raise ValueError("request is not live")
+        if r.kv_off is not None:
+            self.pool.free(r.rid)
+        r.state = "cancelled"
+        self.cancelled_total += 1
+        self._close_request_batch()
 
     def idle(self) -> None:
         self.k += 1
 
     def unfinished(self) -> bool:
-        return any(r.state != "finished" for r in self.reqs)
+        return any(r.state in ("waiting", "running") for r in self.reqs)
 
 
 def run(specs, max_batch: int, max_tokens: int, kv_slots: int, kv_reserve: int = 0, mode: str = "iteration",
-        token_fn: Optional[Callable[[Iteration], Sequence[int]]] = None, max_iters: int = 10 ** 7):
+        token_fn: Optional[Callable[[Iteration], Sequence[int]]] = None, max_iters: int = 10 ** 7,
+        chunked_prefill: bool = False, cancel_at: Optional[dict] = None):
     """Drive a scheduler over request specs until every request finished.
 
     ``token_fn(iteration)`` plays the engine and returns one next token per
-    request (default: a deterministic dummy).  Returns (scheduler, list of
+    request (default: a deterministic dummy).  ``cancel_at`` maps a clock value
+    to the request ids cancelled just before that iteration's selection (ids
+    that are no longer live are skipped).  Returns (scheduler, list of
     Iteration records, one per engine call).
     """
-    s = Scheduler(max_batch, max_tokens, kv_slots, kv_reserve, mode)
+    s = Scheduler(max_batch, max_tokens, kv_slots, kv_reserve, mode, chunked_prefill)
     for sp in specs:
         s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len, sp.ctx0)
     if token_fn is None:
         token_fn = lambda it: [(rid * 31 + it.k) % 50000 for rid in it.rids]
     records = []
     while s.unfinished() and s.k < max_iters:
+        for rid in (cancel_at or {}).get(s.k, ()):
+            r = next((q for q in s.reqs if q.rid == rid), None)
+            if r is not None and r.state in ("waiting", "running") and not (s.mode == "request" and r.done):
+                s.cancel(rid)
+        if not s.unfinished():
+            break
         batch = s.select()
         if not batch:
             s.idle()

@@ -30,17 +30,23 @@ def built():
     build.build()
 
 
-def run_trace_teacher_forced(cfg, w, specs, max_batch, mode, kv_slots, max_tokens=4096, feedback=False):
+def run_trace_teacher_forced(cfg, w, specs, max_batch, mode, kv_slots, max_tokens=4096, feedback=False,
+                             chunked=False, cancel_at=None):
     from iteration_level_scheduling_gb300 import native
     eng = make_engine(cfg, w, max_tokens, max_batch, kv_slots)
-    s = native.Scheduler(max_batch, max_tokens, mode=mode, engine=eng, token_feedback=feedback)
+    s = native.Scheduler(max_batch, max_tokens, mode=mode, engine=eng, token_feedback=feedback,
+                         chunked_prefill=chunked)
     for sp in specs:
         s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len, sp.ctx0)
     store = KVStore(cfg.n_layers, cfg.hidden)
     worst_h = worst_l = 0.0
-    agree = total = iters = 0
+    agree = total = iters = chunks = 0
     prev_next = {}
     while True:
+        for rid in (cancel_at or {}).get(s.stats().clock, ()):
+            if s.request(rid).state in (0, 1):
+                s.cancel(rid)
+                store.drop(rid)
         st, b = s.next()
         if st == 2:
             break
@@ -50,6 +56,7 @@ def run_trace_teacher_forced(cfg, w, specs, max_batch, mode, kv_slots, max_token
         items, p = [], 0
         resolved = []
         for rid, n, c in zip(b.request_id.tolist(), b.n_input.tolist(), b.ctx_len.tolist()):
+            chunks += int(n > 1 and c > 0)
             tk = toks[p:p + n]
             tk = [prev_next[-1 - t] if t < 0 else t for t in tk]
             resolved += tk
@@ -72,7 +79,7 @@ def run_trace_teacher_forced(cfg, w, specs, max_batch, mode, kv_slots, max_token
     s.close()
     eng.close()
     return dict(iters=iters, worst_h=worst_h, worst_l=worst_l, agree=agree / max(total, 1), total=total,
-                generated=st.generated, launches=eng_stats.launches)
+                generated=st.generated, launches=eng_stats.launches, chunks=chunks, cancelled=st.cancelled)
 
 
 @pytest.mark.parametrize("mode,expect_iters", [(0, 50), (1, 90)])
@@ -96,6 +103,36 @@ def test_tiny_fp32_trace_token_feedback():
     w = synth.make_weights(cfg, 1, random_affine=True)
     r = run_trace_teacher_forced(cfg, w, synth.tiny_requests(1), 4, 0, kv_slots=4 * 128, feedback=True)
     assert r["worst_l"] <= TOL_FP32 and r["agree"] == 1.0, r
+
+
+def test_tiny_fp32_chunked_prefill_and_cancellation():
+    """Prompts split over iterations under a 6-row budget (chunks run as
+    multi-row requests with cached context), and three requests cancelled
+    mid-flight (their K/V goes back to the engine's pool and is reused): every
+    iteration matches the oracle to 1e-4."""
+    cfg = synth.TINY
+    w = synth.make_weights(cfg, 2, random_affine=True)
+    specs = synth.tiny_requests(2)
+    r = run_trace_teacher_forced(cfg, w, specs, 4, 0, kv_slots=4 * 128, max_tokens=6, chunked=True,
+                                 cancel_at={3: [1], 9: [4, 6]})
+    assert r["chunks"] >= 3 and r["cancelled"] == 3
+    assert r["worst_h"] <= TOL_FP32 and r["worst_l"] <= TOL_FP32, r
+    assert r["agree"] >= 0.99, r
+
+
+def test_gpt2_medium_chunked_prompt():
+    """GPT-2-medium width (bf16, head_dim 64), two layers: a 300-token prompt
+    beside increment requests under a 128-row budget, so the prompt runs as
+    chunks of cached-context prefill through the tensor-core kernels."""
+    cfg = synth.GPT2_MEDIUM.with_layers(2)
+    w = synth.make_weights(cfg, 1, random_affine=True)
+    rnd = np.random.default_rng(5)
+    specs = [synth.RequestSpec(0, 0.0, rnd.integers(0, cfg.vocab, 300).tolist(), 4)]
+    specs += [synth.RequestSpec(i, 0.0, rnd.integers(0, cfg.vocab, int(rnd.integers(2, 40))).tolist(), 6)
+              for i in range(1, 6)]
+    r = run_trace_teacher_forced(cfg, w, specs, 8, 0, kv_slots=8 * 512, max_tokens=128, chunked=True)
+    assert r["chunks"] >= 2
+    assert r["worst_h"] <= TOL_BF16 and r["worst_l"] <= TOL_BF16, r
 
 
 def run_one_batch(cfg, w, reqs, sample, seed_kv=0, max_tokens=None, pack_weights=True):

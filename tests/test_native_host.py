@@ -150,3 +150,87 @@ def test_token_feedback_enabled_midway(native):
     s.complete([8])
     st, b = s.next()
     assert b.tokens.tolist() == [-1]
+
+
+def drive_native_ext(native, specs, max_batch, max_tokens, kv_slots, mode=0, chunked=False, cancel_at=None):
+    """drive_native with chunked prefill and cancellations before selections."""
+    s = native.Scheduler(max_batch, max_tokens, kv_slots, 0, mode, False, chunked_prefill=chunked)
+    for sp in specs:
+        s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len, sp.ctx0)
+    recs = []
+    while True:
+        for rid in (cancel_at or {}).get(s.stats().clock, ()):
+            info = s.request(rid)
+            live = info.state in (0, 1) and not (mode == 1 and info.n_generated >= specs[rid].out_len)
+            if live:
+                s.cancel(rid)
+        st, b = s.next()
+        if st == 2:
+            break
+        if st == 0:
+            continue
+        toks = [(int(r) * 31 + s.stats().clock) % 50000 for r in b.request_id]
+        recs.append((s.stats().clock, b))
+        s.complete(toks)
+    return s, recs
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_native_matches_oracle_chunked_prefill(native, seed):
+    rnd = random.Random(300 + seed)
+    mt = rnd.randint(8, 80)
+    trace = synth.poisson_trace(seed, n=60, rate=rnd.choice([0.3, 1.0, 3.0]), prompt_range=(1, 3 * mt),
+                                out_range=(1, 30), vocab=1000)
+    mb = rnd.randint(1, 8)
+    s, recs = drive_native_ext(native, trace, mb, mt, 10 ** 5, chunked=True)
+    _, orecs = osched.run(trace, mb, mt, 10 ** 5, chunked_prefill=True,
+                          token_fn=lambda it: [(rid * 31 + it.k) % 50000 for rid in it.rids])
+    assert_same(recs, orecs)
+    assert any(n > 1 and c > 0 for _, b in recs for n, c in zip(b.n_input.tolist(), b.ctx_len.tolist()))
+    for sp in trace:
+        assert s.request(sp.rid).n_generated == sp.out_len
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_native_matches_oracle_cancellation(native, seed):
+    rnd = random.Random(400 + seed)
+    trace = synth.poisson_trace(seed, n=60, rate=rnd.choice([0.3, 1.0, 3.0]), prompt_range=(1, 40),
+                                out_range=(1, 30), vocab=1000)
+    cancel_at = {}
+    for sp in rnd.sample(trace, 20):
+        cancel_at.setdefault(rnd.randint(0, 80), []).append(sp.rid)
+    mb, mt = rnd.randint(1, 8), rnd.randint(40, 200)
+    for mode in (0, 1):
+        s, recs = drive_native_ext(native, trace, mb, mt, 3000, mode=mode, cancel_at=cancel_at)
+        o, orecs = osched.run(trace, mb, mt, 3000, 0, "iteration" if mode == 0 else "request",
+                              token_fn=lambda it: [(rid * 31 + it.k) % 50000 for rid in it.rids],
+                              cancel_at=cancel_at)
+        assert_same(recs, orecs)
+        st = s.stats()
+        assert st.cancelled == o.cancelled_total >= 1 and st.kv_reserved == 0
+        for r in o.reqs:
+            info = s.request(r.rid)
+            assert info.state == {"finished": 2, "cancelled": 3}[r.state]
+            assert s.tokens(r.rid).tolist() == r.generated
+
+
+def test_cancel_errors(native):
+    s = native.Scheduler(2, 4096, kv_slots=100)
+    s.submit(0, 0.0, [1, 2], 3)
+    s.submit(1, 0.0, [3], 3)
+    with pytest.raises(native.OrcaError) as e:
+        s.cancel(7)
+    assert e.value.code == native.ERR_NOT_FOUND
+    st, b = s.next()
+    with pytest.raises(native.OrcaError) as e:  # a batch is open
+        s.cancel(0)
+    assert e.value.code == native.ERR_INVALID
+    s.complete([5, 6])
+    assert s.stats().kv_reserved == (2 + 3) + (1 + 3)
+    s.cancel(0)
+    assert s.stats().kv_reserved == 1 + 3 and s.request(0).state == 3
+    with pytest.raises(native.OrcaError):
+        s.cancel(0)                              # already cancelled
+    assert s.tokens(0).tolist() == [5]
+    with pytest.raises(native.OrcaError):        # chunked prefill is an iteration-level option
+        native.Scheduler(2, 4096, kv_slots=100, mode=1, chunked_prefill=True)

@@ -224,3 +224,20 @@ def test_pins_catch_planted_mistakes(mutation, monkeypatch):
     r = model.iteration(w, TINY.n_heads, [BatchItem(0, toks, 0)], store)
     y, logits = torch_reference_prefill(tiny_weights(3), TINY.n_heads, toks)
     assert not np.allclose(r.logits[0], logits, rtol=1e-6, atol=1e-8)
+
+
+def test_chunked_prompt_equals_whole_prompt():
+    """A prompt processed in chunks (each chunk attending to the K/V the earlier
+    chunks cached) gives the same last-row hidden state and logits as the whole
+    prompt at once: the chunked-prefill schedule computes the same function."""
+    w = tiny_weights(7)
+    seq = [5, 17, 3, 250, 9, 1, 44, 8, 120, 6, 2, 77, 31]
+    whole = model.iteration(w, TINY.n_heads, [BatchItem(0, seq, 0)], KVStore(TINY.n_layers, TINY.hidden))
+    for cuts in ([4], [1, 7], [6, 11, 12]):
+        store = KVStore(TINY.n_layers, TINY.hidden)
+        bounds = [0] + cuts + [len(seq)]
+        for a, b in zip(bounds, bounds[1:]):
+            res = model.iteration(w, TINY.n_heads, [BatchItem(0, seq[a:b], a)], store)
+        np.testing.assert_allclose(res.hidden, whole.hidden, rtol=1e-10, atol=1e-10)
+        np.testing.assert_allclose(res.logits, whole.logits, rtol=1e-10, atol=1e-10)
+        assert res.next_tokens == whole.next_tokens

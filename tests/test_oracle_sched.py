@@ -217,3 +217,126 @@ def test_kv_pool_random_no_overlap():
                 live[rid] = (off, n)
         assert p.used() == sum(l for _, l in live.values())
         assert sum(l for _, l in p.free_list) == 500 - p.used()
+
+
+# --------------------------------------------------------------------------- #
+# cancellation: the request leaves the pool and its K/V is freed at once
+# --------------------------------------------------------------------------- #
+def test_cancel_worked_example_iteration_level():
+    # pool 100, reservations prompt + output: A 2+10 = 12 at 0, B 2+10 at 12, C 2+10 waits (max_batch 2)
+    specs = [synth.RequestSpec(i, 0.0, [1, 2], 10) for i in range(3)]
+    s = sched.Scheduler(2, 4096, 100)
+    for sp in specs:
+        s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len)
+    b = s.select()
+    assert [r.rid for r in b] == [0, 1] and s.pool.used() == 24
+    s.complete(b, [7, 8])
+    s.cancel(1)                      # between iterations: B's 12 slots come back at once
+    assert s.pool.used() == 12 and s.cancelled_total == 1
+    b = s.select()                   # C takes the freed place (first fit: B's old offset)
+    assert [r.rid for r in b] == [0, 2]
+    by = {r.rid: r for r in s.reqs}
+    assert by[2].kv_off == 12 and by[1].state == "cancelled" and by[1].generated == [8]
+    with pytest.raises(ValueError):
+        s.cancel(1)                  # not live any more
+    with pytest.raises(KeyError):
+        s.cancel(9)
+
+
+def test_cancel_worked_example_request_level():
+    specs = [synth.RequestSpec(i, 0.0, [1], L) for i, L in enumerate([2, 5, 3])]
+    s = sched.Scheduler(2, 4096, 100, mode="request")
+    for sp in specs:
+        s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len)
+    b = s.select()
+    s.complete(b, [1, 1])
+    s.cancel(1)                      # immediate release even in request-level mode
+    assert s.pool.used() == 1 + 2    # request 0 (1 + 2) keeps its reservation until the batch completes
+    b = s.select()
+    assert [r.rid for r in b] == [0]
+    s.complete(b, [1])               # request 0 done: the batch (0, cancelled 1) completes
+    assert s.pool.used() == 0 and s.current_batch == []
+    b = s.select()
+    assert [r.rid for r in b] == [2]
+
+
+def test_cancel_invariants_random_traces():
+    for seed in range(6):
+        rnd = random.Random(50 + seed)
+        trace = synth.poisson_trace(seed, n=50, rate=rnd.choice([0.3, 1.0, 3.0]), prompt_range=(1, 30),
+                                    out_range=(1, 25), vocab=100)
+        cancel_at = {}
+        for sp in rnd.sample(trace, 15):
+            cancel_at.setdefault(rnd.randint(0, 60), []).append(sp.rid)
+        for mode in ("iteration", "request"):
+            s, recs = sched.run(trace, rnd.randint(1, 6), rnd.randint(30, 120), 2000, 0, mode, cancel_at=cancel_at)
+            gone = {}
+            for r in s.reqs:
+                if r.state == "cancelled":
+                    gone[r.rid] = r
+            assert s.cancelled_total == len(gone) >= 1
+            for rec in recs:  # a cancelled request never runs after its cancellation
+                for rid in rec.rids:
+                    if rid in gone:
+                        t = min(k for k, ids in cancel_at.items() if rid in ids)
+                        assert rec.k < t
+            for r in s.reqs:
+                assert r.state in ("finished", "cancelled")
+                if r.state == "finished":
+                    assert len(r.generated) == r.out_len
+                else:
+                    assert len(r.generated) < r.out_len
+            assert s.pool.used() == 0 and s.pool.free_list == [(0, 2000)]
+
+
+# --------------------------------------------------------------------------- #
+# chunked prefill: a prompt larger than the budget left runs in chunks
+# --------------------------------------------------------------------------- #
+def test_chunked_prefill_worked_example():
+    a = synth.RequestSpec(0, 0.0, list(range(100, 110)), 2)   # prompt 10
+    b = synth.RequestSpec(1, 0.0, [7, 8, 9], 2)                # prompt 3
+    with pytest.raises(ValueError):
+        sched.run([a, b], 4, 8, 100)                           # 10 > max_tokens without chunking
+    s, recs = sched.run([a, b], 4, 8, 100, chunked_prefill=True)
+    assert [(r.rids, r.n_input, r.ctx, r.phase) for r in recs] == [
+        ([0], [8], [0], [0]),             # A's first 8 prompt tokens use the whole budget; B waits
+        ([0, 1], [2, 3], [8, 0], [1, 0]),  # A's last 2 prompt tokens (8 cached), B's prompt
+        ([0, 1], [1, 1], [10, 3], [1, 1]),
+    ]
+    assert recs[0].tokens == list(range(100, 108))
+    assert recs[1].tokens == [108, 109, 7, 8, 9]
+    by = {r.rid: r for r in s.reqs}
+    # A's first token comes from the iteration that processed its last prompt token
+    assert by[0].generated == [(0 * 31 + 1) % 50000, (0 * 31 + 2) % 50000]
+    assert by[1].generated == [(1 * 31 + 1) % 50000, (1 * 31 + 2) % 50000]
+
+
+def test_chunked_prefill_invariants_random_traces():
+    for seed in range(6):
+        rnd = random.Random(70 + seed)
+        mt = rnd.randint(8, 60)
+        trace = synth.poisson_trace(seed, n=40, rate=rnd.choice([0.3, 1.0, 3.0]), prompt_range=(1, 3 * mt),
+                                    out_range=(1, 20), vocab=1000)
+        s, recs = sched.run(trace, rnd.randint(1, 6), mt, 10 ** 5, chunked_prefill=True)
+        fed = {sp.rid: [] for sp in trace}
+        first_token_at = {}
+        for rec in recs:
+            assert sum(rec.n_input) <= mt
+            p = 0
+            for rid, ph, n, c in zip(rec.rids, rec.phase, rec.n_input, rec.ctx):
+                assert (ph == 0) == (c == 0)
+                spec = trace[rid]
+                if c < len(spec.prompt):  # a prompt chunk: the next unprocessed tokens, in order
+                    assert c == len(fed[rid])
+                    fed[rid] += rec.tokens[p:p + n]
+                    if c + n == len(spec.prompt):
+                        first_token_at[rid] = rec.k
+                else:
+                    assert n == 1
+                p += n
+        for sp in trace:
+            assert fed[sp.rid] == list(sp.prompt)
+        for r in s.reqs:
+            assert r.state == "finished" and len(r.generated) == r.out_len
+            assert r.generated[0] == (r.rid * 31 + first_token_at[r.rid]) % 50000
+        assert s.pool.used() == 0
