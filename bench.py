@@ -64,6 +64,8 @@ def parse():
     p.add_argument("--layers", type=int, default=MODEL.n_layers, help="model depth (40 = the GPT-3 13B shape)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--request-level", action="store_true",
+                   help="also time the request-level baseline scheduler on the same trace and engine")
     p.add_argument("--out", default="")
     return p.parse_args()
 
@@ -315,6 +317,61 @@ def run_reference(args, rank, world):
 # --------------------------------------------------------------------------- #
 # our arm
 # --------------------------------------------------------------------------- #
+def request_level_window(args, eng, trace):
+    """The request-level baseline (a batch is formed only when the previous one
+    has completely finished) on the same trace, engine and device-resident
+    path: tokens/s over a window of args.steps iterations from
+    args.window_start of its own schedule."""
+    import torch
+
+    from iteration_level_scheduling_gb300 import native
+    s = native.Scheduler(MAX_BATCH, MAX_TOKENS, kv_reserve=KV_RESERVE, mode=1, engine=eng)
+    for sp in trace:
+        s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len)
+    advance(s, args.window_start)
+    s.set_token_feedback(True)
+    n_it = args.warmup + args.steps
+    plans, batch = [], []
+    while len(plans) < n_it:
+        st, b = s.next_raw()
+        if st == 2:
+            break
+        if st == 0:
+            continue
+        words = native.check(native.lib.orca_plan_words(eng.handle, native.C.byref(b)), "orca_plan_words")
+        buf = np.zeros(words, np.int32)
+        native.check(native.lib.orca_plan_build(eng.handle, native.C.byref(b), buf.ctypes.data, words),
+                     "orca_plan_build")
+        plans.append(buf)
+        batch.append(int(b.n_req))
+        s.complete(np.zeros(b.n_req, np.int32))
+    s.close()
+    if len(plans) < n_it:
+        raise RuntimeError("trace too short for the request-level window")
+    offs = np.cumsum([0] + [((p.size + 63) // 64) * 64 for p in plans])
+    host_all = np.zeros(int(offs[-1]), np.int32)
+    for p, o in zip(plans, offs):
+        host_all[o:o + p.size] = p
+    dev_all = torch.from_numpy(host_all).cuda()
+    base = dev_all.data_ptr()
+    for i in range(args.warmup):
+        eng.run_planned(plans[i], base + 4 * int(offs[i]))
+    eng.sync()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for i in range(args.warmup, n_it):
+        eng.run_planned(plans[i], base + 4 * int(offs[i]))
+    b.record()
+    torch.cuda.synchronize()
+    eng.sync()
+    ms = a.elapsed_time(b)
+    tokens = sum(batch[args.warmup:])
+    return {"value": tokens / (ms / 1000.0), "unit": "tokens/s", "ms_per_step": ms / args.steps,
+            "mean_batch": float(np.mean(batch[args.warmup:])),
+            "scheduler": "request-level: a batch forms only when the previous one has finished"}
+
+
 def run_orca(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -482,6 +539,11 @@ def run_orca(args, rank, world, local_rank):
                "d2h_bytes_per_step": d2h / args.steps, "ms_per_step": 1000 * e2e_s / args.steps}
         s2.close()
 
+    req = None
+    if args.request_level and world == 1:
+        req = request_level_window(args, eng, trace)
+        req["iteration_level_over_request_level"] = value / req["value"]
+
     # ---------------- CPU oracle on a bounded sample (rank 0, N=1) ----------
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
@@ -509,6 +571,8 @@ def run_orca(args, rank, world, local_rank):
         "roofline": roof, "kernels": breakdown, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
         "cpu_baseline": cpu,
     }
+    if req is not None:
+        line["request_level"] = req
     del keep
     return line
 
