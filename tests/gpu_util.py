@@ -84,3 +84,89 @@ def load_context(eng, pool: torch.Tensor, cfg: synth.ModelConfig, seed: int, rid
 
 def normwise(a: np.ndarray, ref: np.ndarray) -> float:
     return float(np.max(np.abs(np.asarray(a, np.float64) - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+# --------------------------------------------------------------------------- #
+# full-depth checks on sampled requests: the oracle streams each layer's
+# weights and each sampled request's cached K/V back from the device
+# --------------------------------------------------------------------------- #
+LAYER_KEYS = ("w_qkv", "w_o", "w_1", "w_2", "b_qkv", "b_o", "b_1", "b_2", "ln1_g", "ln1_b", "ln2_g", "ln2_b")
+
+
+class DeviceLayers:
+    """Iterates over the layers of device-resident weights (the keep list of
+    bench.gpu_weights: 12 tensors per layer in LAYER_KEYS order), one layer's
+    arrays on the host at a time."""
+
+    def __init__(self, keep, n_layers):
+        self.keep, self.n_layers = keep, n_layers
+
+    def __iter__(self):
+        for l in range(self.n_layers):
+            yield {k: self.keep[12 * l + j].float().cpu().numpy() for j, k in enumerate(LAYER_KEYS)}
+
+    def __len__(self):
+        return self.n_layers
+
+
+def device_weight_dict(keep, cfg):
+    """The oracle's weight dict over bench.gpu_weights' tensors (layers streamed)."""
+    L = cfg.n_layers
+    assert len(keep) == 12 * L + 4
+    tail = [t.float().cpu().numpy() for t in keep[12 * L:]]
+    return {"tok_emb": tail[0], "pos_emb": tail[1], "lnf_g": tail[2], "lnf_b": tail[3],
+            "layers": DeviceLayers(keep, L)}
+
+
+class PoolStore:
+    """The oracle's KVStore interface over the engine's pool: a request's cached
+    rows of layer l are read from the device the first time they are needed
+    and dropped once layer l + 1 has been written."""
+
+    def __init__(self, pool, ctx_of, kv_off_of, n_layers, hidden):
+        from oracle.model import KVStore
+        self.inner = KVStore(n_layers, hidden)
+        self.pool, self.ctx_of, self.kv_off_of = pool, ctx_of, kv_off_of
+        self.k, self.v = self.inner.k, self.inner.v
+
+    def _fetch(self, rid, l):
+        if (rid, l) not in self.inner.k:
+            c, o = self.ctx_of[rid], self.kv_off_of[rid]
+            nh, d = self.pool.shape[2], self.pool.shape[4]
+            k = self.pool[l, 0, :, o:o + c, :].permute(1, 0, 2).reshape(c, nh * d).float().cpu().numpy()
+            v = self.pool[l, 1, :, o:o + c, :].permute(1, 0, 2).reshape(c, nh * d).float().cpu().numpy()
+            self.inner.load(rid, l, k, v)
+
+    def length(self, rid):
+        return self.ctx_of[rid]
+
+    def write(self, rid, layer, pos, k_rows, v_rows):
+        self._fetch(rid, layer)
+        self.inner.write(rid, layer, pos, k_rows, v_rows)
+        if layer > 0:
+            self.inner.k.pop((rid, layer - 1), None)
+            self.inner.v.pop((rid, layer - 1), None)
+
+
+def full_depth_check(eng, keep, cfg, batch, sample_idx):
+    """Run `batch` (a native.BatchDesc) through the engine and recompute the
+    requests at `sample_idx` with the oracle from the same device weights and
+    K/V.  Returns normwise errors of the final-LN hidden rows and the logits,
+    the greedy-token agreement, and the engine's argmax consistency."""
+    from oracle.model import BatchItem, iteration
+    got = eng.run_iteration(batch)
+    hid = eng.last_hidden(batch.n_req)
+    lg = eng.last_logits(batch.n_req)
+    pool = kv_pool_tensor(eng)
+    rid = batch.request_id.tolist()
+    n = batch.n_input.tolist()
+    ctx = batch.ctx_len.tolist()
+    off = np.concatenate([[0], np.cumsum(n)]).tolist()
+    toks = batch.tokens.tolist()
+    items = [BatchItem(rid[i], toks[off[i]:off[i + 1]], ctx[i]) for i in sample_idx]
+    store = PoolStore(pool, {rid[i]: ctx[i] for i in sample_idx},
+                      {rid[i]: int(batch.kv_offset[i]) for i in sample_idx}, cfg.n_layers, cfg.hidden)
+    ref = iteration(device_weight_dict(keep, cfg), cfg.n_heads, items, store)
+    return dict(h=normwise(hid[sample_idx], ref.hidden), l=normwise(lg[sample_idx], ref.logits),
+                agree=float(np.mean([got[i] == t for i, t in zip(sample_idx, ref.next_tokens)])),
+                argmax_ok=got.tolist() == lg.argmax(1).tolist())
