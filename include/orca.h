@@ -317,6 +317,9 @@ typedef struct orca_sched_config {
     int32_t token_feedback;/* 1: increment inputs are emitted as references to
                               the previous iteration's outputs (see orca_batch) */
     int32_t chunked_prefill; /* 0 or 1 (see above) */
+    int32_t n_workers;     /* batches that may be open at once ([houmin] 3.1.3
+                              pipelining); 0 or 1 = one; > 1 needs mode 0 and
+                              token_feedback 0 */
 } orca_sched_config;
 
 typedef struct orca_sched orca_sched;
@@ -343,12 +346,17 @@ int orca_sched_set_token_feedback(orca_sched *s, int32_t enable);
 /* Select the batch for the current iteration.  *status = 1 and *out filled
  * (arrays owned by the scheduler, valid until the next call) when there is
  * work; *status = 0 for an idle tick (the clock advanced, no batch); *status
- * = 2 when every request has finished. */
+ * = 2 when every request has finished; *status = 3 when nothing can be
+ * selected until an open batch completes.  A selected batch stays open until
+ * orca_sched_complete; with n_workers > 1 up to n_workers batches may be open
+ * ([houmin] 3.1.3: while one batch runs the next is scheduled), and a request
+ * in an open batch is never selected again before it completes, so open
+ * batches are disjoint.  The clock advances at each selection and idle tick.
+ * Errors: INVALID when n_workers batches are already open. */
 int orca_sched_next(orca_sched *s, orca_batch *out, int32_t *status);
 
-/* Report the iteration's next tokens (HOST, one per request of the batch last
- * returned by orca_sched_next); advances the clock and retires finished
- * requests. */
+/* Report the next tokens (HOST, one per request) of the OLDEST open batch;
+ * retires its finished requests. */
 int orca_sched_complete(orca_sched *s, const int32_t *next_tokens);
 
 /* Cancel a waiting or running request between iterations ([houmin] 3.1.1: a
@@ -356,8 +364,8 @@ int orca_sched_complete(orca_sched *s, const int32_t *next_tokens);
  * again, its K/V reservation is freed immediately (also in request-level
  * mode), its tokens so far stay readable (state 3), and a request-level batch
  * whose remaining members are all done completes at once.
- * Errors: NOT_FOUND (unknown id), INVALID (a batch is open, or the request is
- * finished or already cancelled). */
+ * Errors: NOT_FOUND (unknown id), INVALID (the request is in an open batch,
+ * finished, or already cancelled). */
 int orca_sched_cancel(orca_sched *s, int64_t id);
 
 typedef struct orca_sched_stats {
@@ -382,9 +390,10 @@ int orca_sched_request_get(orca_sched *s, int64_t id, orca_request_info *out);
 /* Generated tokens of a request (HOST buffer of cap entries). */
 int orca_sched_request_tokens(orca_sched *s, int64_t id, int32_t *out, int32_t cap, int32_t *n_out);
 
-/* Serve loop: repeat next -> orca_run_iteration -> complete until every
- * request has finished or max_iterations engine iterations ran.  The engine is
- * the one the scheduler was created with. */
+/* Serve loop: keep up to n_workers batches selected, run the oldest with
+ * orca_run_iteration and complete it, until every request has finished or
+ * max_iterations engine iterations ran.  The engine is the one the scheduler
+ * was created with. */
 int orca_sched_run(orca_sched *s, int64_t max_iterations);
 
 #ifdef __cplusplus

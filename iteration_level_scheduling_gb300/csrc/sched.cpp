@@ -26,10 +26,15 @@
 // still in its prompt whose remaining prompt exceeds the budget left takes the
 // budget left as a chunk (>= 1 token) and the scan stops; only the iteration
 // that processes its last prompt token yields a token.
+// Pipelining (houmin 3.1.3, n_workers): up to n_workers batches may be open
+// (selected, not yet completed); a request in an open batch is not selectable,
+// so open batches are disjoint, and completions come oldest first.  The clock
+// advances when a batch is selected or an idle tick passes.
 #include <algorithm>
 #include <cstring>
 #include <memory>
 #include <new>
+#include <numeric>
 #include <unordered_map>
 #include <vector>
 
@@ -55,6 +60,7 @@ struct Request {
     int64_t last_iter = -1;  // engine iteration this request last ran in
     int32_t last_index = -1; // its index in that iteration's batch
     int32_t chunk = 0;       // its input rows in the batch being formed
+    bool in_flight = false;  // member of an open batch
 
     // prompt tokens remain to be processed (never for requests entered with ctx0 > 0)
     bool in_prompt() const { return ctx0 == 0 && ctx < (int32_t)prompt.size(); }
@@ -70,6 +76,12 @@ bool fcfs_less(const Request *a, const Request *b) {
 
 }  // namespace
 
+struct OpenBatch {
+    int64_t clock;  // the clock at its selection
+    std::vector<Request *> reqs;
+    std::vector<int32_t> chunk;  // each member's input rows in it
+};
+
 struct orca_sched {
     orca_sched_config cfg{};
     orca_engine *eng = nullptr;
@@ -77,8 +89,8 @@ struct orca_sched {
     std::unordered_map<int64_t, std::unique_ptr<Request>> by_id;
     std::vector<Request *> live;  // unfinished requests, sorted by (arrival, id)
     std::vector<Request *> current_batch;  // request-level mode only
-    std::vector<Request *> batch;          // batch of the last orca_sched_next
-    bool batch_open = false;
+    std::vector<Request *> batch;          // batch being formed by orca_sched_next
+    std::vector<OpenBatch> open;           // selected, not yet completed; oldest first
     int64_t clock = 0, iterations = 0, generated = 0, finished = 0, cancelled = 0;
     int64_t feedback_since = 0;  // first iteration run with token feedback on
     // descriptor arrays handed out by orca_sched_next
@@ -160,10 +172,14 @@ int orca_sched_create(const orca_sched_config *cfg, orca_engine *eng, orca_sched
     if (cfg->max_batch <= 0 || cfg->max_tokens <= 0 || cfg->kv_reserve < 0 || (cfg->mode != 0 && cfg->mode != 1) ||
         (cfg->chunked_prefill != 0 && cfg->chunked_prefill != 1) || (cfg->chunked_prefill && cfg->mode != 0))
         return ORCA_ERR_INVALID;
+    // pipelining: iteration-level only, and increment inputs must be literal tokens
+    const int32_t nw = cfg->n_workers ? cfg->n_workers : 1;
+    if (nw < 1 || nw > 64 || (nw > 1 && (cfg->mode != 0 || cfg->token_feedback))) return ORCA_ERR_INVALID;
     if (!eng && cfg->kv_slots <= 0) return ORCA_ERR_INVALID;
     orca_sched *s = new (std::nothrow) orca_sched();
     if (!s) return ORCA_ERR_OOM;
     s->cfg = *cfg;
+    s->cfg.n_workers = nw;
     s->eng = eng;
     if (!eng) s->own_pool.reset(new orca::KVPool(cfg->kv_slots));
     *out = s;
@@ -220,7 +236,7 @@ int orca_sched_submit(orca_sched *s, int64_t id, double arrival, const int32_t *
 }
 
 int orca_sched_set_token_feedback(orca_sched *s, int32_t enable) {
-    if (!s) return ORCA_ERR_INVALID;
+    if (!s || (enable && s->cfg.n_workers > 1)) return ORCA_ERR_INVALID;
     if (enable && !s->cfg.token_feedback) s->feedback_since = s->iterations;
     s->cfg.token_feedback = enable ? 1 : 0;
     return ORCA_OK;
@@ -228,8 +244,8 @@ int orca_sched_set_token_feedback(orca_sched *s, int32_t enable) {
 
 int orca_sched_next(orca_sched *s, orca_batch *out, int32_t *status) {
     if (!s || !out || !status) return ORCA_ERR_INVALID;
-    if (s->batch_open) return ORCA_ERR_INVALID;  // previous batch not completed
-    if (s->live.empty()) {
+    if ((int32_t)s->open.size() >= s->cfg.n_workers) return ORCA_ERR_INVALID;  // complete one first
+    if (s->live.empty() && s->open.empty()) {
         *status = 2;
         return ORCA_OK;
     }
@@ -237,6 +253,7 @@ int orca_sched_next(orca_sched *s, orca_batch *out, int32_t *status) {
     std::vector<Request *> cands;
     for (Request *r : s->live) {
         if (r->arrival > k) break;  // live is sorted by arrival first
+        if (r->in_flight) continue;
         if (s->cfg.mode == 1 && r->state != W_WAITING) continue;
         cands.push_back(r);  // (live holds no finished or cancelled request)
     }
@@ -252,6 +269,10 @@ int orca_sched_next(orca_sched *s, orca_batch *out, int32_t *status) {
             }
     }
     if (s->batch.empty()) {
+        if (!s->open.empty()) {  // all runnable requests are in flight: complete one first
+            *status = 3;
+            return ORCA_OK;
+        }
         s->clock++;
         *status = 0;
         return ORCA_OK;
@@ -285,16 +306,25 @@ int orca_sched_next(orca_sched *s, orca_batch *out, int32_t *status) {
     out->ctx_len = s->d_ctx.data();
     out->kv_offset = s->d_kv.data();
     out->tokens = s->d_tok.data();
-    s->batch_open = true;
+    OpenBatch ob{s->clock, s->batch, {}};
+    for (Request *r : s->batch) {
+        r->in_flight = true;
+        ob.chunk.push_back(r->chunk);
+    }
+    s->open.push_back(std::move(ob));
+    s->clock++;
     *status = 1;
     return ORCA_OK;
 }
 
 int orca_sched_complete(orca_sched *s, const int32_t *next_tokens) {
-    if (!s || !next_tokens || !s->batch_open) return ORCA_ERR_INVALID;
-    for (size_t i = 0; i < s->batch.size(); ++i) {
-        Request *r = s->batch[i];
-        r->ctx += r->chunk;
+    if (!s || !next_tokens || s->open.empty()) return ORCA_ERR_INVALID;
+    OpenBatch ob = std::move(s->open.front());  // the oldest open batch
+    s->open.erase(s->open.begin());
+    for (size_t i = 0; i < ob.reqs.size(); ++i) {
+        Request *r = ob.reqs[i];
+        r->in_flight = false;
+        r->ctx += ob.chunk[i];
         r->last_iter = s->iterations;
         r->last_index = (int32_t)i;
         if (r->in_prompt()) continue;  // a prompt chunk before the last: its output is not a token
@@ -303,7 +333,7 @@ int orca_sched_complete(orca_sched *s, const int32_t *next_tokens) {
         s->generated++;
         if (r->done()) {
             r->state = W_FINISHED;
-            r->finished_at = s->clock;
+            r->finished_at = ob.clock;
             s->finished++;
             if (s->cfg.mode == 0) s->kv_free(r->id);
         }
@@ -311,18 +341,16 @@ int orca_sched_complete(orca_sched *s, const int32_t *next_tokens) {
     s->close_request_batch();
     s->live.erase(std::remove_if(s->live.begin(), s->live.end(), [](Request *r) { return r->state == W_FINISHED; }),
                   s->live.end());
-    s->batch_open = false;
     s->iterations++;
-    s->clock++;
     return ORCA_OK;
 }
 
 int orca_sched_cancel(orca_sched *s, int64_t id) {
     if (!s) return ORCA_ERR_INVALID;
-    if (s->batch_open) return ORCA_ERR_INVALID;  // only between iterations
     auto it = s->by_id.find(id);
     if (it == s->by_id.end()) return ORCA_ERR_NOT_FOUND;
     Request *r = it->second.get();
+    if (r->in_flight) return ORCA_ERR_INVALID;  // its batch is still open
     if (r->state != W_WAITING && r->state != W_RUNNING) return ORCA_ERR_INVALID;
     if (r->kv_off >= 0) s->kv_free(r->id);
     r->state = W_CANCELLED;
@@ -375,22 +403,50 @@ int orca_sched_request_tokens(orca_sched *s, int64_t id, int32_t *out, int32_t c
 
 int orca_sched_run(orca_sched *s, int64_t max_iterations) {
     if (!s || !s->eng) return ORCA_ERR_INVALID;
+    // copies of the open batches' descriptors (the scheduler reuses its arrays)
+    struct Desc {
+        std::vector<int64_t> id, kv;
+        std::vector<int32_t> phase, n, ctx, tok;
+        orca_batch view() {
+            return orca_batch{(int32_t)id.size(), id.data(), phase.data(), n.data(), ctx.data(), kv.data(), tok.data()};
+        }
+    };
+    std::vector<Desc> queued;  // oldest first
+    auto abandon = [&]() {      // the open batches are dropped; the requests keep their state
+        for (OpenBatch &ob : s->open)
+            for (Request *r : ob.reqs) r->in_flight = false;
+        s->open.clear();
+    };
     std::vector<int32_t> next;
     int64_t done_iters = 0;
     while (done_iters < max_iterations) {
-        orca_batch b{};
-        int32_t status = 0;
-        int rc = orca_sched_next(s, &b, &status);
-        if (rc != ORCA_OK) return rc;
-        if (status == 2) break;
-        if (status == 0) continue;
+        // select until n_workers batches are open or nothing more can be selected now
+        while ((int32_t)s->open.size() < s->cfg.n_workers &&
+               done_iters + (int64_t)queued.size() < max_iterations) {
+            orca_batch b{};
+            int32_t status = 0;
+            int rc = orca_sched_next(s, &b, &status);
+            if (rc != ORCA_OK) {
+                abandon();
+                return rc;
+            }
+            if (status == 0) continue;  // idle tick
+            if (status != 1) break;     // 2: every request finished; 3: wait for an open batch
+            const int64_t rows = std::accumulate(b.n_input, b.n_input + b.n_req, (int64_t)0);
+            queued.push_back(Desc{{b.request_id, b.request_id + b.n_req}, {b.kv_offset, b.kv_offset + b.n_req},
+                                  {b.phase, b.phase + b.n_req}, {b.n_input, b.n_input + b.n_req},
+                                  {b.ctx_len, b.ctx_len + b.n_req}, {b.tokens, b.tokens + rows}});
+        }
+        if (queued.empty()) break;
+        orca_batch b = queued.front().view();
         next.resize(b.n_req);
-        rc = orca_run_iteration(s->eng, &b, next.data());
+        int rc = orca_run_iteration(s->eng, &b, next.data());
         if (rc != ORCA_OK) {
-            s->batch_open = false;  // the batch is abandoned; state unchanged
+            abandon();
             return rc;
         }
         rc = orca_sched_complete(s, next.data());
+        queued.erase(queued.begin());
         if (rc != ORCA_OK) return rc;
         ++done_iters;
     }

@@ -83,7 +83,7 @@ class KernelTime(C.Structure):
 class SchedConfig(C.Structure):
     _fields_ = [("max_batch", C.c_int32), ("max_tokens", C.c_int32), ("kv_slots", C.c_int64),
                 ("kv_reserve", C.c_int32), ("mode", C.c_int32), ("token_feedback", C.c_int32),
-                ("chunked_prefill", C.c_int32)]
+                ("chunked_prefill", C.c_int32), ("n_workers", C.c_int32)]
 
 
 class SchedStats(C.Structure):
@@ -312,9 +312,10 @@ class Scheduler:
     ``engine=None`` it keeps its own host-side K/V pool and needs no GPU."""
 
     def __init__(self, max_batch: int, max_tokens: int, kv_slots: int = 0, kv_reserve: int = 0, mode: int = 0,
-                 token_feedback: bool = False, engine: Optional[Engine] = None, chunked_prefill: bool = False):
+                 token_feedback: bool = False, engine: Optional[Engine] = None, chunked_prefill: bool = False,
+                 n_workers: int = 1):
         self.cfg = SchedConfig(max_batch, max_tokens, kv_slots, kv_reserve, mode, int(token_feedback),
-                               int(chunked_prefill))
+                               int(chunked_prefill), int(n_workers))
         self._h = P()
         self.engine = engine
         check(lib.orca_sched_create(C.byref(self.cfg), engine.handle if engine else None, C.byref(self._h)),
@@ -343,7 +344,7 @@ class Scheduler:
         check(lib.orca_sched_set_token_feedback(self._h, int(enable)), "orca_sched_set_token_feedback")
 
     def next(self):
-        """Returns (status, BatchDesc or None); status 1 batch, 0 idle tick, 2 done."""
+        """Returns (status, BatchDesc or None); status 1 batch, 0 idle tick, 2 done, 3 wait for an open batch."""
         b = Batch()
         st = C.c_int32()
         check(lib.orca_sched_next(self._h, C.byref(b), C.byref(st)), "orca_sched_next")

@@ -52,6 +52,14 @@ there; its chunks run in consecutive selections, each with the tokens
 processed so far as context; only the iteration that processes the last
 prompt token yields a generated token (the engine's output for an earlier
 chunk is ignored).  Prompts longer than max_tokens become admissible.
+
+Pipelining ([houmin] 3.1.3, ``n_workers``: while one batch runs, the next is
+scheduled; a request whose batch is still running is not selected again, so
+the batches in flight are disjoint).  Up to ``n_workers`` selected batches may
+be open; completions come oldest first.  The clock advances when a batch is
+selected and at an idle tick; an iteration with nothing selectable while
+batches are open just waits for the oldest to complete.  With n_workers = 1
+this is the plain loop above.
 """
 
 from __future__ import annotations
@@ -78,6 +86,7 @@ class Req:
     admitted_at: Optional[int] = None
     finished_at: Optional[int] = None
     chunk: int = 0  # input rows of the request in the batch being formed
+    in_flight: bool = False  # member of an open batch
 
     @property
     def done(self) -> bool:
@@ -94,6 +103,14 @@ class Req:
 
     def input_tokens(self) -> List[int]:
         return list(self.prompt[self.ctx:self.ctx + self.chunk]) if self.in_prompt else [self.pending]
+
+
+@dataclasses.dataclass
+class OpenBatch:
+    k: int  # the clock at its selection
+    batch: List[Req]
+    chunks: List[int]
+    record: "Iteration" = None
 
 
 @dataclasses.dataclass
@@ -120,11 +137,15 @@ class Iteration:
 
 class Scheduler:
     def __init__(self, max_batch: int, max_tokens: int, kv_slots: int, kv_reserve: int = 0,
-                 mode: str = "iteration", chunked_prefill: bool = False):
+                 mode: str = "iteration", chunked_prefill: bool = False, n_workers: int = 1):
         if mode not in ("iteration", "request"):
             raise ValueError(mode)
         if chunked_prefill and mode != "iteration":
             raise ValueError("chunked prefill is an iteration-level option")
+        if n_workers < 1 or (n_workers > 1 and mode != "iteration"):
+            raise ValueError("pipelining is an iteration-level option")
+        self.n_workers = n_workers
+        self.open: List[OpenBatch] = []  # selected, not yet completed; oldest first
         self.max_batch, self.max_tokens, self.kv_reserve, self.mode = max_batch, max_tokens, kv_reserve, mode
         self.chunked_prefill = chunked_prefill
         self.cancelled_total = 0
@@ -162,7 +183,7 @@ class Scheduler:
         return r
 
     def _ordered(self, k: int) -> List[Req]:
-        c = [r for r in self.reqs if r.state in ("waiting", "running") and r.arrival <= k]
+        c = [r for r in self.reqs if r.state in ("waiting", "running") and r.arrival <= k and not r.in_flight]
         c.sort(key=lambda r: (r.arrival, r.rid))
         return c
 
@@ -188,40 +209,62 @@ class Scheduler:
         return batch
 
     def select(self) -> List[Req]:
-        """Batch for the current iteration ``self.k`` (empty = idle tick)."""
+        """Select the batch of iteration ``self.k``; a non-empty batch is open
+        until ``complete`` and advances the clock (empty: nothing selectable)."""
+        if len(self.open) >= self.n_workers:
+            raise RuntimeError("n_workers batches are open")
         k = self.k
         if self.mode == "iteration":
-            return self._admit_prefix(self._ordered(k), k)
-        if not self.current_batch:
-            self.current_batch = self._admit_prefix([r for r in self._ordered(k) if r.state == "waiting"], k)
-        batch = [r for r in self.current_batch if r.state == "running" and not r.done]
-        for r in batch:
-            r.chunk = r.n_input()
+            batch = self._admit_prefix(self._ordered(k), k)
+        else:
+            if not self.current_batch:
+                self.current_batch = self._admit_prefix([r for r in self._ordered(k) if r.state == "waiting"], k)
+            batch = [r for r in self.current_batch if r.state == "running" and not r.done]
+            for r in batch:
+                r.chunk = r.n_input()
+        if batch:
+            for r in batch:
+                r.in_flight = True
+            self.open.append(OpenBatch(k, batch, [r.chunk for r in batch]))
+            self.k += 1
         return batch
 
+    def _entry(self, batch: List[Req]) -> OpenBatch:
+        for e in self.open:
+            if e.batch is batch:
+                return e
+        raise ValueError("not an open batch")
+
     def describe(self, batch: List[Req]) -> Iteration:
+        e = self._entry(batch)
         toks = []
         for r in batch:
             toks += r.input_tokens()
-        return Iteration(self.k, [r.rid for r in batch], [0 if r.ctx == 0 else 1 for r in batch],
-                         [r.chunk for r in batch], [r.ctx for r in batch], [r.kv_off for r in batch], toks)
+        e.record = Iteration(e.k, [r.rid for r in batch], [0 if r.ctx == 0 else 1 for r in batch], list(e.chunks),
+                             [r.ctx for r in batch], [r.kv_off for r in batch], toks)
+        return e.record
 
     def complete(self, batch: List[Req], next_tokens: Sequence[int]) -> None:
-        """Engine returned: append tokens, advance contexts, retire finished requests."""
-        for r, t in zip(batch, next_tokens):
-            r.ctx += r.chunk
+        """Engine returned for the oldest open batch: append tokens, advance
+        contexts, retire finished requests."""
+        e = self._entry(batch)
+        if e is not self.open[0]:
+            raise ValueError("batches complete oldest first")
+        self.open.pop(0)
+        for r, t, n in zip(batch, next_tokens, e.chunks):
+            r.in_flight = False
+            r.ctx += n
             if r.in_prompt:
                 continue  # a prompt chunk before the last: its output is not a token
             r.generated.append(int(t))
             r.pending = int(t)
             self.generated_total += 1
             if r.done:
-                r.state, r.finished_at = "finished", self.k
+                r.state, r.finished_at = "finished", e.k
                 if self.mode == "iteration":
                     self.pool.free(r.rid)
         self._close_request_batch()
         self.iterations += 1
-        self.k += 1
 
     def _close_request_batch(self) -> None:
         """Request-level: the batch completes when every member is done or
@@ -239,8 +282,8 @@ class Scheduler:
         r = next((q for q in self.reqs if q.rid == rid), None)
         if r is None:
             raise KeyError(rid)
-        if r.state not in ("waiting", "running") or (self.mode == "request" and r.done):
-            raise ValueError("request is not live")
+        if r.state not in ("waiting", "running") or (self.mode == "request" and r.done) or r.in_flight:
+            raise ValueError("request is not live, or its batch is still open")
         if r.kv_off is not None:
             self.pool.free(r.rid)
         r.state = "cancelled"
@@ -256,35 +299,42 @@ class Scheduler:
 
 def run(specs, max_batch: int, max_tokens: int, kv_slots: int, kv_reserve: int = 0, mode: str = "iteration",
         token_fn: Optional[Callable[[Iteration], Sequence[int]]] = None, max_iters: int = 10 ** 7,
-        chunked_prefill: bool = False, cancel_at: Optional[dict] = None):
+        chunked_prefill: bool = False, cancel_at: Optional[dict] = None, n_workers: int = 1):
     """Drive a scheduler over request specs until every request finished.
 
     ``token_fn(iteration)`` plays the engine and returns one next token per
     request (default: a deterministic dummy).  ``cancel_at`` maps a clock value
-    to the request ids cancelled just before that iteration's selection (ids
-    that are no longer live are skipped).  Returns (scheduler, list of
-    Iteration records, one per engine call).
+    to the request ids cancelled just before a selection at that clock (ids
+    that are no longer live, or whose batch is open, are skipped).  With
+    ``n_workers`` > 1 up to that many batches are selected before the oldest
+    completes.  Returns (scheduler, list of Iteration records, one per engine
+    call, in selection order).
     """
-    s = Scheduler(max_batch, max_tokens, kv_slots, kv_reserve, mode, chunked_prefill)
+    s = Scheduler(max_batch, max_tokens, kv_slots, kv_reserve, mode, chunked_prefill, n_workers)
     for sp in specs:
         s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len, sp.ctx0)
     if token_fn is None:
         token_fn = lambda it: [(rid * 31 + it.k) % 50000 for rid in it.rids]
     records = []
-    while s.unfinished() and s.k < max_iters:
-        for rid in (cancel_at or {}).get(s.k, ()):
-            r = next((q for q in s.reqs if q.rid == rid), None)
-            if r is not None and r.state in ("waiting", "running") and not (s.mode == "request" and r.done):
-                s.cancel(rid)
-        if not s.unfinished():
+    while True:
+        if len(s.open) < s.n_workers and s.unfinished() and s.k < max_iters:
+            for rid in (cancel_at or {}).get(s.k, ()):
+                r = next((q for q in s.reqs if q.rid == rid), None)
+                if (r is not None and r.state in ("waiting", "running") and not r.in_flight
+                        and not (s.mode == "request" and r.done)):
+                    s.cancel(rid)
+            if s.unfinished():
+                batch = s.select()
+                if batch:
+                    records.append(s.describe(batch))
+                    continue
+                if not s.open:
+                    s.idle()
+                    continue
+        if not s.open:
             break
-        batch = s.select()
-        if not batch:
-            s.idle()
-            continue
-        it = s.describe(batch)
-        records.append(it)
-        s.complete(batch, token_fn(it))
+        e = s.open[0]
+        s.complete(e.batch, token_fn(e.record))
     return s, records
 
 

@@ -31,27 +31,34 @@ def built():
 
 
 def run_trace_teacher_forced(cfg, w, specs, max_batch, mode, kv_slots, max_tokens=4096, feedback=False,
-                             chunked=False, cancel_at=None):
+                             chunked=False, cancel_at=None, n_workers=1):
     from iteration_level_scheduling_gb300 import native
     eng = make_engine(cfg, w, max_tokens, max_batch, kv_slots)
     s = native.Scheduler(max_batch, max_tokens, mode=mode, engine=eng, token_feedback=feedback,
-                         chunked_prefill=chunked)
+                         chunked_prefill=chunked, n_workers=n_workers)
     for sp in specs:
         s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len, sp.ctx0)
     store = KVStore(cfg.n_layers, cfg.hidden)
     worst_h = worst_l = 0.0
     agree = total = iters = chunks = 0
     prev_next = {}
+    queue = []  # selected batches not yet run, oldest first (n_workers of them at most)
     while True:
-        for rid in (cancel_at or {}).get(s.stats().clock, ()):
-            if s.request(rid).state in (0, 1):
-                s.cancel(rid)
-                store.drop(rid)
-        st, b = s.next()
-        if st == 2:
+        while len(queue) < n_workers:
+            for rid in (cancel_at or {}).get(s.stats().clock, ()):
+                if s.request(rid).state in (0, 1):
+                    s.cancel(rid)
+                    store.drop(rid)
+            st, b = s.next()
+            if st == 1:
+                queue.append(b)
+                continue
+            if st == 0:
+                continue
             break
-        if st == 0:
-            continue
+        if not queue:
+            break
+        b = queue.pop(0)
         toks = b.tokens.tolist()
         items, p = [], 0
         resolved = []
@@ -103,6 +110,39 @@ def test_tiny_fp32_trace_token_feedback():
     w = synth.make_weights(cfg, 1, random_affine=True)
     r = run_trace_teacher_forced(cfg, w, synth.tiny_requests(1), 4, 0, kv_slots=4 * 128, feedback=True)
     assert r["worst_l"] <= TOL_FP32 and r["agree"] == 1.0, r
+
+
+def test_tiny_fp32_pipelined_two_workers():
+    """Two batches open at once ([houmin] 3.1.3 n_workers = 2): the next batch is
+    selected (from the requests not in flight) before the previous one runs;
+    every iteration matches the oracle."""
+    cfg = synth.TINY
+    w = synth.make_weights(cfg, 3, random_affine=True)
+    r = run_trace_teacher_forced(cfg, w, synth.tiny_requests(3), 4, 0, kv_slots=4 * 128, n_workers=2)
+    assert r["generated"] == 155
+    assert r["worst_h"] <= TOL_FP32 and r["worst_l"] <= TOL_FP32, r
+    assert r["agree"] >= 0.99, r
+
+
+def test_serve_loop_tokens_independent_of_batching():
+    """Selective batching: a request's greedy tokens do not depend on which
+    requests share its iterations, so the C serve loop gives every request the
+    same tokens with one or two open batches (different batch compositions)."""
+    from iteration_level_scheduling_gb300 import native
+    cfg = synth.TINY
+    w = synth.make_weights(cfg, 4, random_affine=True)
+    out = []
+    for nw in (1, 2):
+        eng = make_engine(cfg, w, 4096, 4, 4 * 128)
+        s = native.Scheduler(4, 4096, engine=eng, n_workers=nw)
+        for sp in synth.tiny_requests(4):
+            s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len)
+        s.run()
+        out.append({sp.rid: s.tokens(sp.rid).tolist() for sp in synth.tiny_requests(4)})
+        assert s.stats().iterations == (50 if nw == 1 else s.stats().iterations)
+        s.close()
+        eng.close()
+    assert out[0] == out[1]
 
 
 def test_tiny_fp32_chunked_prefill_and_cancellation():

@@ -42,13 +42,14 @@ def drive_native(native, specs, max_batch, max_tokens, kv_slots, kv_reserve=0, m
         s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len, sp.ctx0)
     recs = []
     while True:
+        clock = s.stats().clock  # the selection's clock (a selection advances it)
         st, b = s.next()
         if st == 2:
             break
         if st == 0:
             continue
-        toks = [(int(r) * 31 + s.stats().clock) % 50000 for r in b.request_id]
-        recs.append((s.stats().clock, b))
+        toks = [(int(r) * 31 + clock) % 50000 for r in b.request_id]
+        recs.append((clock, b))
         s.complete(toks)
     return s, recs
 
@@ -164,13 +165,14 @@ def drive_native_ext(native, specs, max_batch, max_tokens, kv_slots, mode=0, chu
             live = info.state in (0, 1) and not (mode == 1 and info.n_generated >= specs[rid].out_len)
             if live:
                 s.cancel(rid)
+        clock = s.stats().clock
         st, b = s.next()
         if st == 2:
             break
         if st == 0:
             continue
-        toks = [(int(r) * 31 + s.stats().clock) % 50000 for r in b.request_id]
-        recs.append((s.stats().clock, b))
+        toks = [(int(r) * 31 + clock) % 50000 for r in b.request_id]
+        recs.append((clock, b))
         s.complete(toks)
     return s, recs
 
@@ -234,3 +236,61 @@ def test_cancel_errors(native):
     assert s.tokens(0).tolist() == [5]
     with pytest.raises(native.OrcaError):        # chunked prefill is an iteration-level option
         native.Scheduler(2, 4096, kv_slots=100, mode=1, chunked_prefill=True)
+
+
+def drive_native_pipelined(native, specs, max_batch, max_tokens, kv_slots, n_workers):
+    s = native.Scheduler(max_batch, max_tokens, kv_slots, 0, 0, False, n_workers=n_workers)
+    for sp in specs:
+        s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len, sp.ctx0)
+    recs, queue = [], []
+    while True:
+        while len(queue) < n_workers:
+            clock = s.stats().clock
+            st, b = s.next()
+            if st == 1:
+                queue.append((clock, b))
+                recs.append((clock, b))
+                continue
+            if st == 0:
+                continue
+            break
+        if not queue:
+            break
+        clock, b = queue.pop(0)
+        s.complete([(int(r) * 31 + clock) % 50000 for r in b.request_id])
+    return s, recs
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_native_matches_oracle_pipelined(native, seed):
+    rnd = random.Random(500 + seed)
+    trace = synth.poisson_trace(seed, n=60, rate=rnd.choice([0.3, 1.0, 3.0]), prompt_range=(1, 40),
+                                out_range=(1, 30), vocab=1000)
+    mb, mt = rnd.randint(1, 8), rnd.randint(40, 200)
+    for nw in (2, 3):
+        s, recs = drive_native_pipelined(native, trace, mb, mt, 5000, nw)
+        _, orecs = osched.run(trace, mb, mt, 5000, n_workers=nw,
+                              token_fn=lambda it: [(rid * 31 + it.k) % 50000 for rid in it.rids])
+        assert_same(recs, orecs)
+        assert s.stats().kv_reserved == 0
+
+
+def test_pipelined_protocol(native):
+    s = native.Scheduler(1, 4096, kv_slots=100, n_workers=2)
+    s.submit(0, 0.0, [1], 2)
+    s.submit(1, 0.0, [2], 2)
+    st, b = s.next()
+    assert st == 1 and b.request_id.tolist() == [0]
+    st, b = s.next()
+    assert st == 1 and b.request_id.tolist() == [1]
+    with pytest.raises(native.OrcaError):  # two batches already open
+        s.next()
+    s.complete([5])                         # completes the oldest: request 0
+    assert s.tokens(0).tolist() == [5] and s.tokens(1).tolist() == []
+    st, b = s.next()
+    assert st == 1 and b.request_id.tolist() == [0] and b.tokens.tolist() == [5]
+    with pytest.raises(native.OrcaError):   # request 1's batch is still open
+        s.cancel(1)
+    for bad in (dict(mode=1), dict(token_feedback=True)):
+        with pytest.raises(native.OrcaError):
+            native.Scheduler(2, 4096, kv_slots=100, n_workers=2, **bad)

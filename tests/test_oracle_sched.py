@@ -340,3 +340,56 @@ def test_chunked_prefill_invariants_random_traces():
             assert r.state == "finished" and len(r.generated) == r.out_len
             assert r.generated[0] == (r.rid * 31 + first_token_at[r.rid]) % 50000
         assert s.pool.used() == 0
+
+
+# --------------------------------------------------------------------------- #
+# pipelining ([houmin] 3.1.3 n_workers): open batches are disjoint
+# --------------------------------------------------------------------------- #
+def test_pipelined_worked_example():
+    specs = [synth.RequestSpec(i, 0.0, [1], L) for i, L in enumerate([2, 2, 1, 3])]
+    s, recs = sched.run(specs, 2, 4096, 100, n_workers=2)
+    assert [(r.k, r.rids, r.ctx) for r in recs] == [
+        (0, [0, 1], [0, 0]),   # A
+        (1, [2, 3], [0, 0]),   # B, selected while A runs: 0 and 1 are in flight
+        (2, [0, 1], [1, 1]),   # after A completed
+        (3, [3], [1]),         # after B completed (2 finished); 0, 1 in flight
+        (4, [3], [2]),         # nothing else selectable at clock 4 until the previous batch completed
+    ]
+    assert all(len(r.generated) == r.out_len for r in s.reqs) and s.pool.used() == 0
+
+
+def test_pipelined_invariants_random_traces():
+    for seed in range(6):
+        rnd = random.Random(90 + seed)
+        trace = synth.poisson_trace(seed, n=60, rate=rnd.choice([0.3, 1.0, 3.0]), prompt_range=(1, 40),
+                                    out_range=(1, 30), vocab=100)
+        mb, mt = rnd.randint(1, 8), rnd.randint(40, 200)
+        s1, r1 = sched.run(trace, mb, mt, 5000)
+        s1b, r1b = sched.run(trace, mb, mt, 5000, n_workers=1)
+        assert [vars(a) for a in r1] == [vars(b) for b in r1b]  # one worker is the plain loop
+        for nw in (2, 3):
+            s = sched.Scheduler(mb, mt, 5000, n_workers=nw)
+            for sp in trace:
+                s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len)
+            recs, most_open = [], 0
+            while True:
+                if len(s.open) < nw and s.unfinished():
+                    open_ids = [{r.rid for r in e.batch} for e in s.open]
+                    batch = s.select()
+                    if batch:  # a new batch shares no request with the batches still open
+                        assert all(not ({r.rid for r in batch} & o) for o in open_ids)
+                        recs.append(s.describe(batch))
+                        most_open = max(most_open, len(s.open))
+                        continue
+                    if not s.open:
+                        s.idle()
+                        continue
+                if not s.open:
+                    break
+                e = s.open[0]
+                s.complete(e.batch, [7] * len(e.batch))
+            assert most_open == nw
+            for r in s.reqs:
+                assert r.state == "finished" and len(r.generated) == r.out_len
+            assert s.pool.used() == 0
+            assert sum(len(r.rids) for r in recs) == sum(sp.out_len for sp in trace)
