@@ -372,6 +372,18 @@ def request_level_window(args, eng, trace):
             "scheduler": "request-level: a batch forms only when the previous one has finished"}
 
 
+def split_by_prefill(work, it_ms, fr):
+    """Iterations with only increment rows vs iterations that also carry prompt rows."""
+    out = {}
+    for name, sel in (("decode_only", lambda w: w["R"] == w["B"]), ("with_prefill", lambda w: w["R"] > w["B"])):
+        idx = [i for i, w in enumerate(work) if sel(w)]
+        if idx:
+            out[name] = {"iterations": len(idx), "mean_ms": float(np.mean([it_ms[i] for i in idx])),
+                         "mean_rows": float(np.mean([work[i]["R"] for i in idx])),
+                         "mean_frac": float(np.mean([fr[i] for i in idx]))}
+    return out
+
+
 def run_orca(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -567,7 +579,8 @@ def run_orca(args, rank, world, local_rank):
                                "peaks": {"hbm_GBs": peaks["hbm"], "bf16_TFLOPs_sustained": peaks["tc_sus"],
                                          "source": peaks["src"]},
                                "mean_batch": float(np.mean([w["B"] for w in work[args.warmup:]])),
-                               "mean_rows": float(np.mean([w["R"] for w in work[args.warmup:]]))},
+                               "mean_rows": float(np.mean([w["R"] for w in work[args.warmup:]])),
+                               "by_kind": split_by_prefill(work[args.warmup:], it_ms, fr)},
         "roofline": roof, "kernels": breakdown, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
         "cpu_baseline": cpu,
     }

@@ -772,7 +772,7 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
                         }
                     } else {  // 16-token boxes at 2 KiB (16-row) offsets keep the 128-byte swizzle phase
                         const int nq = (ntok + 15) / 16;
-                        mbar_arrive_expect_tx(&sm.full[s], (uint32_t)nq * (kStage / 4));
+                        mbar_arrive_expect_tx(&sm.full[s], (uint32_t)nq * (kStage / (kMdTok / 16)));
                         for (int j = 0; j < nq; ++j)
 #pragma unroll
                             for (int b = 0; b < NB; ++b) {
