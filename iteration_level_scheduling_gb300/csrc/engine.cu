@@ -101,6 +101,8 @@ struct orca_engine {
     size_t part_cap = 0;
     float *attn_part = nullptr;
     int *attn_cnt = nullptr;
+    float *sk_part = nullptr;  // stream-K GEMM: partial tiles of cut tiles
+    int *sk_cnt = nullptr;     // stream-K GEMM: per-tile arrival counters
     int64_t attn_part_work = 0;
     unsigned *d_err = nullptr, *h_err = nullptr;
 
@@ -116,7 +118,7 @@ struct orca_engine {
 
     ~orca_engine() {
         for (cudaEvent_t e : events) cudaEventDestroy(e);
-        void *dev[] = {kv, x, y32, logits, h, qkv, attn, f, y, next, d_plan, part, attn_part, attn_cnt, d_err,
+        void *dev[] = {kv, x, y32, logits, h, qkv, attn, f, y, next, d_plan, part, attn_part, attn_cnt, sk_part, sk_cnt, d_err,
                        packed_buf};
         for (void *p : dev)
             if (p) cudaFree(p);
@@ -459,6 +461,7 @@ int check_flag(orca_engine *E) {
     cudaMemsetAsync(E->d_err, 0, sizeof(unsigned), E->st);
     // a kernel that gave up may have left split-request arrival counters part-way
     cudaMemsetAsync(E->attn_cnt, 0, (size_t)E->cfg.max_batch * E->cfg.n_heads * 4, E->st);
+    if (E->sk_cnt) cudaMemsetAsync(E->sk_cnt, 0, (size_t)E->gs.sk_cnt_n * 4, E->st);
     cudaStreamSynchronize(E->st);
     return ORCA_ERR_DEVICE_FLAG;
 }
@@ -550,6 +553,16 @@ int orca_engine_create(const orca_model_config *cfg, const orca_weights *w, void
     if (rc == ORCA_OK && E->part_cap) rc = dev_alloc(&E->part, E->part_cap * 4);
     if (rc == ORCA_OK) rc = dev_alloc(&E->attn_part, (size_t)E->attn_part_work * c.n_heads * (d + 2) * 4);
     if (rc == ORCA_OK) rc = dev_alloc(&E->attn_cnt, B * c.n_heads * 4);
+    if (rc == ORCA_OK && E->bf) {
+        // stream-K GEMM workspace (token rows of any linear layer, the LM head's included)
+        E->gs.sk_part_floats = gemm_sk_part_floats(E->num_sms);
+        E->gs.sk_cnt_n = gemm_sk_counters((int)R, std::max({3 * c.hidden, c.ffn, c.vocab}));
+        rc = dev_alloc(&E->sk_part, E->gs.sk_part_floats * 4);
+        if (rc == ORCA_OK) rc = dev_alloc(&E->sk_cnt, (size_t)E->gs.sk_cnt_n * 4);
+        if (rc == ORCA_OK && cudaMemset(E->sk_cnt, 0, (size_t)E->gs.sk_cnt_n * 4) != cudaSuccess) rc = ORCA_ERR_CUDA;
+        E->gs.sk_part = E->sk_part;
+        E->gs.sk_cnt = E->sk_cnt;
+    }
     if (rc == ORCA_OK) rc = dev_alloc(&E->d_err, 4);
     if (rc == ORCA_OK && (cudaMallocHost((void **)&E->h_plan, (size_t)E->plan_cap * 4) != cudaSuccess ||
                           cudaMallocHost((void **)&E->h_next, B * 4) != cudaSuccess ||

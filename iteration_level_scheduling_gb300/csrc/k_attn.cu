@@ -688,11 +688,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }
-__device__ __forceinline__ int atom_add_acq_rel(int *p, int v) {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
 
 template <int D>
 __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm,

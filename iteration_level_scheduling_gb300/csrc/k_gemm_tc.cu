@@ -52,7 +52,7 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
 constexpr int kMaxSplits = 8;  // split-K ways (partial slabs)
 constexpr int kStageA = BM * BK * 2;  // 16 KiB
 constexpr int kGroup = 16;            // feature tiles per raster group
@@ -64,6 +64,7 @@ constexpr size_t kSmemExtra = 1024 + 256;  // alignment slack + barriers
 
 struct TcArgs {
     int m_tok, n_out, num_kb, kb_per_split, splits, bn, stages;
+    int kpb;  // 64-wide K blocks per ring stage (consecutive, one bulk copy of packed weights)
     int n_feat_tiles, n_tok_tiles;
     uint32_t idesc, tmem_cols;
     Epilogue e;
@@ -105,7 +106,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stage_b = a.bn * BK * 2;
-    const int stage_bytes = kStageA + stage_b;
+    const int kpb = a.kpb;
+    const int stage_bytes = kpb * (kStageA + stage_b);  // kpb weight blocks, then kpb activation blocks
     float *stage_c = reinterpret_cast<float *>(smem);  // accumulator tile [bn][128] after the mainloop
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.stages * stage_bytes);
     uint64_t *empty = full + kMaxStages;
@@ -120,6 +122,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tile_coords(blockIdx.x / S, a, ft, tt);
     const int kb0 = split * a.kb_per_split;
     const int nkb = min(a.num_kb, kb0 + a.kb_per_split) - kb0;
+    const int n_st = (nkb + kpb - 1) / kpb;  // ring steps; step i holds K blocks kb0 + i * kpb ..
+    auto blocks_of = [&](int i) { return min(kpb, nkb - i * kpb); };
     const int t_base = tt * a.bn;
     const int t_lim = min(a.bn, a.m_tok - t_base);  // valid token columns of this tile
 
@@ -154,32 +158,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         // packed weights: tile (ft, kb) is one contiguous 16 KiB block, already in
         // the swizzled shared-memory image, so one bulk copy moves it
         const bf16 *wp = a.w_packed ? a.w_packed + (size_t)ft * a.num_kb * (BM * BK) : nullptr;
+        // step i: the weight blocks of K blocks kb0 + i * kpb .. (consecutive in the
+        // packed layout: one bulk copy), then the matching activation blocks
         auto load_w = [&](int i, int s) {
             uint8_t *sa = smem + (size_t)s * stage_bytes;
-            if (wp)
-                bulk_load(sa, wp + (size_t)(kb0 + i) * (BM * BK), kStageA, &full[s], pol_w);
-            else if (stream_w)
-                tma_load_2d_hint(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM, pol_w);
-            else
-                tma_load_2d(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM);
+            const int kb = kb0 + i * kpb, nb = blocks_of(i);
+            if (wp) {
+                bulk_load(sa, wp + (size_t)kb * (BM * BK), (uint32_t)(nb * kStageA), &full[s], pol_w);
+            } else {
+                for (int j = 0; j < nb; ++j) {
+                    if (stream_w)
+                        tma_load_2d_hint(sa + j * kStageA, &tmw, &full[s], (kb + j) * BK, ft * BM, pol_w);
+                    else
+                        tma_load_2d(sa + j * kStageA, &tmw, &full[s], (kb + j) * BK, ft * BM);
+                }
+            }
         };
+        auto load_x = [&](int i, int s) {
+            uint8_t *sb = smem + (size_t)s * stage_bytes + kpb * kStageA;
+            const int kb = kb0 + i * kpb, nb = blocks_of(i);
+            for (int j = 0; j < nb; ++j) tma_load_2d(sb + j * stage_b, &tmx, &full[s], (kb + j) * BK, t_base);
+        };
+        auto step_bytes = [&](int i) { return (uint32_t)(blocks_of(i) * (kStageA + stage_b)); };
         // The weights do not depend on earlier kernels: fill the first stages
         // with weight slices before waiting for the previous kernel, then add
         // the activation slices.
-        const int pre = min(nkb, a.stages);
+        const int pre = min(n_st, a.stages);
         if (leader)
             for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&full[i], (uint32_t)stage_bytes);
+                mbar_arrive_expect_tx(&full[i], step_bytes(i));
                 load_w(i, i);
             }
         pdl_wait();
         if (leader)
-            for (int i = 0; i < pre; ++i)
-                tma_load_2d(smem + (size_t)i * stage_bytes + kStageA, &tmx, &full[i], (kb0 + i) * BK, t_base);
+            for (int i = 0; i < pre; ++i) load_x(i, i);
         __syncwarp();
         int issued = pre;
         bool ok = true;
-        for (int i = pre; i < nkb; ++i) {
+        for (int i = pre; i < n_st; ++i) {
             const int s = i % a.stages;
             const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], ph ^ 1u, a.err))) {
@@ -187,9 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             if (leader) {
-                mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
+                mbar_arrive_expect_tx(&full[s], step_bytes(i));
                 load_w(i, s);
-                tma_load_2d(smem + (size_t)s * stage_bytes + kStageA, &tmx, &full[s], (kb0 + i) * BK, t_base);
+                load_x(i, s);
             }
             __syncwarp();
             ++issued;
@@ -205,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_wait();
         const bool leader = elect_one();
         bool ok = true;
-        for (int i = 0; i < nkb; ++i) {
+        for (int i = 0; i < n_st; ++i) {
             const int s = i % a.stages;
             const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], ph, a.err))) {
@@ -214,12 +230,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-            const uint64_t ad = smem_desc_k128(sa), bd = smem_desc_k128(sa + kStageA);
+            const uint32_t sb = sa + (uint32_t)(kpb * kStageA);
+            const int nb = blocks_of(i);
             if (leader) {
+                for (int j = 0; j < nb; ++j) {
+                    const uint64_t ad = smem_desc_k128(sa + (uint32_t)(j * kStageA));
+                    const uint64_t bd = smem_desc_k128(sb + (uint32_t)(j * stage_b));
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)  // 16 bf16 = 32 B per MMA: +2 in the >>4 address field
-                    tc_mma_f16(tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), a.idesc,
-                               (uint32_t)((i | kk) != 0));
+                    for (int kk = 0; kk < BK / 16; ++kk)  // 16 bf16 = 32 B per MMA: +2 in the >>4 address field
+                        tc_mma_f16(tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), a.idesc,
+                                   (uint32_t)((i | j | kk) != 0));
+                }
                 tc_commit(&empty[s]);
             }
             __syncwarp();
@@ -352,6 +373,402 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Stream-K variant (many token rows).
+//
+// With a few hundred token rows the layer is compute-bound, yet the one-tile-
+// per-CTA kernel leaves SMs idle: 80 tiles on 152 SMs for the 5120-wide
+// outputs, 2.1 waves of 320 tiles for the 20480-wide one, each tile paying its
+// own pipeline fill and an epilogue the MMAs do not overlap.  Here the
+// iteration space "tiles x 64-wide K blocks" (K block innermost) is cut into
+// equal contiguous ranges, one persistent CTA per SM, so every SM does the
+// same share of MMAs and streams the same share of weight bytes whatever the
+// tile count.  A CTA walks its range tile piece by tile piece; the producer
+// runs ahead across piece boundaries, and the accumulator is double-buffered
+// in TMEM (2 x bn <= 512 columns) so the epilogue of one piece overlaps the
+// MMAs of the next.  A tile cut between CTAs is completed by whichever of them
+// finishes last (an arrival counter per tile; no CTA ever waits on another):
+// each other piece is stored as an fp32 partial tile and the finisher sums the
+// pieces in CTA order -- a fixed order, so results do not depend on timing --
+// before the epilogue.
+//
+// Warp roles (320 threads): warp 0 = producer, warp 1 = TMEM owner and MMA
+// issuer, warps 2-9 = epilogue, two per TMEM lane quarter (warp % 4), taking
+// alternate 16-column chunks.  The epilogue runs straight from TMEM: thread =
+// output feature, 16 token columns per tcgen05.ld, so a warp's 32 features
+// make each store one contiguous run.
+// ---------------------------------------------------------------------------
+constexpr int kSkThreads = 320;
+constexpr int kSkEpiThreads = 256;
+constexpr int kSkEpiWarps = kSkEpiThreads / 32;
+constexpr int kSkMaxStages = 12;
+constexpr int kSkMaxBn = 256;
+// after the ring: full[12], empty[12], acc_full[2], acc_empty[2] (224 B), the
+// TMEM base address, flags[2]; the tile's K/V slots from byte 256
+constexpr int kSkTail = 256 + kSkMaxBn * 4;
+constexpr size_t kSkSmemExtra = 1024 + kSkTail;
+
+struct SkArgs {
+    int m_tok, n_out, num_kb, bn, stages;
+    int n_tok_tiles, n_units, chunk;
+    uint32_t idesc, tmem_cols;
+    Epilogue e;
+    const bf16 *w_packed;  // tile-contiguous weights (pack_weight_bf16), or null (tensor map)
+    // piece of a cut tile held by CTA b: slot 2b if it is b's first tile, else
+    // 2b + 1 (a cut tile is the first or the last tile of every CTA holding a
+    // piece of it); slot layout [feature 128][bn tokens]
+    float *part;
+    int *cnt;  // per-tile arrival counters, zero between launches
+    unsigned *err;
+};
+
+__device__ __forceinline__ int sk_unit_begin(int b, const SkArgs &a) { return min(b * a.chunk, a.n_units); }
+__device__ __forceinline__ int sk_part_slot(int b, int tile, const SkArgs &a) {
+    return 2 * b + (sk_unit_begin(b, a) / a.num_kb == tile ? 0 : 1);
+}
+// barrier / AND over the 256 epilogue threads (named barrier 1)
+__device__ __forceinline__ void sk_epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool sk_epi_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, 256, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+__global__ void __launch_bounds__(kSkThreads, 1)
+    gemm_sk_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx, const SkArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int stage_bytes = kStageA + a.bn * BK * 2;
+    uint8_t *tail = smem + (size_t)a.stages * stage_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(tail);
+    uint64_t *empty = full + kSkMaxStages;
+    uint64_t *acc_full = empty + kSkMaxStages;  // [2] accumulator buffer ready for the epilogue
+    uint64_t *acc_empty = acc_full + 2;         // [2] accumulator buffer drained
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);  // [0] abort, [1] finisher
+    int *tile_slot = reinterpret_cast<int *>(tail + 256);                  // [bn] K/V pool slot of each token
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int u_begin = sk_unit_begin(blockIdx.x, a), u_end = sk_unit_begin(blockIdx.x + 1, a);
+    const int nkb = a.num_kb, ntt = a.n_tok_tiles;
+
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], kSkEpiWarps);  // one arrival per epilogue warp
+        }
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmw);
+        prefetch_tmap(&tmx);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        // Stage i of the ring holds unit u_begin + i; the whole warp runs the
+        // loop (warp-uniform control) and one elected lane issues the copies.
+        const bool leader = elect_one();
+        const uint64_t pol_w = l2_policy_evict_first();
+        auto load_w = [&](int u, int s) {
+            const int tile = u / nkb, kb = u - tile * nkb, ft = tile / ntt;
+            uint8_t *sa = smem + (size_t)s * stage_bytes;
+            if (a.w_packed)  // tile (ft, kb) is one contiguous 16 KiB block, already in the swizzled image
+                bulk_load(sa, a.w_packed + ((size_t)ft * nkb + kb) * (BM * BK), kStageA, &full[s], pol_w);
+            else
+                tma_load_2d(sa, &tmw, &full[s], kb * BK, ft * BM);
+        };
+        auto load_x = [&](int u, int s) {
+            const int tile = u / nkb, kb = u - tile * nkb, tt = tile % ntt;
+            tma_load_2d(smem + (size_t)s * stage_bytes + kStageA, &tmx, &full[s], kb * BK, tt * a.bn);
+        };
+        const int n_mine = u_end - u_begin;
+        // the weights do not depend on earlier kernels: fill the first stages
+        // with weight slices before waiting for the previous kernel
+        const int pre = min(n_mine, a.stages);
+        if (leader)
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full[i], (uint32_t)stage_bytes);
+                load_w(u_begin + i, i);
+            }
+        pdl_wait();
+        if (leader)
+            for (int i = 0; i < pre; ++i) load_x(u_begin + i, i);
+        __syncwarp();
+        int issued = pre;
+        bool ok = true;
+        for (int i = pre; i < n_mine; ++i) {
+            const int s = i % a.stages;
+            const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], ph ^ 1u, a.err))) {
+                ok = false;
+                break;
+            }
+            if (leader) {
+                mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
+                load_w(u_begin + i, s);
+                load_x(u_begin + i, s);
+            }
+            __syncwarp();
+            ++issued;
+        }
+        if (!ok && leader) {
+            flags[0] = 1;
+            // let the copies already in flight land before the CTA exits
+            for (int j = max(0, issued - a.stages); j < issued; ++j)
+                mbar_wait_bounded(&full[j % a.stages], (uint32_t)(j / a.stages) & 1u, a.err);
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        const bool leader = elect_one();
+        bool ok = true;
+        int i = 0, p = 0;
+        for (int u = u_begin; u < u_end; ++p) {
+            const int tile = u / nkb, k0 = u - tile * nkb, k1 = min(nkb, k0 + (u_end - u));
+            const int buf = p & 1;
+            if (p >= 2) {  // the epilogue has drained this buffer's previous piece
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_bounded(&acc_empty[buf], (uint32_t)((p - 2) >> 1) & 1u, a.err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            const uint32_t d_tmem = tmem + (uint32_t)(buf * a.bn);
+            for (int kb = k0; kb < k1; ++kb, ++i) {
+                const int s = i % a.stages;
+                const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], ph, a.err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+                const uint64_t ad = smem_desc_k128(sa), bd = smem_desc_k128(sa + kStageA);
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)  // 16 bf16 = 32 B per MMA: +2 in the >>4 address field
+                        tc_mma_f16(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), a.idesc,
+                                   (uint32_t)(kb != k0 || kk != 0));
+                    tc_commit(&empty[s]);
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (leader) tc_commit(&acc_full[buf]);
+            __syncwarp();
+            u += k1 - k0;
+        }
+        if (!ok && leader) {
+            flags[0] = 1;
+            tc_commit(&acc_full[p & 1]);  // arrives once every MMA issued so far has completed
+        }
+    } else {
+        // ------------------------------ epilogue ------------------------------
+        pdl_wait();
+        const Epilogue &e = a.e;
+        const int quarter = warp & 3;        // TMEM lanes 32 * (warp % 4) ..
+        const int half = (warp - 2) >> 2;    // this warp's 16-column chunks: c0 = 16 * half + 32 j
+        const int row = quarter * 32 + lane;  // output feature within the tile
+        const int et = threadIdx.x - 64;     // 0 .. 255
+        const uint32_t lane_taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+        int p = 0;
+        for (int u = u_begin; u < u_end; ++p) {
+            const int tile = u / nkb, k0 = u - tile * nkb, k1 = min(nkb, k0 + (u_end - u));
+            u += k1 - k0;
+            const int buf = p & 1;
+            const int ft = tile / ntt, tt = tile - ft * ntt;
+            const int t_base = tt * a.bn, t_lim = min(a.bn, a.m_tok - t_base);
+            const int f = ft * BM + row;
+            const bool f_ok = f < a.n_out;
+            // everything the epilogue reads is fetched while the MMAs run
+            const float bias = (e.bias && f_ok) ? e.bias[f] : 0.f;
+            // K/V append: output features >= kv_h go to the pool at the row's slot
+            bf16 *kv_dst = nullptr;
+            if (e.kv_pool && f_ok && f >= e.kv_h) {
+                int c = f - e.kv_h;
+                const int which = c >= e.kv_h;
+                c -= which * e.kv_h;
+                const int head = c / e.kv_hd;
+                kv_dst = e.kv_pool + ((size_t)(which * e.kv_nh + head) * e.kv_slots) * e.kv_hd + (c - head * e.kv_hd);
+            }
+            if (e.kv_pool) {
+                sk_epi_sync();  // the previous piece's slots are no longer read
+                for (int t = et; t < t_lim; t += kSkEpiThreads) tile_slot[t] = e.row_slot[t_base + t];
+                sk_epi_sync();
+            }
+            // A cut tile: its pieces are summed in CTA order b_first .. b_last by
+            // the finisher -- the piece that finds every other piece stored
+            // (its own part straight from TMEM), else the last to arrive.
+            const bool cut = !(k0 == 0 && k1 == nkb);
+            const int b_first = cut ? (tile * nkb) / a.chunk : 0;
+            const int b_last = cut ? (tile * nkb + nkb - 1) / a.chunk : 0;
+            auto piece = [&](int b) { return a.part + (size_t)sk_part_slot(b, tile, a) * a.bn * BM + (size_t)row * a.bn; };
+            auto others_stored = [&]() {  // uniform over the epilogue threads
+                if (et == 0) flags[1] = ld_acquire(&a.cnt[tile]) == b_last - b_first;
+                sk_epi_sync();
+                const bool r = flags[1];
+                sk_epi_sync();
+                return r;
+            };
+            bool fast = cut && others_stored();
+            const bool ok = mbar_wait_bounded(&acc_full[buf], (uint32_t)(p >> 1) & 1u, a.err);
+            tc_fence_after();
+            if (!sk_epi_all(ok && flags[0] == 0)) {  // the epilogue warps leave together
+                if (et == 0) flags[0] = 1;
+                break;
+            }
+            __syncwarp();  // tcgen05.ld is .sync.aligned
+            // bias / GeLU / residual / store of 16 token columns from c0 (v is overwritten)
+            auto finish = [&](float *v, int c0) {
+                if (!f_ok) return;
+                const int n = min(16, t_lim - c0);
+                const size_t ld = (size_t)e.ld_out;
+                const size_t o0 = (size_t)(t_base + c0) * ld + f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += bias;
+                if (e.gelu) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = gelu_erf(v[j]);
+                }
+                if (e.resid) {
+                    float r[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) r[j] = j < n ? e.resid[o0 + j * ld] : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < n) e.out_f32[o0 + j * ld] = v[j] + r[j];
+                } else if (e.out_f32) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < n) e.out_f32[o0 + j * ld] = v[j];
+                } else if (kv_dst) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < n) kv_dst[(size_t)tile_slot[c0 + j] * e.kv_hd] = __float2bfloat16_rn(v[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < n) e.out_bf16[o0 + j * ld] = __float2bfloat16_rn(v[j]);
+                }
+            };
+            auto release = [&]() {  // this accumulator buffer may take the next piece
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            };
+            // v = sum of the pieces in CTA order over 16 tokens from c0, this
+            // CTA's own values in its place; two pieces in flight at a time
+            auto sum_pieces = [&](float *v, const float *own, int c0) {
+                float acc[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+                for (int b = b_first; b <= b_last; b += 2) {
+                    float4 q[2][4];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+                        if (b + i <= b_last && b + i != (int)blockIdx.x) {
+                            const float4 *src = reinterpret_cast<const float4 *>(piece(b + i) + c0);
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) q[i][h] = __ldcg(src + h);
+                        }
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        if (b + i > b_last) break;
+                        if (b + i == (int)blockIdx.x) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) acc[j] += own[j];
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                acc[4 * h] += q[i][h].x, acc[4 * h + 1] += q[i][h].y;
+                                acc[4 * h + 2] += q[i][h].z, acc[4 * h + 3] += q[i][h].w;
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = acc[j];
+            };
+            const uint32_t taddr = lane_taddr + (uint32_t)(buf * a.bn);
+            auto finish_tile = [&]() {  // the finisher: own piece from TMEM, the others from their slots
+                for (int c0 = 16 * half; c0 < t_lim; c0 += 32) {
+                    float own[16], v[16];
+                    tmem_ld16(taddr + c0, own);
+                    sum_pieces(v, own, c0);
+                    finish(v, c0);
+                }
+            };
+            if (!cut) {
+                // the whole tile is in this CTA's accumulator
+                for (int c0 = 16 * half; c0 < t_lim; c0 += 32) {
+                    float v[16];
+                    tmem_ld16(taddr + c0, v);
+                    finish(v, c0);
+                }
+            } else {
+                if (!fast) fast = others_stored();  // second look, now that this piece is done
+                if (fast) {
+                    finish_tile();
+                    if (et == 0) a.cnt[tile] = 0;  // every other piece has arrived: ready for the next launch
+                } else {
+                    // store this piece and arrive; the last to arrive completes the tile
+                    float *mine = piece(blockIdx.x);
+                    for (int c0 = 16 * half; c0 < t_lim; c0 += 32) {
+                        float v[16];
+                        tmem_ld16(taddr + c0, v);
+#pragma unroll
+                        for (int h = 0; h < 4; ++h)
+                            *reinterpret_cast<float4 *>(mine + c0 + 4 * h) =
+                                make_float4(v[4 * h], v[4 * h + 1], v[4 * h + 2], v[4 * h + 3]);
+                    }
+                    sk_epi_sync();  // every thread's stores precede the one release below
+                    if (et == 0) {
+                        __threadfence();
+                        const int old = atom_add_acq_rel(&a.cnt[tile], 1);
+                        const int last = old == b_last - b_first;
+                        if (last) a.cnt[tile] = 0;
+                        flags[1] = last;
+                    }
+                    sk_epi_sync();
+                    const bool last = flags[1];
+                    sk_epi_sync();  // flags[1] is read by all before it is rewritten
+                    if (last) finish_tile();
+                }
+            }
+            release();
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, a.tmem_cols);
+    }
+}
+
 // Pack w [n_out, k] into tiles of 128 rows x 64 columns, tile (ft, kb) at
 // element offset (ft * (k / 64) + kb) * 8192, each tile laid out exactly as
 // the 128-byte-swizzled K-major shared-memory image (row r at r * 128 bytes,
@@ -412,6 +829,17 @@ int override_stages() {
     static int v = env_int("ORCA_GEMM_STAGES");
     return v;
 }
+int override_kpb() {
+    static int v = env_int("ORCA_GEMM_KPB");
+    return v;
+}
+// ORCA_GEMM_SK: 1 = stream-K whenever the workspace allows, -1 = never,
+// unset / 0 = by token rows (kSkMinRows).
+int override_sk() {
+    static int v = env_int("ORCA_GEMM_SK");
+    return v;
+}
+constexpr int kSkMinRows = 129;
 
 }  // namespace
 
@@ -450,10 +878,13 @@ TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool al
     t.kb_per_split = ceil_div(num_kb, splits);
     t.splits = ceil_div(num_kb, t.kb_per_split);
     // one CTA per SM with a deep ring when everything runs in one wave, else two
-    const int stage_bytes = kStageA + t.bn * BK * 2;
-    const size_t max_stages_1cta = (kSmemMaxCta - kSmemExtra) / stage_bytes;
     const int ctas_per_sm = (tiles * t.splits > s.num_sms && t.bn <= 128) ? 2 : 1;
     const size_t budget = std::min(kSmemMaxCta, kSmemPerSm / ctas_per_sm - kSmemReserve) - kSmemExtra;
+    // K blocks per ring stage: at least two stages must fit
+    t.kpb = std::max(1, std::min(override_kpb() > 0 ? override_kpb() : 1, t.kb_per_split));
+    while (t.kpb > 1 && budget / (size_t)(t.kpb * (kStageA + t.bn * BK * 2)) < 2) --t.kpb;
+    const int stage_bytes = t.kpb * (kStageA + t.bn * BK * 2);
+    const size_t max_stages_1cta = (kSmemMaxCta - kSmemExtra) / stage_bytes;
     t.stages = std::min<int>(kMaxStages, (int)(budget / stage_bytes));
     if (override_stages() > 0) t.stages = std::min<int>(std::min(override_stages(), kMaxStages), (int)max_stages_1cta);
     // the ring must also hold the staged fp32 accumulator tile (bn x 512 B) after the mainloop
@@ -464,15 +895,101 @@ TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool al
 
 size_t packed_weight_elems(int n_out, int k) { return (size_t)ceil_div(n_out, BM) * BM * (size_t)k; }
 
+SkShape gemm_sk_shape(int m_tok, int n_out, int k, int num_sms) {
+    SkShape t{};
+    const int m = std::max(m_tok, 1);
+    t.n_tok_tiles = ceil_div(m, kSkMaxBn);
+    t.bn = std::min(kSkMaxBn, std::max(16, ceil_div(ceil_div(m, t.n_tok_tiles), 16) * 16));
+    t.n_feat_tiles = ceil_div(n_out, BM);
+    t.tiles = t.n_tok_tiles * t.n_feat_tiles;
+    t.num_kb = k / BK;
+    t.units = t.tiles * t.num_kb;
+    const int g0 = std::max(1, std::min(num_sms, t.units));
+    t.chunk = ceil_div(t.units, g0);
+    t.grid = ceil_div(t.units, t.chunk);
+    t.tmem_cols = 32;  // two accumulator buffers of bn columns
+    while (t.tmem_cols < 2 * t.bn) t.tmem_cols *= 2;
+    const int stage_bytes = kStageA + t.bn * BK * 2;
+    t.stages = std::min<int>(kSkMaxStages, (int)((kSmemMaxCta - kSkSmemExtra) / stage_bytes));
+    if (override_stages() > 0) t.stages = std::min(t.stages, override_stages());
+    t.smem = (size_t)t.stages * stage_bytes + kSkSmemExtra;
+    t.part_floats = (size_t)2 * t.grid * t.bn * BM;
+    return t;
+}
+
+size_t gemm_sk_part_floats(int num_sms) { return (size_t)2 * std::max(num_sms, 1) * kSkMaxBn * BM; }
+int gemm_sk_counters(int max_rows, int max_n) {
+    // at least 64 Ki tiles, so stand-alone linear calls of other shapes qualify too
+    return std::max(1 << 16, ceil_div(std::max(max_rows, 1), kSkMaxBn) * ceil_div(std::max(max_n, 1), BM));
+}
+
+bool gemm_uses_sk(int m_tok, int n_out, int k, const GemmScratch &s) {
+    if (!s.sk_part || !s.sk_cnt || m_tok <= 0 || k % BK != 0 || k <= 0 || n_out <= 0) return false;
+    if (override_sk() < 0) return false;
+    const SkShape t = gemm_sk_shape(m_tok, n_out, k, s.num_sms);
+    // by default only with many rows and at least one tile per CTA, so a tile
+    // is cut at most once (a two-piece finish)
+    if (override_sk() == 0 && (m_tok < kSkMinRows || t.tiles < t.grid)) return false;
+    return t.tiles <= s.sk_cnt_n && t.part_floats <= s.sk_part_floats && t.stages >= 2 &&
+           !(reinterpret_cast<uintptr_t>(s.sk_part) & 15);
+}
+
+namespace {
+cudaError_t launch_sk(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_packed, int m_tok, int n_out, int k,
+                      const Epilogue &e, const GemmScratch &s, cudaStream_t st) {
+    const SkShape t = gemm_sk_shape(m_tok, n_out, k, s.num_sms);
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t ae = cudaFuncSetAttribute(gemm_sk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)kSmemMaxCta);
+        if (ae != cudaSuccess) return ae;
+        attr_done = true;
+    }
+    CUtensorMap mw, mx;
+    if (!make_map(&mw, w, w_packed ? BM : n_out, k, BM) || !make_map(&mx, x, x_rows_cap, k, t.bn))
+        return cudaErrorInvalidValue;  // (the weight map is unused when the weights are packed)
+    SkArgs a;
+    a.m_tok = m_tok;
+    a.n_out = n_out;
+    a.num_kb = t.num_kb;
+    a.bn = t.bn;
+    a.stages = t.stages;
+    a.n_tok_tiles = t.n_tok_tiles;
+    a.n_units = t.units;
+    a.chunk = t.chunk;
+    a.idesc = idesc_bf16_f32(BM, t.bn);
+    a.tmem_cols = (uint32_t)t.tmem_cols;
+    a.e = e;
+    a.w_packed = w_packed ? w : nullptr;
+    a.part = s.sk_part;
+    a.cnt = s.sk_cnt;
+    a.err = s.err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(t.grid);
+    cfg.blockDim = dim3(kSkThreads);
+    cfg.dynamicSmemBytes = t.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_sk_kernel, mw, mx, a);
+}
+}  // namespace
+
 cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_packed, int m_tok, int n_out, int k,
                          const Epilogue &e, const GemmScratch &s, cudaStream_t st, int *n_partials) {
     if (n_partials) *n_partials = 0;
     if (m_tok <= 0) return cudaSuccess;
     if (k % BK != 0 || k <= 0 || n_out <= 0 || x_rows_cap < m_tok) return cudaErrorInvalidValue;
     if (e.kv_pool && (e.kv_hd % 4 != 0 || !e.row_slot || !e.out_bf16)) return cudaErrorInvalidValue;
+    if (w_packed && (reinterpret_cast<uintptr_t>(w) & 15)) return cudaErrorInvalidValue;
+    if (gemm_uses_sk(m_tok, n_out, k, s)) return launch_sk(x, x_rows_cap, w, w_packed, m_tok, n_out, k, e, s, st);
     const bool allow_partial = e.part != nullptr && !(reinterpret_cast<uintptr_t>(e.part) & 15);
     const TcShape t = gemm_tc_shape(m_tok, n_out, k, s, allow_partial, e.part_cap);
-    if ((size_t)t.stages * (kStageA + t.bn * BK * 2) < (size_t)t.bn * BM * 4) return cudaErrorInvalidValue;
+    if (t.stages < 2 || (size_t)t.stages * t.kpb * (kStageA + t.bn * BK * 2) < (size_t)t.bn * BM * 4)
+        return cudaErrorInvalidValue;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t ae = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -492,6 +1009,7 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_pa
     a.splits = t.splits;
     a.bn = t.bn;
     a.stages = t.stages;
+    a.kpb = t.kpb;
     a.n_feat_tiles = t.n_feat_tiles;
     a.n_tok_tiles = t.n_tok_tiles;
     a.idesc = idesc_bf16_f32(BM, t.bn);

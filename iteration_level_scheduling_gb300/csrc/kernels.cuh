@@ -36,10 +36,17 @@ struct Epilogue {
     int kv_h = 0, kv_hd = 0, kv_nh = 0;
 };
 
-// Launch context of the tensor-core GEMM: the device error word and the SM count.
+// Launch context of the tensor-core GEMM: the device error word, the SM
+// count and the stream-K workspace (partial tiles of cut tiles and one
+// arrival counter per tile, zero between launches).  Without a workspace the
+// stream-K kernel is never chosen.
 struct GemmScratch {
     unsigned *err = nullptr;
     int num_sms = 148;
+    float *sk_part = nullptr;
+    size_t sk_part_floats = 0;
+    int *sk_cnt = nullptr;
+    int sk_cnt_n = 0;
 };
 
 // tcgen05 GEMM, bf16 operands, fp32 accumulation in tensor memory.
@@ -54,11 +61,24 @@ size_t packed_weight_elems(int n_out, int k);
 cudaError_t pack_weight_bf16(const bf16 *w, int n_out, int k, bf16 *out, cudaStream_t st);
 // Shape the tcgen05 GEMM would use (for scratch sizing and accounting).
 struct TcShape {
-    int bn, n_tok_tiles, n_feat_tiles, splits, kb_per_split, stages, tmem_cols;
+    int bn, n_tok_tiles, n_feat_tiles, splits, kb_per_split, kpb, stages, tmem_cols;
     size_t smem;
 };
 TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool allow_partial = false,
                       size_t part_cap = 0);
+// Stream-K launch shape: token tiles of bn <= 256 rows, the units
+// (tile, 64-wide K block) cut into `grid` ranges of `chunk` units.
+struct SkShape {
+    int bn, n_tok_tiles, n_feat_tiles, tiles, num_kb, units, chunk, grid, stages, tmem_cols;
+    size_t smem, part_floats;
+};
+SkShape gemm_sk_shape(int m_tok, int n_out, int k, int num_sms);
+// Whether gemm_tc_bf16 takes the stream-K kernel for this shape.
+bool gemm_uses_sk(int m_tok, int n_out, int k, const GemmScratch &s);
+// Workspace the stream-K kernel needs at most for up to max_rows token rows
+// and outputs of up to max_n features.
+size_t gemm_sk_part_floats(int num_sms);
+int gemm_sk_counters(int max_rows, int max_n);
 
 // cuTensorMapEncodeTiled, reached through the runtime's driver entry point;
 // dims/strides/box innermost first (strides in bytes, rank - 1 of them).

@@ -42,6 +42,10 @@ SHAPES = [
     (1, 128, 64), (16, 256, 128), (5, 130, 64), (64, 384, 1024), (100, 200, 512), (64, 5120, 1024),
     (300, 640, 256), (477, 1024, 1024), (600, 1280, 320), (1000, 384, 128), (2048, 512, 64), (64, 128, 20480),
     (16, 128, 64), (33, 15360, 128), (256, 2560, 5120),
+    # stream-K (>= 129 rows): tiles cut into several pieces at odd offsets, CTAs
+    # holding a first and a last piece, three whole tiles per CTA (accumulator
+    # buffer reuse), ragged rows and features
+    (136, 12800, 320), (200, 6400, 192), (144, 51200, 64), (129, 1000, 2048),
 ]
 
 
@@ -130,6 +134,21 @@ def test_linear_tc_repeatable(eng):
     eng.op_linear(native.DTYPE_BF16, xd.data_ptr(), wd.data_ptr(), m, n, k, out_f32=a.data_ptr())
     eng.op_linear(native.DTYPE_BF16, xd.data_ptr(), wd.data_ptr(), m, n, k, out_f32=b.data_ptr())
     assert torch.equal(a, b)
+
+
+def test_linear_sk_repeatable(eng):
+    """Stream-K sums the pieces of a cut tile in CTA order whoever finishes last:
+    launches agree bit for bit (and the arrival counters are back at zero after each)."""
+    from iteration_level_scheduling_gb300 import native
+    m, n, k = 300, 1280, 1024
+    g = np.random.default_rng(5)
+    xd = torch.from_numpy(synth.bf16_round(g.standard_normal((m, k), dtype=np.float32))).cuda().to(torch.bfloat16)
+    wd = torch.from_numpy(synth.bf16_round(g.standard_normal((n, k), dtype=np.float32))).cuda().to(torch.bfloat16)
+    outs = [torch.zeros((m, n), device="cuda") for _ in range(4)]
+    for o in outs:
+        eng.op_linear(native.DTYPE_BF16, xd.data_ptr(), wd.data_ptr(), m, n, k, out_f32=o.data_ptr())
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
 
 
 @pytest.mark.parametrize("m,n,k", [(1, 64, 64), (37, 256, 64), (130, 200, 256), (64, 512, 20)])
