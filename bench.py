@@ -437,7 +437,6 @@ def run_orca(args, rank, world, local_rank):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     clocks = Clocks(vis.split(",")[local_rank].strip() if vis else str(torch.cuda.current_device()))
     time.sleep(0.3)
-    eng.timing(True)
     launches0 = eng.stats().launches
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     if world > 1:
@@ -453,6 +452,14 @@ def run_orca(args, rank, world, local_rank):
         dist.barrier()
     launches = eng.stats().launches - launches0
     clk = clocks.stop()
+    eng.sync()
+    # Per-kernel breakdown: a separate pass over the same plans with CUDA events
+    # around every launch of one sampled layer per iteration (events between
+    # launches forgo their programmatic-launch overlap, so this pass is not timed).
+    eng.timing(True)
+    for j in range(args.steps):
+        i = args.warmup + j
+        eng.run_planned(plans[i], base + 4 * int(offs[i]))
     eng.sync()
     recs = eng.timing_read()
     eng.timing(False)
@@ -491,6 +498,18 @@ def run_orca(args, rank, world, local_rank):
                      "GB/s": d["bytes"] / (d["ms"] / 1000) / 1e9 if d["ms"] else None,
                      "TFLOP/s": d["flops"] / (d["ms"] / 1000) / 1e12 if d["ms"] else None}
                  for k, d in sorted(kinds.items(), key=lambda kv: -kv[1]["est"])}
+    # the linear layers one by one (sampled-layer launches; lm_head once per iteration)
+    gk = {}
+    for r in recs:
+        if r["kind"].startswith("gemm") or r["kind"] == "lm_head":
+            d = gk.setdefault(r["kind"], dict(ms=0.0, bytes=0.0, flops=0.0, n=0))
+            d["ms"] += r["ms"]
+            d["bytes"] += r["bytes"]
+            d["flops"] += r["flops"]
+            d["n"] += 1
+    gemm_by_kind = {k: {"launches_timed": d["n"], "avg_us": 1000 * d["ms"] / d["n"],
+                        "GB/s": d["bytes"] / (d["ms"] / 1000) / 1e9, "TFLOP/s": d["flops"] / (d["ms"] / 1000) / 1e12}
+                    for k, d in gk.items() if d["n"] and d["ms"]}
     dom_name, dom = max(((k, d) for k, d in kinds.items() if k != "lm_head (gemm_tc)"), key=lambda kv: kv[1]["est"])
     t_hbm = dom["bytes"] / (peaks["hbm"] * 1e9)
     t_tc = dom["flops"] / (peaks["tc_sus"] * 1e12)
@@ -581,7 +600,8 @@ def run_orca(args, rank, world, local_rank):
                                "mean_batch": float(np.mean([w["B"] for w in work[args.warmup:]])),
                                "mean_rows": float(np.mean([w["R"] for w in work[args.warmup:]])),
                                "by_kind": split_by_prefill(work[args.warmup:], it_ms, fr)},
-        "roofline": roof, "kernels": breakdown, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
+        "roofline": roof, "kernels": breakdown, "gemm_by_kind": gemm_by_kind, "gpu_launches": launches,
+        "clocks": clk, "e2e": e2e,
         "cpu_baseline": cpu,
     }
     if req is not None:

@@ -26,6 +26,9 @@
 // partial tile to a slab; no CTA waits on another.  Otherwise one CTA per tile
 // with a deep stage ring, one CTA per SM when the tiles fit in one wave.
 //
+// With 129+ token rows and at least one output tile per SM the stream-K
+// kernel further below takes the layer instead (gemm_uses_sk).
+//
 // Weights can be pre-packed (pack_weight_bf16) so each 128 x 64 stage tile is
 // one contiguous, already swizzled 16 KiB block read by a single bulk copy:
 // sequential DRAM streaming instead of 128 rows of 128 bytes each.
