@@ -96,7 +96,12 @@ struct orca_engine {
     int32_t *h_next = nullptr;
     int32_t *h_plan = nullptr, *d_plan = nullptr;
     int64_t plan_cap = 0;
-    GemmScratch gs;
+    // GEMM launch contexts: `gs` for the iteration (one-tile-per-CTA kernel
+    // only), `gs_op` for stand-alone orca_op_linear calls (stream-K allowed).
+    // Inside an iteration the stream-K kernel, which fills every SM, is slower
+    // end to end: the one-tile kernel's idle SMs let the next launch start
+    // early under programmatic launch.
+    GemmScratch gs, gs_op;
     float *part = nullptr;  // split-K partial slabs of the residual projections
     size_t part_cap = 0;
     float *attn_part = nullptr;
@@ -461,7 +466,7 @@ int check_flag(orca_engine *E) {
     cudaMemsetAsync(E->d_err, 0, sizeof(unsigned), E->st);
     // a kernel that gave up may have left split-request arrival counters part-way
     cudaMemsetAsync(E->attn_cnt, 0, (size_t)E->cfg.max_batch * E->cfg.n_heads * 4, E->st);
-    if (E->sk_cnt) cudaMemsetAsync(E->sk_cnt, 0, (size_t)E->gs.sk_cnt_n * 4, E->st);
+    if (E->sk_cnt) cudaMemsetAsync(E->sk_cnt, 0, (size_t)E->gs_op.sk_cnt_n * 4, E->st);
     cudaStreamSynchronize(E->st);
     return ORCA_ERR_DEVICE_FLAG;
 }
@@ -555,13 +560,14 @@ int orca_engine_create(const orca_model_config *cfg, const orca_weights *w, void
     if (rc == ORCA_OK) rc = dev_alloc(&E->attn_cnt, B * c.n_heads * 4);
     if (rc == ORCA_OK && E->bf) {
         // stream-K GEMM workspace (token rows of any linear layer, the LM head's included)
-        E->gs.sk_part_floats = gemm_sk_part_floats(E->num_sms);
-        E->gs.sk_cnt_n = gemm_sk_counters((int)R, std::max({3 * c.hidden, c.ffn, c.vocab}));
-        rc = dev_alloc(&E->sk_part, E->gs.sk_part_floats * 4);
-        if (rc == ORCA_OK) rc = dev_alloc(&E->sk_cnt, (size_t)E->gs.sk_cnt_n * 4);
-        if (rc == ORCA_OK && cudaMemset(E->sk_cnt, 0, (size_t)E->gs.sk_cnt_n * 4) != cudaSuccess) rc = ORCA_ERR_CUDA;
-        E->gs.sk_part = E->sk_part;
-        E->gs.sk_cnt = E->sk_cnt;
+        E->gs_op.sk_part_floats = gemm_sk_part_floats(E->num_sms);
+        E->gs_op.sk_cnt_n = gemm_sk_counters((int)R, std::max({3 * c.hidden, c.ffn, c.vocab}));
+        rc = dev_alloc(&E->sk_part, E->gs_op.sk_part_floats * 4);
+        if (rc == ORCA_OK) rc = dev_alloc(&E->sk_cnt, (size_t)E->gs_op.sk_cnt_n * 4);
+        if (rc == ORCA_OK && cudaMemset(E->sk_cnt, 0, (size_t)E->gs_op.sk_cnt_n * 4) != cudaSuccess)
+            rc = ORCA_ERR_CUDA;
+        E->gs_op.sk_part = E->sk_part;
+        E->gs_op.sk_cnt = E->sk_cnt;
     }
     if (rc == ORCA_OK) rc = dev_alloc(&E->d_err, 4);
     if (rc == ORCA_OK && (cudaMallocHost((void **)&E->h_plan, (size_t)E->plan_cap * 4) != cudaSuccess ||
@@ -571,6 +577,8 @@ int orca_engine_create(const orca_model_config *cfg, const orca_weights *w, void
     if (rc == ORCA_OK) {
         *E->h_err = 0;
         E->gs.err = E->d_err;
+        E->gs_op.err = E->d_err;
+        E->gs_op.num_sms = E->num_sms;
         if (cudaMemset(E->attn_cnt, 0, B * c.n_heads * 4) != cudaSuccess || cudaMemset(E->d_err, 0, 4) != cudaSuccess ||
             cudaMemset(E->next, 0, B * 4) != cudaSuccess)
             rc = ORCA_ERR_CUDA;
@@ -887,7 +895,7 @@ int orca_op_linear(orca_engine *E, int32_t dtype, const void *x, const void *w, 
     cudaError_t ce;
     if (dtype == ORCA_DTYPE_BF16) {
         if (k % 64) return ORCA_ERR_INVALID;
-        ce = gemm_tc_bf16((const bf16 *)x, m, (const bf16 *)w, w_packed != 0, m, n, k, e, E->gs, E->st);
+        ce = gemm_tc_bf16((const bf16 *)x, m, (const bf16 *)w, w_packed != 0, m, n, k, e, E->gs_op, E->st);
     } else if (dtype == ORCA_DTYPE_FP32) {
         if (out_bf16 || w_packed) return ORCA_ERR_INVALID;
         ce = gemm_simt_f32((const float *)x, (const float *)w, m, n, k, e, E->st);

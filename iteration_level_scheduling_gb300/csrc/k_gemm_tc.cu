@@ -27,7 +27,10 @@
 // with a deep stage ring, one CTA per SM when the tiles fit in one wave.
 //
 // With 129+ token rows and at least one output tile per SM the stream-K
-// kernel further below takes the layer instead (gemm_uses_sk).
+// kernel further below takes the layer instead (gemm_uses_sk), when the
+// caller's launch context carries a stream-K workspace.  The engine gives one
+// to stand-alone linear calls only: inside an iteration the one-tile kernel is
+// faster end to end, because its idle SMs let the next launch start early.
 //
 // Weights can be pre-packed (pack_weight_bf16) so each 128 x 64 stage tile is
 // one contiguous, already swizzled 16 KiB block read by a single bulk copy:
@@ -55,7 +58,7 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxStages = 12;
+constexpr int kMaxStages = 8;
 constexpr int kMaxSplits = 8;  // split-K ways (partial slabs)
 constexpr int kStageA = BM * BK * 2;  // 16 KiB
 constexpr int kGroup = 16;            // feature tiles per raster group
@@ -67,7 +70,6 @@ constexpr size_t kSmemExtra = 1024 + 256;  // alignment slack + barriers
 
 struct TcArgs {
     int m_tok, n_out, num_kb, kb_per_split, splits, bn, stages;
-    int kpb;  // 64-wide K blocks per ring stage (consecutive, one bulk copy of packed weights)
     int n_feat_tiles, n_tok_tiles;
     uint32_t idesc, tmem_cols;
     Epilogue e;
@@ -109,8 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stage_b = a.bn * BK * 2;
-    const int kpb = a.kpb;
-    const int stage_bytes = kpb * (kStageA + stage_b);  // kpb weight blocks, then kpb activation blocks
+    const int stage_bytes = kStageA + stage_b;
     float *stage_c = reinterpret_cast<float *>(smem);  // accumulator tile [bn][128] after the mainloop
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.stages * stage_bytes);
     uint64_t *empty = full + kMaxStages;
@@ -125,8 +126,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tile_coords(blockIdx.x / S, a, ft, tt);
     const int kb0 = split * a.kb_per_split;
     const int nkb = min(a.num_kb, kb0 + a.kb_per_split) - kb0;
-    const int n_st = (nkb + kpb - 1) / kpb;  // ring steps; step i holds K blocks kb0 + i * kpb ..
-    auto blocks_of = [&](int i) { return min(kpb, nkb - i * kpb); };
     const int t_base = tt * a.bn;
     const int t_lim = min(a.bn, a.m_tok - t_base);  // valid token columns of this tile
 
@@ -161,44 +160,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // packed weights: tile (ft, kb) is one contiguous 16 KiB block, already in
         // the swizzled shared-memory image, so one bulk copy moves it
         const bf16 *wp = a.w_packed ? a.w_packed + (size_t)ft * a.num_kb * (BM * BK) : nullptr;
-        // step i: the weight blocks of K blocks kb0 + i * kpb .. (consecutive in the
-        // packed layout: one bulk copy), then the matching activation blocks
         auto load_w = [&](int i, int s) {
             uint8_t *sa = smem + (size_t)s * stage_bytes;
-            const int kb = kb0 + i * kpb, nb = blocks_of(i);
-            if (wp) {
-                bulk_load(sa, wp + (size_t)kb * (BM * BK), (uint32_t)(nb * kStageA), &full[s], pol_w);
-            } else {
-                for (int j = 0; j < nb; ++j) {
-                    if (stream_w)
-                        tma_load_2d_hint(sa + j * kStageA, &tmw, &full[s], (kb + j) * BK, ft * BM, pol_w);
-                    else
-                        tma_load_2d(sa + j * kStageA, &tmw, &full[s], (kb + j) * BK, ft * BM);
-                }
-            }
+            if (wp)
+                bulk_load(sa, wp + (size_t)(kb0 + i) * (BM * BK), kStageA, &full[s], pol_w);
+            else if (stream_w)
+                tma_load_2d_hint(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM, pol_w);
+            else
+                tma_load_2d(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM);
         };
-        auto load_x = [&](int i, int s) {
-            uint8_t *sb = smem + (size_t)s * stage_bytes + kpb * kStageA;
-            const int kb = kb0 + i * kpb, nb = blocks_of(i);
-            for (int j = 0; j < nb; ++j) tma_load_2d(sb + j * stage_b, &tmx, &full[s], (kb + j) * BK, t_base);
-        };
-        auto step_bytes = [&](int i) { return (uint32_t)(blocks_of(i) * (kStageA + stage_b)); };
         // The weights do not depend on earlier kernels: fill the first stages
         // with weight slices before waiting for the previous kernel, then add
         // the activation slices.
-        const int pre = min(n_st, a.stages);
+        const int pre = min(nkb, a.stages);
         if (leader)
             for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&full[i], step_bytes(i));
+                mbar_arrive_expect_tx(&full[i], (uint32_t)stage_bytes);
                 load_w(i, i);
             }
         pdl_wait();
         if (leader)
-            for (int i = 0; i < pre; ++i) load_x(i, i);
+            for (int i = 0; i < pre; ++i)
+                tma_load_2d(smem + (size_t)i * stage_bytes + kStageA, &tmx, &full[i], (kb0 + i) * BK, t_base);
         __syncwarp();
         int issued = pre;
         bool ok = true;
-        for (int i = pre; i < n_st; ++i) {
+        for (int i = pre; i < nkb; ++i) {
             const int s = i % a.stages;
             const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], ph ^ 1u, a.err))) {
@@ -206,9 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             if (leader) {
-                mbar_arrive_expect_tx(&full[s], step_bytes(i));
+                mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
                 load_w(i, s);
-                load_x(i, s);
+                tma_load_2d(smem + (size_t)s * stage_bytes + kStageA, &tmx, &full[s], (kb0 + i) * BK, t_base);
             }
             __syncwarp();
             ++issued;
@@ -224,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_wait();
         const bool leader = elect_one();
         bool ok = true;
-        for (int i = 0; i < n_st; ++i) {
+        for (int i = 0; i < nkb; ++i) {
             const int s = i % a.stages;
             const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], ph, a.err))) {
@@ -233,17 +220,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-            const uint32_t sb = sa + (uint32_t)(kpb * kStageA);
-            const int nb = blocks_of(i);
+            const uint64_t ad = smem_desc_k128(sa), bd = smem_desc_k128(sa + kStageA);
             if (leader) {
-                for (int j = 0; j < nb; ++j) {
-                    const uint64_t ad = smem_desc_k128(sa + (uint32_t)(j * kStageA));
-                    const uint64_t bd = smem_desc_k128(sb + (uint32_t)(j * stage_b));
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)  // 16 bf16 = 32 B per MMA: +2 in the >>4 address field
-                        tc_mma_f16(tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), a.idesc,
-                                   (uint32_t)((i | j | kk) != 0));
-                }
+                for (int kk = 0; kk < BK / 16; ++kk)  // 16 bf16 = 32 B per MMA: +2 in the >>4 address field
+                    tc_mma_f16(tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), a.idesc,
+                               (uint32_t)((i | kk) != 0));
                 tc_commit(&empty[s]);
             }
             __syncwarp();
@@ -413,7 +395,8 @@ constexpr size_t kSkSmemExtra = 1024 + kSkTail;
 
 struct SkArgs {
     int m_tok, n_out, num_kb, bn, stages;
-    int n_tok_tiles, n_units, chunk;
+    int n_tok_tiles, n_feat_tiles, n_units, chunk;
+    int tt_major;  // tile order: token-tile major (tile = tt * nft + ft) or feature-tile major (ft * ntt + tt)
     uint32_t idesc, tmem_cols;
     Epilogue e;
     const bf16 *w_packed;  // tile-contiguous weights (pack_weight_bf16), or null (tensor map)
@@ -460,7 +443,14 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int u_begin = sk_unit_begin(blockIdx.x, a), u_end = sk_unit_begin(blockIdx.x + 1, a);
-    const int nkb = a.num_kb, ntt = a.n_tok_tiles;
+    // Tile order.  Feature-tile major, a CTA takes a feature tile's token
+    // tiles one after the other, re-reading its weights.  Token-tile major
+    // (chosen with four or more token tiles), the CTAs holding the token tiles
+    // of one feature tile are nft * nkb units apart: they walk the same weight
+    // blocks at about the same time and share them in L2.
+    const int nkb = a.num_kb, ntt = a.n_tok_tiles, nft = a.n_feat_tiles;
+    auto ft_of = [&](int tile) { return a.tt_major ? tile % nft : tile / ntt; };
+    auto tt_of = [&](int tile) { return a.tt_major ? tile / nft : tile % ntt; };
 
     pdl_trigger();
     if (threadIdx.x == 0) {
@@ -492,9 +482,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         // Stage i of the ring holds unit u_begin + i; the whole warp runs the
         // loop (warp-uniform control) and one elected lane issues the copies.
         const bool leader = elect_one();
-        const uint64_t pol_w = l2_policy_evict_first();
+        // weights are streamed past L2 unless token tiles share them there
+        const uint64_t pol_w = a.tt_major ? l2_policy_evict_normal() : l2_policy_evict_first();
         auto load_w = [&](int u, int s) {
-            const int tile = u / nkb, kb = u - tile * nkb, ft = tile / ntt;
+            const int tile = u / nkb, kb = u - tile * nkb, ft = ft_of(tile);
             uint8_t *sa = smem + (size_t)s * stage_bytes;
             if (a.w_packed)  // tile (ft, kb) is one contiguous 16 KiB block, already in the swizzled image
                 bulk_load(sa, a.w_packed + ((size_t)ft * nkb + kb) * (BM * BK), kStageA, &full[s], pol_w);
@@ -502,7 +493,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 tma_load_2d(sa, &tmw, &full[s], kb * BK, ft * BM);
         };
         auto load_x = [&](int u, int s) {
-            const int tile = u / nkb, kb = u - tile * nkb, tt = tile % ntt;
+            const int tile = u / nkb, kb = u - tile * nkb, tt = tt_of(tile);
             tma_load_2d(smem + (size_t)s * stage_bytes + kStageA, &tmx, &full[s], kb * BK, tt * a.bn);
         };
         const int n_mine = u_end - u_begin;
@@ -600,7 +591,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             const int tile = u / nkb, k0 = u - tile * nkb, k1 = min(nkb, k0 + (u_end - u));
             u += k1 - k0;
             const int buf = p & 1;
-            const int ft = tile / ntt, tt = tile - ft * ntt;
+            const int ft = ft_of(tile), tt = tt_of(tile);
             const int t_base = tt * a.bn, t_lim = min(a.bn, a.m_tok - t_base);
             const int f = ft * BM + row;
             const bool f_ok = f < a.n_out;
@@ -832,10 +823,7 @@ int override_stages() {
     static int v = env_int("ORCA_GEMM_STAGES");
     return v;
 }
-int override_kpb() {
-    static int v = env_int("ORCA_GEMM_KPB");
-    return v;
-}
+
 // ORCA_GEMM_SK: 1 = stream-K whenever the workspace allows, -1 = never,
 // unset / 0 = by token rows (kSkMinRows).
 int override_sk() {
@@ -883,10 +871,7 @@ TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool al
     // one CTA per SM with a deep ring when everything runs in one wave, else two
     const int ctas_per_sm = (tiles * t.splits > s.num_sms && t.bn <= 128) ? 2 : 1;
     const size_t budget = std::min(kSmemMaxCta, kSmemPerSm / ctas_per_sm - kSmemReserve) - kSmemExtra;
-    // K blocks per ring stage: at least two stages must fit
-    t.kpb = std::max(1, std::min(override_kpb() > 0 ? override_kpb() : 1, t.kb_per_split));
-    while (t.kpb > 1 && budget / (size_t)(t.kpb * (kStageA + t.bn * BK * 2)) < 2) --t.kpb;
-    const int stage_bytes = t.kpb * (kStageA + t.bn * BK * 2);
+    const int stage_bytes = kStageA + t.bn * BK * 2;
     const size_t max_stages_1cta = (kSmemMaxCta - kSmemExtra) / stage_bytes;
     t.stages = std::min<int>(kMaxStages, (int)(budget / stage_bytes));
     if (override_stages() > 0) t.stages = std::min<int>(std::min(override_stages(), kMaxStages), (int)max_stages_1cta);
@@ -958,6 +943,8 @@ cudaError_t launch_sk(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_packe
     a.bn = t.bn;
     a.stages = t.stages;
     a.n_tok_tiles = t.n_tok_tiles;
+    a.n_feat_tiles = t.n_feat_tiles;
+    a.tt_major = t.n_tok_tiles >= 4;
     a.n_units = t.units;
     a.chunk = t.chunk;
     a.idesc = idesc_bf16_f32(BM, t.bn);
@@ -991,7 +978,7 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_pa
     if (gemm_uses_sk(m_tok, n_out, k, s)) return launch_sk(x, x_rows_cap, w, w_packed, m_tok, n_out, k, e, s, st);
     const bool allow_partial = e.part != nullptr && !(reinterpret_cast<uintptr_t>(e.part) & 15);
     const TcShape t = gemm_tc_shape(m_tok, n_out, k, s, allow_partial, e.part_cap);
-    if (t.stages < 2 || (size_t)t.stages * t.kpb * (kStageA + t.bn * BK * 2) < (size_t)t.bn * BM * 4)
+    if (t.stages < 2 || (size_t)t.stages * (kStageA + t.bn * BK * 2) < (size_t)t.bn * BM * 4)
         return cudaErrorInvalidValue;
     static bool attr_done = false;
     if (!attr_done) {
@@ -1012,7 +999,6 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_pa
     a.splits = t.splits;
     a.bn = t.bn;
     a.stages = t.stages;
-    a.kpb = t.kpb;
     a.n_feat_tiles = t.n_feat_tiles;
     a.n_tok_tiles = t.n_tok_tiles;
     a.idesc = idesc_bf16_f32(BM, t.bn);

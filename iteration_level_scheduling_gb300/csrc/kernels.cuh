@@ -61,7 +61,7 @@ size_t packed_weight_elems(int n_out, int k);
 cudaError_t pack_weight_bf16(const bf16 *w, int n_out, int k, bf16 *out, cudaStream_t st);
 // Shape the tcgen05 GEMM would use (for scratch sizing and accounting).
 struct TcShape {
-    int bn, n_tok_tiles, n_feat_tiles, splits, kb_per_split, kpb, stages, tmem_cols;
+    int bn, n_tok_tiles, n_feat_tiles, splits, kb_per_split, stages, tmem_cols;
     size_t smem;
 };
 TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool allow_partial = false,

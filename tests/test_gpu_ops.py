@@ -46,6 +46,9 @@ SHAPES = [
     # holding a first and a last piece, three whole tiles per CTA (accumulator
     # buffer reuse), ragged rows and features
     (136, 12800, 320), (200, 6400, 192), (144, 51200, 64), (129, 1000, 2048),
+    # stream-K over several token tiles: feature-tile major with cut tiles (2
+    # token tiles), token-tile major with cut tiles (5 token tiles)
+    (300, 12800, 320), (1100, 5120, 512),
 ]
 
 
