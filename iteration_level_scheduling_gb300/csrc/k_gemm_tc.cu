@@ -71,7 +71,9 @@ constexpr size_t kSmemExtra = 1024 + 256;  // alignment slack + barriers
 struct TcArgs {
     int m_tok, n_out, num_kb, kb_per_split, splits, bn, stages;
     int n_feat_tiles, n_tok_tiles;
-    uint32_t idesc, tmem_cols;
+    // a token tile of more than 256 rows is two MMAs per K step: columns
+    // [0, 256) with idesc, [256, bn) with idesc1 (TMEM columns likewise)
+    uint32_t idesc, idesc1, tmem_cols;
     Epilogue e;
     int vec_out;  // output / residual rows allow 16-byte (fp32) or 8-byte (bf16) vector access
     int mode;     // kDirect, or kPartial (split-K slabs to e.part)
@@ -106,8 +108,14 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
 
 __device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
 
+// kWide: token tiles of more than 256 rows, two activation boxes and two MMAs
+// per K step (a separate instantiation: the single MMA-issuing lane is on the
+// critical path of the ordinary kernel, and a run-time branch beside every MMA
+// cost it up to 20 % at decode sizes).
+template <bool kWide>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
+                   const __grid_constant__ CUtensorMap tmx1, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stage_b = a.bn * BK * 2;
@@ -128,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nkb = min(a.num_kb, kb0 + a.kb_per_split) - kb0;
     const int t_base = tt * a.bn;
     const int t_lim = min(a.bn, a.m_tok - t_base);  // valid token columns of this tile
+    const int bn0 = kWide ? 256 : a.bn;  // rows of the first activation box (the second: a.bn - 256)
 
     pdl_trigger();
     if (threadIdx.x == 0) {
@@ -140,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         prefetch_tmap(&tmw);
         prefetch_tmap(&tmx);
+        if (kWide) prefetch_tmap(&tmx1);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, a.tmem_cols);
@@ -179,9 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load_w(i, i);
             }
         pdl_wait();
+        auto load_x = [&](int i, int s) {
+            uint8_t *sb = smem + (size_t)s * stage_bytes + kStageA;
+            tma_load_2d(sb, &tmx, &full[s], (kb0 + i) * BK, t_base);
+            if constexpr (kWide) tma_load_2d(sb + bn0 * (BK * 2), &tmx1, &full[s], (kb0 + i) * BK, t_base + bn0);
+        };
         if (leader)
-            for (int i = 0; i < pre; ++i)
-                tma_load_2d(smem + (size_t)i * stage_bytes + kStageA, &tmx, &full[i], (kb0 + i) * BK, t_base);
+            for (int i = 0; i < pre; ++i) load_x(i, i);
         __syncwarp();
         int issued = pre;
         bool ok = true;
@@ -195,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) {
                 mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
                 load_w(i, s);
-                tma_load_2d(smem + (size_t)s * stage_bytes + kStageA, &tmx, &full[s], (kb0 + i) * BK, t_base);
+                load_x(i, s);
             }
             __syncwarp();
             ++issued;
@@ -226,6 +240,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < BK / 16; ++kk)  // 16 bf16 = 32 B per MMA: +2 in the >>4 address field
                     tc_mma_f16(tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), a.idesc,
                                (uint32_t)((i | kk) != 0));
+                if constexpr (kWide) {  // token columns 256.. into TMEM columns 256..
+                    const uint64_t bd1 = smem_desc_k128(sa + kStageA + (uint32_t)(bn0 * BK * 2));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc_mma_f16(tmem + 256u, ad + (uint64_t)(2 * kk), bd1 + (uint64_t)(2 * kk), a.idesc1,
+                                   (uint32_t)((i | kk) != 0));
+                }
                 tc_commit(&empty[s]);
             }
             __syncwarp();
@@ -239,111 +260,123 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // --------- epilogue phase 1: TMEM -> shared memory tile [token][feature] ---------
+        // the accumulator is complete once `done` fires (every MMA, hence every
+        // load of the ring, has finished): the ring may then hold the staged tile
         pdl_wait();
-        const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;  // output feature within the tile
         bool ok = mbar_wait_bounded(done, 0, a.err);
         tc_fence_after();
         ok = epilogue_all(ok && flags[0] == 0);  // the four epilogue warps take the same branch
-        __syncwarp();                            // tcgen05.ld is .sync.aligned
-        if (ok) {
-            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-            for (int c0 = 0; c0 < t_lim; c0 += 16) {
-                float v[16];
-                tmem_ld16(taddr + c0, v);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) stage_c[(c0 + j) * BM + row] = v[j];
-            }
-        } else if (threadIdx.x == 64) {
-            flags[0] = 1;
-        }
+        if (!ok && threadIdx.x == 64) flags[0] = 1;
     }
     tc_fence_before();
     __syncwarp();
     __syncthreads();
 
-    // --------- epilogue phase 2: reduce the split partials, bias / GeLU / residual, store ---------
-    if (flags[0] == 0 && a.mode == kPartial) {
-        // this split's partial tile, as is, to slab `split` of the workspace
-        const int f0 = ft * BM + 4 * lane;
-        if (f0 < a.n_out) {
-            float *slab = a.e.part + (size_t)split * a.m_tok * a.n_out;
-            for (int t = warp; t < t_lim; t += kWarps)
-                *reinterpret_cast<float4 *>(slab + (size_t)(t_base + t) * a.n_out + f0) =
-                    *reinterpret_cast<const float4 *>(stage_c + t * BM + 4 * lane);
-        }
-    } else if (flags[0] == 0) {
-        const Epilogue &e = a.e;
-        const int f0 = ft * BM + 4 * lane;
-        const bool full4 = a.vec_out && f0 + 3 < a.n_out;
-        float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (e.bias) {
-            if (f0 + 0 < a.n_out) bias.x = e.bias[f0 + 0];
-            if (f0 + 1 < a.n_out) bias.y = e.bias[f0 + 1];
-            if (f0 + 2 < a.n_out) bias.z = e.bias[f0 + 2];
-            if (f0 + 3 < a.n_out) bias.w = e.bias[f0 + 3];
-        }
-        const int r0 = 0, r1 = t_lim;
-        // K/V append: output features >= kv_h go to the pool at the row's slot
-        bf16 *kv_dst = nullptr;
-        if (e.kv_pool && f0 >= e.kv_h && f0 < a.n_out) {
-            int c = f0 - e.kv_h;
-            const int which = c >= e.kv_h;
-            c -= which * e.kv_h;
-            const int head = c / e.kv_hd;
-            kv_dst = e.kv_pool + ((size_t)(which * e.kv_nh + head) * e.kv_slots) * e.kv_hd + (c - head * e.kv_hd);
-        }
-        for (int t0 = r0 + warp * kRows; t0 < r1; t0 += kWarps * kRows) {
-            float4 acc[kRows];
-            float4 res[kRows];
+    // The epilogue in halves of at most 256 token columns (the staged fp32 half
+    // tile, 128 KiB at most, fits in the ring).
+    for (int cb = 0; cb < t_lim; cb += 256) {
+        const int r1 = min(256, t_lim - cb);  // token rows of this half
+        const int tb = t_base + cb;          // their first token
+        if (cb > 0) __syncthreads();         // the previous half is stored
+        // --------- phase 1: TMEM -> shared memory tile [token][feature] ---------
+        if (warp >= 2 && flags[0] == 0) {
+            const int quarter = warp & 3;
+            const int row = quarter * 32 + lane;  // output feature within the tile
+            __syncwarp();                         // tcgen05.ld is .sync.aligned
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+            for (int c0 = 0; c0 < r1; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr + (uint32_t)(cb + c0), v);
 #pragma unroll
-            for (int u = 0; u < kRows; ++u) {
-                const int t = t0 + u;
-                acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                res[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (t < r1) {
-                    acc[u] = *reinterpret_cast<const float4 *>(stage_c + t * BM + 4 * lane);
-                    if (e.resid && full4)
-                        res[u] = *reinterpret_cast<const float4 *>(e.resid + (size_t)(t_base + t) * e.ld_out + f0);
-                }
+                for (int j = 0; j < 16; ++j) stage_c[(c0 + j) * BM + row] = v[j];
             }
-#pragma unroll
-            for (int u = 0; u < kRows; ++u) {
-                const int t = t0 + u;
-                if (t >= r1) break;
-                float y[4] = {acc[u].x + bias.x, acc[u].y + bias.y, acc[u].z + bias.z, acc[u].w + bias.w};
-                if (e.gelu) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) y[q] = gelu_erf(y[q]);
-                }
-                const size_t o = (size_t)(t_base + t) * e.ld_out + f0;
-                if (full4) {
-                    if (e.resid) {
-                        *reinterpret_cast<float4 *>(e.out_f32 + o) =
-                            make_float4(res[u].x + y[0], res[u].y + y[1], res[u].z + y[2], res[u].w + y[3]);
-                    } else if (e.out_f32) {
-                        *reinterpret_cast<float4 *>(e.out_f32 + o) = make_float4(y[0], y[1], y[2], y[3]);
-                    } else {
-                        __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]), hi = __floats2bfloat162_rn(y[2], y[3]);
-                        uint2 pk;
-                        pk.x = *reinterpret_cast<uint32_t *>(&lo);
-                        pk.y = *reinterpret_cast<uint32_t *>(&hi);
-                        if (kv_dst)
-                            *reinterpret_cast<uint2 *>(kv_dst + (size_t)e.row_slot[t_base + t] * e.kv_hd) = pk;
-                        else
-                            *reinterpret_cast<uint2 *>(e.out_bf16 + o) = pk;
+        }
+        tc_fence_before();
+        __syncwarp();
+        __syncthreads();
+
+        // --------- phase 2: split partials, or bias / GeLU / residual, stored ---------
+        if (flags[0] == 0 && a.mode == kPartial) {
+            // this split's partial tile, as is, to slab `split` of the workspace
+            const int f0 = ft * BM + 4 * lane;
+            if (f0 < a.n_out) {
+                float *slab = a.e.part + (size_t)split * a.m_tok * a.n_out;
+                for (int t = warp; t < r1; t += kWarps)
+                    *reinterpret_cast<float4 *>(slab + (size_t)(tb + t) * a.n_out + f0) =
+                        *reinterpret_cast<const float4 *>(stage_c + t * BM + 4 * lane);
+            }
+        } else if (flags[0] == 0) {
+            const Epilogue &e = a.e;
+            const int f0 = ft * BM + 4 * lane;
+            const bool full4 = a.vec_out && f0 + 3 < a.n_out;
+            float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e.bias) {
+                if (f0 + 0 < a.n_out) bias.x = e.bias[f0 + 0];
+                if (f0 + 1 < a.n_out) bias.y = e.bias[f0 + 1];
+                if (f0 + 2 < a.n_out) bias.z = e.bias[f0 + 2];
+                if (f0 + 3 < a.n_out) bias.w = e.bias[f0 + 3];
+            }
+            // K/V append: output features >= kv_h go to the pool at the row's slot
+            bf16 *kv_dst = nullptr;
+            if (e.kv_pool && f0 >= e.kv_h && f0 < a.n_out) {
+                int c = f0 - e.kv_h;
+                const int which = c >= e.kv_h;
+                c -= which * e.kv_h;
+                const int head = c / e.kv_hd;
+                kv_dst = e.kv_pool + ((size_t)(which * e.kv_nh + head) * e.kv_slots) * e.kv_hd + (c - head * e.kv_hd);
+            }
+            for (int t0 = warp * kRows; t0 < r1; t0 += kWarps * kRows) {
+                float4 acc[kRows];
+                float4 res[kRows];
+    #pragma unroll
+                for (int u = 0; u < kRows; ++u) {
+                    const int t = t0 + u;
+                    acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    res[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (t < r1) {
+                        acc[u] = *reinterpret_cast<const float4 *>(stage_c + t * BM + 4 * lane);
+                        if (e.resid && full4)
+                            res[u] = *reinterpret_cast<const float4 *>(e.resid + (size_t)(tb + t) * e.ld_out + f0);
                     }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (f0 + q >= a.n_out) break;
-                        if (e.resid)
-                            e.out_f32[o + q] = e.resid[o + q] + y[q];
-                        else if (e.out_f32)
-                            e.out_f32[o + q] = y[q];
-                        else
-                            e.out_bf16[o + q] = __float2bfloat16_rn(y[q]);
+                }
+    #pragma unroll
+                for (int u = 0; u < kRows; ++u) {
+                    const int t = t0 + u;
+                    if (t >= r1) break;
+                    float y[4] = {acc[u].x + bias.x, acc[u].y + bias.y, acc[u].z + bias.z, acc[u].w + bias.w};
+                    if (e.gelu) {
+    #pragma unroll
+                        for (int q = 0; q < 4; ++q) y[q] = gelu_erf(y[q]);
+                    }
+                    const size_t o = (size_t)(tb + t) * e.ld_out + f0;
+                    if (full4) {
+                        if (e.resid) {
+                            *reinterpret_cast<float4 *>(e.out_f32 + o) =
+                                make_float4(res[u].x + y[0], res[u].y + y[1], res[u].z + y[2], res[u].w + y[3]);
+                        } else if (e.out_f32) {
+                            *reinterpret_cast<float4 *>(e.out_f32 + o) = make_float4(y[0], y[1], y[2], y[3]);
+                        } else {
+                            __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]), hi = __floats2bfloat162_rn(y[2], y[3]);
+                            uint2 pk;
+                            pk.x = *reinterpret_cast<uint32_t *>(&lo);
+                            pk.y = *reinterpret_cast<uint32_t *>(&hi);
+                            if (kv_dst)
+                                *reinterpret_cast<uint2 *>(kv_dst + (size_t)e.row_slot[tb + t] * e.kv_hd) = pk;
+                            else
+                                *reinterpret_cast<uint2 *>(e.out_bf16 + o) = pk;
+                        }
+                    } else {
+    #pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if (f0 + q >= a.n_out) break;
+                            if (e.resid)
+                                e.out_f32[o + q] = e.resid[o + q] + y[q];
+                            else if (e.out_f32)
+                                e.out_f32[o + q] = y[q];
+                            else
+                                e.out_bf16[o + q] = __float2bfloat16_rn(y[q]);
+                        }
                     }
                 }
             }
@@ -850,10 +883,19 @@ bool encode_tensor_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t rank, co
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool allow_partial, size_t part_cap) {
+namespace {
+
+// Widest token tile: two MMAs per K step (256 + up to 192 columns of TMEM) and
+// a ring of three 72 KiB stages.
+constexpr int kMaxBn = 448;
+
+// Launch shape with `ntt` token tiles.
+TcShape tc_shape_tiles(int m_tok, int n_out, int k, const GemmScratch &s, bool allow_partial, size_t part_cap,
+                       int ntt) {
     TcShape t{};
-    t.n_tok_tiles = ceil_div(std::max(m_tok, 1), 256);
-    t.bn = std::min(256, std::max(16, ceil_div(ceil_div(std::max(m_tok, 1), t.n_tok_tiles), 16) * 16));
+    const int m = std::max(m_tok, 1);
+    t.n_tok_tiles = ntt;
+    t.bn = std::min(kMaxBn, std::max(16, ceil_div(ceil_div(m, ntt), 16) * 16));
     t.n_feat_tiles = ceil_div(n_out, BM);
     t.tmem_cols = 32;
     while ((int)t.tmem_cols < t.bn) t.tmem_cols *= 2;
@@ -875,10 +917,51 @@ TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool al
     const size_t max_stages_1cta = (kSmemMaxCta - kSmemExtra) / stage_bytes;
     t.stages = std::min<int>(kMaxStages, (int)(budget / stage_bytes));
     if (override_stages() > 0) t.stages = std::min<int>(std::min(override_stages(), kMaxStages), (int)max_stages_1cta);
-    // the ring must also hold the staged fp32 accumulator tile (bn x 512 B) after the mainloop
-    while ((size_t)t.stages * stage_bytes < (size_t)t.bn * BM * 4 && t.stages < (int)max_stages_1cta) ++t.stages;
+    // the ring must also hold a staged fp32 half tile (min(bn, 256) x 512 B) after the mainloop
+    while ((size_t)t.stages * stage_bytes < (size_t)std::min(t.bn, 256) * BM * 4 && t.stages < (int)max_stages_1cta)
+        ++t.stages;
     t.smem = (size_t)t.stages * stage_bytes + kSmemExtra;
     return t;
+}
+
+// Modelled time of a shape (microseconds): rounds of CTAs, each taking its K
+// blocks at the time one ring stage of a token tile of bn rows was measured to
+// take on a GB300 (one CTA per SM, 13B layer shapes, stand-alone launches:
+// 0.46 us at 64 rows, where streaming the 16 KiB weight block bounds it, 0.47
+// at 176, 0.58 at 192, 0.835 at 304, 0.86 at 336, 0.94 at 448; linear in
+// between), plus a fixed cost per round for the pipeline fill and epilogue.
+double tc_stage_us(int bn) {
+    static const double pts[][2] = {{64, 0.46}, {176, 0.47}, {192, 0.58}, {304, 0.835}, {336, 0.86}, {448, 0.94}};
+    const int n = (int)(sizeof(pts) / sizeof(pts[0]));
+    if (bn <= pts[0][0]) return pts[0][1];
+    for (int i = 1; i < n; ++i)
+        if (bn <= pts[i][0])
+            return pts[i - 1][1] + (bn - pts[i - 1][0]) * (pts[i][1] - pts[i - 1][1]) / (pts[i][0] - pts[i - 1][0]);
+    return pts[n - 1][1];
+}
+double tc_model_us(const TcShape &t, int num_sms) {
+    const int ctas = t.n_tok_tiles * t.n_feat_tiles * t.splits;
+    const int per_round = std::max(1, num_sms) * ((ctas > num_sms && t.bn <= 128) ? 2 : 1);
+    const int rounds = ceil_div(ctas, per_round);
+    return rounds * (t.kb_per_split * tc_stage_us(t.bn) + 4.0);
+}
+
+}  // namespace
+
+// Token tiles of at most 256 rows; with 257..448 rows one wide token tile when
+// all its CTAs run in one round and the model prefers it (its weights are then
+// streamed once instead of once per token tile, and fewer tiles leave room for
+// split-K).  Measured on the 13B shapes: QKV at 335 rows 74.8 -> 68.8 us; FFN1,
+// whose 160 wide tiles need two rounds, 115 -> 146 us, hence the round rule.
+TcShape gemm_tc_shape(int m_tok, int n_out, int k, const GemmScratch &s, bool allow_partial, size_t part_cap) {
+    const int m = std::max(m_tok, 1);
+    TcShape best = tc_shape_tiles(m_tok, n_out, k, s, allow_partial, part_cap, ceil_div(m, 256));
+    if (m > 256 && m <= kMaxBn) {
+        const TcShape one = tc_shape_tiles(m_tok, n_out, k, s, allow_partial, part_cap, 1);
+        if (one.n_feat_tiles * one.splits <= s.num_sms && tc_model_us(one, s.num_sms) < tc_model_us(best, s.num_sms))
+            best = one;
+    }
+    return best;
 }
 
 size_t packed_weight_elems(int n_out, int k) { return (size_t)ceil_div(n_out, BM) * BM * (size_t)k; }
@@ -978,18 +1061,22 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_pa
     if (gemm_uses_sk(m_tok, n_out, k, s)) return launch_sk(x, x_rows_cap, w, w_packed, m_tok, n_out, k, e, s, st);
     const bool allow_partial = e.part != nullptr && !(reinterpret_cast<uintptr_t>(e.part) & 15);
     const TcShape t = gemm_tc_shape(m_tok, n_out, k, s, allow_partial, e.part_cap);
-    if (t.stages < 2 || (size_t)t.stages * (kStageA + t.bn * BK * 2) < (size_t)t.bn * BM * 4)
+    if (t.stages < 2 || (size_t)t.stages * (kStageA + t.bn * BK * 2) < (size_t)std::min(t.bn, 256) * BM * 4)
         return cudaErrorInvalidValue;
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t ae = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t ae = cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               (int)kSmemMaxCta);
+        if (ae == cudaSuccess)
+            ae = cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kSmemMaxCta);
         if (ae != cudaSuccess) return ae;
         attr_done = true;
     }
-    CUtensorMap mw, mx;
-    if (w_packed && (reinterpret_cast<uintptr_t>(w) & 15)) return cudaErrorInvalidValue;
-    if (!make_map(&mw, w, w_packed ? BM : n_out, k, BM) || !make_map(&mx, x, x_rows_cap, k, t.bn))
+    CUtensorMap mw, mx, mx1;
+    const int bn0 = std::min(t.bn, 256), bn1 = t.bn - bn0;
+    if (!make_map(&mw, w, w_packed ? BM : n_out, k, BM) || !make_map(&mx, x, x_rows_cap, k, bn0) ||
+        !make_map(&mx1, x, x_rows_cap, k, bn1 ? bn1 : bn0))
         return cudaErrorInvalidValue;  // (the weight map is unused when the weights are packed)
     TcArgs a;
     a.m_tok = m_tok;
@@ -1001,7 +1088,8 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_pa
     a.stages = t.stages;
     a.n_feat_tiles = t.n_feat_tiles;
     a.n_tok_tiles = t.n_tok_tiles;
-    a.idesc = idesc_bf16_f32(BM, t.bn);
+    a.idesc = idesc_bf16_f32(BM, bn0);
+    a.idesc1 = idesc_bf16_f32(BM, bn1 ? bn1 : 16);
     a.tmem_cols = (uint32_t)t.tmem_cols;
     a.e = e;
     const uintptr_t align_mask = e.out_bf16 ? 7 : 15;
@@ -1023,7 +1111,8 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_pa
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, mw, mx, a);
+    return bn1 ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, mw, mx, mx1, a)
+               : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false>, mw, mx, mx1, a);
 }
 
 cudaError_t pack_weight_bf16(const bf16 *w, int n_out, int k, bf16 *out, cudaStream_t st) {

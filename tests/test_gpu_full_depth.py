@@ -111,3 +111,27 @@ def test_gpt3_13b_prefill_heavy_iteration():
     print(r)
     assert r["argmax_ok"]
     assert r["h"] <= TOL_BF16 and r["l"] <= TOL_BF16, r
+
+
+def test_gpt3_13b_mid_rows_iteration():
+    """13B shape, 40 layers: one 300-token prompt with 63 increment requests (363
+    rows, like the prompt-carrying iterations of the bench trace): the linear
+    layers run one wide token tile (two MMAs per K step), the residual
+    projections with split-K slabs."""
+    from iteration_level_scheduling_gb300 import native
+    cfg = bench.MODEL
+    g = np.random.default_rng(6)
+    ctx_inc = g.integers(64, 900, 63).tolist()
+    n = [300] + [1] * 63
+    ctx = [0] + ctx_inc
+    B, rows = len(n), sum(n)
+    need = [c + k for c, k in zip(ctx, n)]
+    keep, eng = make(cfg, rows, B, sum(need), 3)
+    offs = [eng.kv_alloc(i, need[i]) for i in range(B)]
+    toks = g.integers(0, cfg.vocab, rows).tolist()
+    b = native.BatchDesc(list(range(B)), [1 if c else 0 for c in ctx], n, ctx, offs, toks)
+    r = full_depth_check(eng, keep, cfg, b, pick(ctx, n))
+    release(keep, eng)
+    print(r)
+    assert r["argmax_ok"]
+    assert r["h"] <= TOL_BF16 and r["l"] <= TOL_BF16, r

@@ -154,6 +154,25 @@ def test_linear_sk_repeatable(eng):
         assert torch.equal(outs[0], o)
 
 
+def test_linear_wide_token_tile(eng):
+    """257..448 rows in one token tile (two MMAs per K step, the epilogue in two
+    256-column halves), in a process where stand-alone calls may not take the
+    stream-K kernel: every epilogue, packed and unpacked weights, ragged rows."""
+    import json
+    import os
+    import subprocess
+    import sys
+    env = dict(os.environ, ORCA_GEMM_SK="-1")
+    child = os.path.join(os.path.dirname(__file__), "wide_tile_child.py")
+    out = subprocess.run([sys.executable, child], env=env, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    rows = [json.loads(line) for line in out.stdout.splitlines() if line.startswith("{")]
+    assert len(rows) == 4 * 3 * 2
+    for r in rows:
+        tol = 1e-5 * max(1.0, np.sqrt(r["k"] / 1024)) if r["mode"] == "bias_resid_f32" else 8e-3
+        assert r["rel"] < tol, r
+
+
 @pytest.mark.parametrize("m,n,k", [(1, 64, 64), (37, 256, 64), (130, 200, 256), (64, 512, 20)])
 def test_linear_simt_f32(eng, m, n, k):
     from iteration_level_scheduling_gb300 import native
