@@ -96,11 +96,11 @@ struct orca_engine {
     int32_t *h_next = nullptr;
     int32_t *h_plan = nullptr, *d_plan = nullptr;
     int64_t plan_cap = 0;
-    // GEMM launch contexts: `gs` for the iteration (one-tile-per-CTA kernel
-    // only), `gs_op` for stand-alone orca_op_linear calls (stream-K allowed).
-    // Inside an iteration the stream-K kernel, which fills every SM, is slower
-    // end to end: the one-tile kernel's idle SMs let the next launch start
-    // early under programmatic launch.
+    // GEMM launch contexts: `gs` without a stream-K workspace (one-tile-per-CTA
+    // kernel only), `gs_op` with one (stream-K allowed: stand-alone
+    // orca_op_linear calls and FFN1).  Inside an iteration the stream-K kernel,
+    // which fills every SM, is mostly slower end to end: the one-tile kernel's
+    // idle SMs let the next launch start early under programmatic launch.
     GemmScratch gs, gs_op;
     float *part = nullptr;  // split-K partial slabs of the residual projections
     size_t part_cap = 0;
@@ -305,13 +305,18 @@ int build(orca_engine *E, const orca_batch *b, int32_t *buf, int64_t cap) {
     return ORCA_OK;
 }
 
+// stream_k: the layer may take the stream-K kernel (E->gs_op carries its
+// workspace).  Only FFN1 does inside an iteration: its 160 output tiles at
+// the 13B shape quantise worst on 152 SMs, and on the same GPU and trace it
+// made prompt-carrying iterations 1 % faster (15.55 -> 15.38 ms, decode-only
+// unchanged), where stream-K for QKV as well had cost 2 %.
 template <typename T>
 cudaError_t linear(orca_engine *E, const void *x, int x_cap, const void *w, int m, int n, int k, const Epilogue &e,
-                   int *n_partials = nullptr) {
+                   int *n_partials = nullptr, bool stream_k = false) {
     if (n_partials) *n_partials = 0;
     if constexpr (std::is_same<T, bf16>::value)
-        return gemm_tc_bf16((const bf16 *)x, x_cap, (const bf16 *)w, E->packed, m, n, k, e, E->gs, E->st,
-                            n_partials);
+        return gemm_tc_bf16((const bf16 *)x, x_cap, (const bf16 *)w, E->packed, m, n, k, e,
+                            stream_k ? E->gs_op : E->gs, E->st, n_partials);
     else
         return gemm_simt_f32((const float *)x, (const float *)w, m, n, k, e, E->st);
 }
@@ -420,7 +425,7 @@ int run_plan(orca_engine *E, const int32_t *hp, const int32_t *dp, int32_t *dev_
             if (std::is_same<T, bf16>::value) e.out_bf16 = (bf16 *)f; else e.out_f32 = (float *)f;
             e.ld_out = F;
             ORCA_TRY(E->launch(ORCA_K_GEMM_FFN1, l, es * ((double)F * H + (double)R * H + (double)R * F),
-                               2.0 * R * F * H, [&] { return linear<T>(E, h, cap, W.w_1, R, F, H, e); }));
+                               2.0 * R * F * H, [&] { return linear<T>(E, h, cap, W.w_1, R, F, H, e, nullptr, true); }));
         }
         {
             Epilogue e;

@@ -29,8 +29,9 @@
 // With 129+ token rows and at least one output tile per SM the stream-K
 // kernel further below takes the layer instead (gemm_uses_sk), when the
 // caller's launch context carries a stream-K workspace.  The engine gives one
-// to stand-alone linear calls only: inside an iteration the one-tile kernel is
-// faster end to end, because its idle SMs let the next launch start early.
+// to stand-alone linear calls and to FFN1 only: elsewhere in an iteration the
+// one-tile kernel is faster end to end, because its idle SMs let the next
+// launch start early.
 //
 // Weights can be pre-packed (pack_weight_bf16) so each 128 x 64 stage tile is
 // one contiguous, already swizzled 16 KiB block read by a single bulk copy:
