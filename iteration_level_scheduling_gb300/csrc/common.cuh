@@ -188,6 +188,10 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
         "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
+// Pull the line holding `p` into this SM's L1 ahead of a later load.
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -103,6 +103,18 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(float *x, const i
                                                                const float *add_bias) {
     __shared__ float red[33];
     pdl_trigger();
+    // gamma, beta and the completed projection's bias are weights: pulled into
+    // L1 before waiting for the previous kernel, so their loads after the
+    // reductions do not add a memory round trip
+#pragma unroll
+    for (int i = 0; i < kLnMaxVec; ++i) {
+        const int e = (threadIdx.x + i * kLnThreads) * 4;
+        if (e < H) {
+            prefetch_l1(g + e);
+            prefetch_l1(b + e);
+            if (n_part > 0 && add_bias) prefetch_l1(add_bias + e);
+        }
+    }
     pdl_wait();
     const int r = blockIdx.x;
     const int src = row_map ? row_map[r] : r;
