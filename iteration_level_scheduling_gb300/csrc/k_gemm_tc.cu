@@ -200,9 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         int issued = pre;
         bool ok = true;
+        // ring slot and phase kept as running counters (no division per stage:
+        // this loop is on the critical path)
+        int s = pre == a.stages ? 0 : pre;
+        uint32_t ph = pre == a.stages ? 1u : 0u;
         for (int i = pre; i < nkb; ++i) {
-            const int s = i % a.stages;
-            const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], ph ^ 1u, a.err))) {
                 ok = false;
                 break;
@@ -214,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             ++issued;
+            if (++s == a.stages) s = 0, ph ^= 1u;
         }
         if (!ok && leader) {
             flags[0] = 1;
@@ -226,9 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_wait();
         const bool leader = elect_one();
         bool ok = true;
+        int s = 0;
+        uint32_t ph = 0u;
         for (int i = 0; i < nkb; ++i) {
-            const int s = i % a.stages;
-            const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], ph, a.err))) {
                 ok = false;
                 break;
@@ -251,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit(&empty[s]);
             }
             __syncwarp();
+            if (++s == a.stages) s = 0, ph ^= 1u;
         }
         if (leader) {
             if (ok) {
