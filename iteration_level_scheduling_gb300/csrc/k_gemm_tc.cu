@@ -522,47 +522,77 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const bool leader = elect_one();
         // weights are streamed past L2 unless token tiles share them there
         const uint64_t pol_w = a.tt_major ? l2_policy_evict_normal() : l2_policy_evict_first();
-        auto load_w = [&](int u, int s) {
-            const int tile = u / nkb, kb = u - tile * nkb, ft = ft_of(tile);
+        // A unit's tile and K block are tracked as running counters, and the
+        // ring slot and phase too: no division per stage on this path.
+        struct Cursor {
+            int tile, kb, ft, tt;
+        };
+        auto cursor_at = [&](int u) {
+            Cursor c;
+            c.tile = u / nkb;
+            c.kb = u - c.tile * nkb;
+            c.ft = ft_of(c.tile);
+            c.tt = tt_of(c.tile);
+            return c;
+        };
+        auto step = [&](Cursor &c) {
+            if (++c.kb == nkb) {
+                c.kb = 0;
+                ++c.tile;
+                c.ft = ft_of(c.tile);
+                c.tt = tt_of(c.tile);
+            }
+        };
+        auto load_w = [&](const Cursor &c, int s) {
             uint8_t *sa = smem + (size_t)s * stage_bytes;
             if (a.w_packed)  // tile (ft, kb) is one contiguous 16 KiB block, already in the swizzled image
-                bulk_load(sa, a.w_packed + ((size_t)ft * nkb + kb) * (BM * BK), kStageA, &full[s], pol_w);
+                bulk_load(sa, a.w_packed + ((size_t)c.ft * nkb + c.kb) * (BM * BK), kStageA, &full[s], pol_w);
             else
-                tma_load_2d(sa, &tmw, &full[s], kb * BK, ft * BM);
+                tma_load_2d(sa, &tmw, &full[s], c.kb * BK, c.ft * BM);
         };
-        auto load_x = [&](int u, int s) {
-            const int tile = u / nkb, kb = u - tile * nkb, tt = tt_of(tile);
-            tma_load_2d(smem + (size_t)s * stage_bytes + kStageA, &tmx, &full[s], kb * BK, tt * a.bn);
+        auto load_x = [&](const Cursor &c, int s) {
+            tma_load_2d(smem + (size_t)s * stage_bytes + kStageA, &tmx, &full[s], c.kb * BK, c.tt * a.bn);
         };
         const int n_mine = u_end - u_begin;
         // the weights do not depend on earlier kernels: fill the first stages
         // with weight slices before waiting for the previous kernel
         const int pre = min(n_mine, a.stages);
+        Cursor cw = cursor_at(u_begin);
         if (leader)
             for (int i = 0; i < pre; ++i) {
                 mbar_arrive_expect_tx(&full[i], (uint32_t)stage_bytes);
-                load_w(u_begin + i, i);
+                load_w(cw, i);
+                step(cw);
             }
         pdl_wait();
+        Cursor cx = cursor_at(u_begin);
         if (leader)
-            for (int i = 0; i < pre; ++i) load_x(u_begin + i, i);
+            for (int i = 0; i < pre; ++i) {
+                load_x(cx, i);
+                step(cx);
+            }
         __syncwarp();
+        // the copies of units u_begin + pre .. follow (cw and cx are only
+        // advanced by the leader: recompute them warp-wide)
+        Cursor c = cursor_at(u_begin + pre);
         int issued = pre;
         bool ok = true;
+        int s = pre == a.stages ? 0 : pre;
+        uint32_t ph = pre == a.stages ? 1u : 0u;
         for (int i = pre; i < n_mine; ++i) {
-            const int s = i % a.stages;
-            const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], ph ^ 1u, a.err))) {
                 ok = false;
                 break;
             }
             if (leader) {
                 mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
-                load_w(u_begin + i, s);
-                load_x(u_begin + i, s);
+                load_w(c, s);
+                load_x(c, s);
             }
             __syncwarp();
             ++issued;
+            step(c);
+            if (++s == a.stages) s = 0, ph ^= 1u;
         }
         if (!ok && leader) {
             flags[0] = 1;
@@ -575,6 +605,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const bool leader = elect_one();
         bool ok = true;
         int i = 0, p = 0;
+        int s = 0;  // ring slot and phase of unit u_begin + i
+        uint32_t ph = 0u;
         for (int u = u_begin; u < u_end; ++p) {
             const int tile = u / nkb, k0 = u - tile * nkb, k1 = min(nkb, k0 + (u_end - u));
             const int buf = p & 1;
@@ -588,8 +620,6 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             }
             const uint32_t d_tmem = tmem + (uint32_t)(buf * a.bn);
             for (int kb = k0; kb < k1; ++kb, ++i) {
-                const int s = i % a.stages;
-                const uint32_t ph = (uint32_t)(i / a.stages) & 1u;
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], ph, a.err))) {
                     ok = false;
                     break;
@@ -605,6 +635,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     tc_commit(&empty[s]);
                 }
                 __syncwarp();
+                if (++s == a.stages) s = 0, ph ^= 1u;
             }
             if (!ok) break;
             if (leader) tc_commit(&acc_full[buf]);
