@@ -483,16 +483,16 @@ def run_orca(args, rank, world, local_rank):
     # iteration, so the per-iteration time of a kind is sum(ms * weight) / steps.
     kinds = {}
     for r in recs:
-        k = "gemm_tc (all linear layers)" if r["kind"].startswith("gemm") or r["kind"] == "lm_head" else r["kind"]
+        k = "gemm (all linear layers)" if r["kind"].startswith("gemm") or r["kind"] == "lm_head" else r["kind"]
         wgt = cfg.n_layers if r["layer"] >= 0 else 1
-        for key in (k, "lm_head (gemm_tc)") if r["kind"] == "lm_head" else (k,):
+        for key in (k, "lm_head (gemm)") if r["kind"] == "lm_head" else (k,):
             d = kinds.setdefault(key, dict(ms=0.0, bytes=0.0, flops=0.0, n=0, est=0.0))
             d["ms"] += r["ms"]
             d["bytes"] += r["bytes"]
             d["flops"] += r["flops"]
             d["n"] += 1
             d["est"] += r["ms"] * wgt
-    est_tot = sum(d["est"] for k, d in kinds.items() if k != "lm_head (gemm_tc)") or 1.0
+    est_tot = sum(d["est"] for k, d in kinds.items() if k != "lm_head (gemm)") or 1.0
     breakdown = {k: {"share_of_iteration": d["est"] / est_tot, "est_ms_per_iteration": d["est"] / args.steps,
                      "launches_timed": d["n"], "avg_us": 1000 * d["ms"] / max(d["n"], 1),
                      "GB/s": d["bytes"] / (d["ms"] / 1000) / 1e9 if d["ms"] else None,
@@ -510,7 +510,7 @@ def run_orca(args, rank, world, local_rank):
     gemm_by_kind = {k: {"launches_timed": d["n"], "avg_us": 1000 * d["ms"] / d["n"],
                         "GB/s": d["bytes"] / (d["ms"] / 1000) / 1e9, "TFLOP/s": d["flops"] / (d["ms"] / 1000) / 1e12}
                     for k, d in gk.items() if d["n"] and d["ms"]}
-    dom_name, dom = max(((k, d) for k, d in kinds.items() if k != "lm_head (gemm_tc)"), key=lambda kv: kv[1]["est"])
+    dom_name, dom = max(((k, d) for k, d in kinds.items() if k != "lm_head (gemm)"), key=lambda kv: kv[1]["est"])
     t_hbm = dom["bytes"] / (peaks["hbm"] * 1e9)
     t_tc = dom["flops"] / (peaks["tc_sus"] * 1e12)
     if t_tc > t_hbm:
@@ -519,11 +519,14 @@ def run_orca(args, rank, world, local_rank):
     else:
         ach = dom["bytes"] / (dom["ms"] / 1000) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s"}
-    ratio = profiled_traffic_ratio() if dom_name.startswith("gemm_tc") else None
+    ratio = profiled_traffic_ratio() if dom_name.startswith("gemm") else None
     traffic = ratio * dom["bytes"] / dom["n"] if ratio else None
     roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": traffic, "kernel": dom_name,
                  "traffic_source": ("DRAM bytes per launch: algorithmic bytes x the traffic/algorithmic ratio "
-                                    "of profiles/gemm_tc_decode_gpt3_13b.md (2-layer capture, same shapes)")
+                                    "of profiles/gemm_tc_decode_gpt3_13b.md (2-layer capture, decode shapes); "
+                                    "the stream-K FFN1 launches of prompt-carrying iterations (about 4 % of the "
+                                    "launches) read their weights up to once per token tile "
+                                    "(profiles/gemm_sk_prompt_gpt3_13b.md)")
                  if traffic else None,
                  "peak_source": peaks["src"], "launches_timed": dom["n"],
                  "algorithmic_bytes_per_launch": dom["bytes"] / dom["n"],
