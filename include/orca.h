@@ -223,9 +223,18 @@ int orca_engine_timing_read(orca_engine *eng, orca_kernel_time *out, int32_t cap
  *   else          : out_f32 or out_bf16 (exactly one non-NULL) = y.
  * dtype BF16: x, w bf16 (tcgen05 tensor cores, fp32 accumulation; k % 64 == 0);
  * dtype FP32: x, w fp32 (SIMT FFMA).  Rows of out have stride ld_out.
- * Asynchronous on the engine's stream (uses the engine's split-K scratch, so
- * calls on one engine must not overlap); orca_engine_sync waits and reports
- * device-side errors.  Errors: INVALID (shape / pointer combination), CUDA. */
+ * With 129 or more rows and at least one 128-feature output tile per SM the
+ * bf16 path runs the stream-K kernel (units of 64-wide K blocks spread evenly
+ * over every SM, cut tiles finished by whichever piece arrives last, in a
+ * fixed CTA order, so results are reproducible run to run).
+ * Asynchronous on the engine's stream (uses the engine's stream-K workspace
+ * and arrival counters, so calls on one engine must not overlap);
+ * orca_engine_sync waits and reports device-side errors.
+ * Tuning overrides, read once per process from the environment:
+ * ORCA_GEMM_SK (1 = stream-K whenever the workspace allows, -1 = never),
+ * ORCA_GEMM_STAGES (ring depth cap), ORCA_GEMM_SPLITS (split-K ways where the
+ * caller completes partials; orca_run_iteration only).
+ * Errors: INVALID (shape / pointer combination), CUDA. */
 int orca_op_linear(orca_engine *eng, int32_t dtype, const void *x, const void *w, int32_t w_packed, int32_t m_tok,
                    int32_t n_out, int32_t k, const float *bias, int32_t gelu, const float *resid, float *out_f32,
                    void *out_bf16, int32_t ld_out);

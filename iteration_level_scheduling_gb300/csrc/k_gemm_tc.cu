@@ -879,7 +879,7 @@ bool make_map(CUtensorMap *m, const void *ptr, int rows, int k, int box_rows) {
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Optional tuning overrides (ORCA_GEMM_SPLITS, ORCA_GEMM_STAGES), read once.
+// Optional tuning overrides (ORCA_GEMM_SPLITS, ORCA_GEMM_STAGES, ORCA_GEMM_SK), read once.
 int env_int(const char *name) {
     const char *v = getenv(name);
     return v ? atoi(v) : 0;
