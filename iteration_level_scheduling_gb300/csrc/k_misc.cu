@@ -59,8 +59,8 @@ __global__ void __launch_bounds__(kRowThreads) embed_kernel(const int32_t *token
     }
 }
 
-constexpr int kLnThreads = 1024;
-constexpr int kLnMaxVec = 2;  // H <= kLnThreads * 4 * kLnMaxVec = 8192
+constexpr int kLnThreads = 512;
+constexpr int kLnMaxVec = 4;  // H <= kLnThreads * 4 * kLnMaxVec = 8192
 
 __device__ __forceinline__ float block_sum(float v, float *red) {
     v = warp_sum(v);
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(float *x, const i
     float *xr = x + (size_t)src * H;
     // every load of the row (and of its split-K partials and bias) is issued
     // before the first use
-    constexpr int kInline = 4;  // partial slabs loaded up front (the engine splits K at most 3 ways here)
+    constexpr int kInline = 3;  // partial slabs loaded up front (13B shapes split K at most 3 ways; more: second pass)
     float4 q[kLnMaxVec], bias[kLnMaxVec], pv[kLnMaxVec][kInline];
 #pragma unroll
     for (int i = 0; i < kLnMaxVec; ++i) {
