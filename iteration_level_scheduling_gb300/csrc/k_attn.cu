@@ -743,7 +743,7 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
             const uint64_t pol = l2_policy_evict_first();  // every cached row is read once per iteration
             uint32_t g = 0, issued = 0;
             bool ok = true;
-            int4 r0, r1, n0, n1;
+            int4 r0, n0, n1;  // the producer reads only the first half of a record
             if (nth(0) < total) rec(nth(0), n0, n1);
             for (int k = 0, q = nth(0); q < total && ok; q = nth(++k)) {
                 r0 = n0;

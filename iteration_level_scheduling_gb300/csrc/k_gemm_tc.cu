@@ -9,7 +9,10 @@
 //
 // Orientation ("swap AB"): the weight is the MMA's A operand (M = 128 output
 // features per CTA), the token rows are the B operand (N = BN tokens, a
-// multiple of 16 up to 256).  Both are K-major in memory (w[f, k], x[t, k]), so
+// multiple of 16 up to 256; or one wide tile of 257..448 rows, taken as two
+// MMAs per K step into 512 TMEM columns, in its own kernel instantiation, when
+// a launch model of measured per-stage times prefers it and its CTAs fit one
+// round).  Both are K-major in memory (w[f, k], x[t, k]), so
 // TMA loads 64-wide K slices with 128-byte swizzling straight into the layout
 // tcgen05.mma reads.  The fp32 accumulator tile (128 lanes x BN columns) lives
 // in tensor memory; lane = output feature, column = token.
@@ -37,9 +40,14 @@
 // one contiguous, already swizzled 16 KiB block read by a single bulk copy:
 // sequential DRAM streaming instead of 128 rows of 128 bytes each.
 //
-// Epilogue: + bias, exact GeLU, + residual (fp32), store fp32 or bf16 rows
-// [token, feature] with 16-byte (fp32) or 8-byte (bf16) stores along the
-// feature dimension, four rows per warp in flight.
+// Epilogue: the accumulator is staged in the idle ring (at most 256 token
+// columns at a time), then + bias, exact GeLU, + residual (fp32), store fp32
+// or bf16 rows [token, feature] with 16-byte (fp32) or 8-byte (bf16) stores
+// along the feature dimension, four rows per warp in flight.
+//
+// The producer and MMA loops keep the ring slot and phase as running
+// counters: they are single-thread critical paths, and a division per stage
+// there (the ring depth is a run-time value) cost up to 20 %.
 //
 // Every mbarrier wait is bounded (see common.cuh); on expiry the CTA records
 // an error bit, skips its remaining work and still frees its tensor memory.
@@ -106,8 +114,6 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
         : "memory");
     return r != 0;
 }
-
-__device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
 
 // kWide: token tiles of more than 256 rows, two activation boxes and two MMAs
 // per K step (a separate instantiation: the single MMA-issuing lane is on the
