@@ -220,7 +220,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load_w(i, s);
                 load_x(i, s);
             }
-            __syncwarp();
             ++issued;
             if (++s == a.stages) s = 0, ph ^= 1u;
         }
@@ -259,7 +258,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_commit(&empty[s]);
             }
-            __syncwarp();
             if (++s == a.stages) s = 0, ph ^= 1u;
         }
         if (leader) {
