@@ -67,3 +67,22 @@ def test_iteration_work_counts():
     pairs = 3 * 0 + 3 * 4 // 2 + 11  # prefill rows see 1, 2, 3 keys; the decode row sees 11
     assert w["flops"] == 2.0 * 4 * L * (4 * H * H + 2 * H * F) + 2.0 * 2 * H * V + 4.0 * H * pairs * L
     assert w["kv_bytes"] == (3 + 11) * L * 2 * H * 2
+
+
+def test_split_by_prefill():
+    """Decode-only vs prompt-carrying iterations: counts, mean times, rows and fractions."""
+    import bench
+    work = [dict(R=64, B=64), dict(R=300, B=64), dict(R=64, B=64), dict(R=500, B=64)]
+    out = bench.split_by_prefill(work, [8.0, 14.0, 10.0, 18.0], [0.8, 0.5, 0.6, 0.4])
+    assert out["decode_only"] == {"iterations": 2, "mean_ms": 9.0, "mean_rows": 64.0, "mean_frac": 0.7}
+    assert out["with_prefill"]["iterations"] == 2 and out["with_prefill"]["mean_ms"] == 16.0
+    assert out["with_prefill"]["mean_rows"] == 400.0 and abs(out["with_prefill"]["mean_frac"] - 0.45) < 1e-12
+    assert "with_prefill" not in bench.split_by_prefill(work[:1], [8.0], [0.8])
+
+
+def test_profiled_traffic_ratio_present():
+    """bench.py reads roofline.traffic's DRAM/algorithmic ratio from the committed
+    decode-GEMM ncu summary; the line must be there and near 1 (no re-reads)."""
+    import bench
+    r = bench.profiled_traffic_ratio()
+    assert r is not None and 0.9 < r < 1.1
