@@ -984,13 +984,9 @@ template <typename T, int D>
 cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStream_t st) {
     if constexpr (std::is_same<T, bf16>::value && D % 64 == 0)
         if (decode && a.p.n_dec_work > 0) {
-            static bool attr = false;
-            if (!attr) {
-                cudaError_t e = cudaFuncSetAttribute(attn_decode_mma_kernel<D>,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     (int)md_smem_bytes<D>());
+            {
+                cudaError_t e = max_smem_once((const void *)attn_decode_mma_kernel<D>, (int)md_smem_bytes<D>());
                 if (e != cudaSuccess) return e;
-                attr = true;
             }
             // the layer's pool as [K|V][head] planes of [slot][D]
             CUtensorMap tm, tm16;
@@ -1014,12 +1010,9 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
             decode = false;
         }
     if (decode && a.p.n_dec_work > 0) {
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)sizeof(DecodeSmem<T, D>));
+        {
+            cudaError_t e = max_smem_once((const void *)attn_decode_kernel<T, D>, (int)sizeof(DecodeSmem<T, D>));
             if (e != cudaSuccess) return e;
-            attr = true;
         }
         int sms = 0, dev = 0;
         cudaGetDevice(&dev);
@@ -1032,13 +1025,9 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
     }
     if (prefill && a.p.n_pre_tiles > 0) {
         if constexpr (std::is_same<T, bf16>::value && (D == 64 || D == 128)) {
-            static bool attr = false;
-            if (!attr) {
-                cudaError_t e = cudaFuncSetAttribute(attn_prefill_mma_kernel<D>,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     (int)sizeof(PrefillSmem<D>));
+            {
+                cudaError_t e = max_smem_once((const void *)attn_prefill_mma_kernel<D>, (int)sizeof(PrefillSmem<D>));
                 if (e != cudaSuccess) return e;
-                attr = true;
             }
             cudaError_t e = launch_pdl(attn_prefill_mma_kernel<D>, dim3(a.p.n_pre_tiles, a.n_heads), dim3(128),
                                        sizeof(PrefillSmem<D>), st, a);

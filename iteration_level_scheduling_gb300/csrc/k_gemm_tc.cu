@@ -1049,12 +1049,9 @@ namespace {
 cudaError_t launch_sk(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_packed, int m_tok, int n_out, int k,
                       const Epilogue &e, const GemmScratch &s, cudaStream_t st) {
     const SkShape t = gemm_sk_shape(m_tok, n_out, k, s.num_sms);
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t ae = cudaFuncSetAttribute(gemm_sk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)kSmemMaxCta);
+    {
+        cudaError_t ae = max_smem_once((const void *)gemm_sk_kernel, (int)kSmemMaxCta);
         if (ae != cudaSuccess) return ae;
-        attr_done = true;
     }
     CUtensorMap mw, mx;
     if (!make_map(&mw, w, w_packed ? BM : n_out, k, BM) || !make_map(&mx, x, x_rows_cap, k, t.bn))
@@ -1103,15 +1100,10 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_pa
     const TcShape t = gemm_tc_shape(m_tok, n_out, k, s, allow_partial, e.part_cap);
     if (t.stages < 2 || (size_t)t.stages * (kStageA + t.bn * BK * 2) < (size_t)std::min(t.bn, 256) * BM * 4)
         return cudaErrorInvalidValue;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t ae = cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)kSmemMaxCta);
-        if (ae == cudaSuccess)
-            ae = cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kSmemMaxCta);
+    {
+        cudaError_t ae = max_smem_once((const void *)gemm_tc_kernel<false>, (int)kSmemMaxCta);
+        if (ae == cudaSuccess) ae = max_smem_once((const void *)gemm_tc_kernel<true>, (int)kSmemMaxCta);
         if (ae != cudaSuccess) return ae;
-        attr_done = true;
     }
     CUtensorMap mw, mx, mx1;
     const int bn0 = std::min(t.bn, 256), bn1 = t.bn - bn0;

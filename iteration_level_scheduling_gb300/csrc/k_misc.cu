@@ -6,6 +6,9 @@
 // vector accesses along the row.
 #include <cfloat>
 #include <climits>
+#include <mutex>
+#include <set>
+#include <utility>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -291,5 +294,18 @@ template cudaError_t layernorm<bf16>(float *, const int32_t *, const float *, co
                                      cudaStream_t, const float *, int, int, const float *);
 template cudaError_t kv_append<float>(const float *, const int32_t *, float *, int64_t, int, int, int, cudaStream_t);
 template cudaError_t kv_append<bf16>(const bf16 *, const int32_t *, bf16 *, int64_t, int, int, int, cudaStream_t);
+
+cudaError_t max_smem_once(const void *kernel, int bytes) {
+    static std::mutex mu;
+    static std::set<std::pair<int, const void *>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({dev, kernel})) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert({dev, kernel});
+    return e;
+}
 
 }  // namespace orca

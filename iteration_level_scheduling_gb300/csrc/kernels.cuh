@@ -141,6 +141,12 @@ cudaError_t argmax_rows(const float *logits, int n_rows, int V, int32_t *next, i
 
 constexpr int kPrefillRowsPerTile = 64;
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device.  The attribute belongs to the device that was current when it was
+// set, so it is set once per (device, kernel): an engine or an
+// allocation-free call on another GPU sets its own.
+cudaError_t max_smem_once(const void *kernel, int bytes);
+
 // Launch with programmatic stream serialization (the kernel calls pdl_wait()).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,

@@ -45,12 +45,12 @@ from scipy.special import erf
 LN_EPS = 1e-5
 
 
-def layer_norm(x: np.ndarray, g: np.ndarray, b: np.ndarray, eps: float = LN_EPS) -> np.ndarray:
+def layer_norm(x: np.ndarray, g: np.ndarray, b: np.ndarray, eps: float = LN_EPS, dtype=np.float64) -> np.ndarray:
     """Row-wise LayerNorm: (x - mean) / sqrt(biased var + eps) * g + b."""
-    x = np.asarray(x, np.float64)
+    x = np.asarray(x, dtype)
     mean = x.mean(axis=-1, keepdims=True)
     var = ((x - mean) ** 2).mean(axis=-1, keepdims=True)
-    return (x - mean) / np.sqrt(var + eps) * np.asarray(g, np.float64) + np.asarray(b, np.float64)
+    return (x - mean) / np.sqrt(var + dtype(eps)) * np.asarray(g, dtype) + np.asarray(b, dtype)
 
 
 def gelu(x: np.ndarray) -> np.ndarray:
@@ -79,8 +79,8 @@ class KVStore:
     oracle), since the model's result does not depend on it.
     """
 
-    def __init__(self, n_layers: int, hidden: int):
-        self.n_layers, self.hidden = n_layers, hidden
+    def __init__(self, n_layers: int, hidden: int, dtype=np.float64):
+        self.n_layers, self.hidden, self.dtype = n_layers, hidden, dtype
         self.k: Dict[Tuple[int, int], np.ndarray] = {}
         self.v: Dict[Tuple[int, int], np.ndarray] = {}
 
@@ -89,13 +89,13 @@ class KVStore:
         return 0 if a is None else a.shape[0]
 
     def load(self, rid: int, layer: int, k: np.ndarray, v: np.ndarray) -> None:
-        self.k[(rid, layer)] = np.asarray(k, np.float64).copy()
-        self.v[(rid, layer)] = np.asarray(v, np.float64).copy()
+        self.k[(rid, layer)] = np.asarray(k, self.dtype).copy()
+        self.v[(rid, layer)] = np.asarray(v, self.dtype).copy()
 
     def write(self, rid: int, layer: int, pos: int, k_rows: np.ndarray, v_rows: np.ndarray) -> None:
         """Store rows at positions pos .. pos+n-1 (pos must equal the cached length)."""
-        cur_k = self.k.get((rid, layer), np.zeros((0, self.hidden)))
-        cur_v = self.v.get((rid, layer), np.zeros((0, self.hidden)))
+        cur_k = self.k.get((rid, layer), np.zeros((0, self.hidden), self.dtype))
+        cur_v = self.v.get((rid, layer), np.zeros((0, self.hidden), self.dtype))
         if cur_k.shape[0] != pos:
             raise ValueError(f"request {rid} layer {layer}: cache holds {cur_k.shape[0]} rows, writing at {pos}")
         self.k[(rid, layer)] = np.concatenate([cur_k, k_rows])
@@ -107,7 +107,7 @@ class KVStore:
             self.v.pop((rid, l), None)
 
     def copy(self) -> "KVStore":
-        c = KVStore(self.n_layers, self.hidden)
+        c = KVStore(self.n_layers, self.hidden, self.dtype)
         c.k = {key: a.copy() for key, a in self.k.items()}
         c.v = {key: a.copy() for key, a in self.v.items()}
         return c
@@ -135,9 +135,9 @@ def offsets(batch: Sequence[BatchItem]) -> List[int]:
     return off
 
 
-def flatten(per_request_rows: Sequence[np.ndarray]) -> np.ndarray:
+def flatten(per_request_rows: Sequence[np.ndarray], dtype=np.float64) -> np.ndarray:
     """Selective batching's stacking: [(L_i, H)] -> (sum L_i, H), no batch dim."""
-    return np.concatenate([np.asarray(r, np.float64) for r in per_request_rows], axis=0)
+    return np.concatenate([np.asarray(r, dtype) for r in per_request_rows], axis=0)
 
 
 def attention_one(q: np.ndarray, k: np.ndarray, v: np.ndarray, pos: np.ndarray, n_heads: int) -> np.ndarray:
@@ -146,18 +146,24 @@ def attention_one(q: np.ndarray, k: np.ndarray, v: np.ndarray, pos: np.ndarray, 
     n, H = q.shape
     d = H // n_heads
     T = k.shape[0]
-    out = np.zeros((n, H))
+    out = np.zeros((n, H), q.dtype)
     allowed = np.arange(T)[None, :] <= pos[:, None]
     for j in range(n_heads):
         sl = slice(j * d, (j + 1) * d)
-        s = (q[:, sl] @ k[:, sl].T) / math.sqrt(d)
+        s = (q[:, sl] @ k[:, sl].T) / q.dtype.type(math.sqrt(d))
         s = np.where(allowed, s, -np.inf)
         out[:, sl] = softmax(s) @ v[:, sl]
     return out
 
 
-def iteration(w: dict, n_heads: int, batch: Sequence[BatchItem], store: KVStore, hidden_only: bool = False) -> Result:
-    """One engine iteration over ``batch``; appends this iteration's K/V to ``store``."""
+def iteration(w: dict, n_heads: int, batch: Sequence[BatchItem], store: KVStore, hidden_only: bool = False,
+              dtype=np.float64) -> Result:
+    """One engine iteration over ``batch``; appends this iteration's K/V to ``store``.
+
+    ``dtype`` is the arithmetic type: float64 (the default, used for every
+    parity comparison) or float32, the precision the performance target names
+    for timing this oracle as a CPU baseline."""
+    f = lambda a: np.asarray(a, dtype)
     H = w["tok_emb"].shape[1]
     off = offsets(batch)
     tok = np.array([t for it in batch for t in it.tokens], dtype=np.int64)
@@ -165,10 +171,10 @@ def iteration(w: dict, n_heads: int, batch: Sequence[BatchItem], store: KVStore,
     for it in batch:
         if store.length(it.rid) != it.ctx:
             raise ValueError(f"request {it.rid}: phase/context mismatch ({store.length(it.rid)} cached, ctx {it.ctx})")
-    x = np.asarray(w["tok_emb"], np.float64)[tok] + np.asarray(w["pos_emb"], np.float64)[pos]
+    x = f(w["tok_emb"])[tok] + f(w["pos_emb"])[pos]
     for l, L in enumerate(w["layers"]):
-        h = layer_norm(x, L["ln1_g"], L["ln1_b"])
-        qkv = h @ np.asarray(L["w_qkv"], np.float64).T + np.asarray(L["b_qkv"], np.float64)
+        h = layer_norm(x, L["ln1_g"], L["ln1_b"], dtype=dtype)
+        qkv = h @ f(L["w_qkv"]).T + f(L["b_qkv"])
         q, k, v = qkv[:, :H], qkv[:, H:2 * H], qkv[:, 2 * H:]
         a = np.zeros_like(q)
         for i, it in enumerate(batch):  # split ...
@@ -176,13 +182,13 @@ def iteration(w: dict, n_heads: int, batch: Sequence[BatchItem], store: KVStore,
             store.write(it.rid, l, it.ctx, k[rows], v[rows])
             a[rows] = attention_one(q[rows], store.k[(it.rid, l)], store.v[(it.rid, l)], pos[rows], n_heads)
         # ... merge: a is again one [sum L, H] matrix
-        x = x + a @ np.asarray(L["w_o"], np.float64).T + np.asarray(L["b_o"], np.float64)
-        h2 = layer_norm(x, L["ln2_g"], L["ln2_b"])
-        f = gelu(h2 @ np.asarray(L["w_1"], np.float64).T + np.asarray(L["b_1"], np.float64))
-        x = x + f @ np.asarray(L["w_2"], np.float64).T + np.asarray(L["b_2"], np.float64)
+        x = x + a @ f(L["w_o"]).T + f(L["b_o"])
+        h2 = layer_norm(x, L["ln2_g"], L["ln2_b"], dtype=dtype)
+        g1 = gelu(h2 @ f(L["w_1"]).T + f(L["b_1"]))
+        x = x + g1 @ f(L["w_2"]).T + f(L["b_2"])
     last = [off[i + 1] - 1 for i in range(len(batch))]
-    y = layer_norm(x[last], w["lnf_g"], w["lnf_b"])
+    y = layer_norm(x[last], w["lnf_g"], w["lnf_b"], dtype=dtype)
     if hidden_only:
         return Result(y, np.zeros((len(batch), 0)), [])
-    logits = y @ np.asarray(w["tok_emb"], np.float64).T
+    logits = y @ f(w["tok_emb"]).T
     return Result(y, logits, [argmax_lowest(r) for r in logits])

@@ -16,7 +16,7 @@ from iteration_level_scheduling_gb300 import synth
 from oracle import model as omodel
 from oracle import sched as osched
 from oracle.model import BatchItem, KVStore
-from gpu_util import kv_pool_tensor, load_context, make_engine, normwise
+from gpu_util import MIN_AGREE, disagreements, kv_pool_tensor, load_context, make_engine, normwise
 
 pytestmark = pytest.mark.gpu
 
@@ -30,6 +30,13 @@ def built():
     build.build()
 
 
+def f64_weights(w):
+    f = lambda a: np.asarray(a, np.float64)
+    out = {k: f(v) for k, v in w.items() if k != "layers"}
+    out["layers"] = [{k: f(v) for k, v in L.items()} for L in w["layers"]]
+    return out
+
+
 def run_trace_teacher_forced(cfg, w, specs, max_batch, mode, kv_slots, max_tokens=4096, feedback=False,
                              chunked=False, cancel_at=None, n_workers=1):
     from iteration_level_scheduling_gb300 import native
@@ -39,8 +46,10 @@ def run_trace_teacher_forced(cfg, w, specs, max_batch, mode, kv_slots, max_token
     for sp in specs:
         s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len, sp.ctx0)
     store = KVStore(cfg.n_layers, cfg.hidden)
+    w64 = f64_weights(w)  # converted once, not on every oracle call
     worst_h = worst_l = 0.0
     agree = total = iters = chunks = 0
+    mismatches = []
     prev_next = {}
     queue = []  # selected batches not yet run, oldest first (n_workers of them at most)
     while True:
@@ -70,13 +79,14 @@ def run_trace_teacher_forced(cfg, w, specs, max_batch, mode, kv_slots, max_token
             items.append(BatchItem(rid, tk, c))
             p += n
         got = eng.run_iteration(b)
-        ref = omodel.iteration(w, cfg.n_heads, items, store)
+        ref = omodel.iteration(w64, cfg.n_heads, items, store)
         hid = eng.last_hidden(b.n_req)
         lg = eng.last_logits(b.n_req)
         worst_h = max(worst_h, normwise(hid, ref.hidden))
         worst_l = max(worst_l, normwise(lg, ref.logits))
         assert got.tolist() == lg.argmax(1).tolist()  # argmax kernel == argmax of its own logits
         agree += sum(int(a == r) for a, r in zip(got.tolist(), ref.next_tokens))
+        mismatches += [dict(m, iteration=iters) for m in disagreements(got, lg, ref.logits, ref.next_tokens)]
         total += b.n_req
         iters += 1
         prev_next = dict(enumerate(ref.next_tokens))
@@ -86,7 +96,8 @@ def run_trace_teacher_forced(cfg, w, specs, max_batch, mode, kv_slots, max_token
     s.close()
     eng.close()
     return dict(iters=iters, worst_h=worst_h, worst_l=worst_l, agree=agree / max(total, 1), total=total,
-                generated=st.generated, launches=eng_stats.launches, chunks=chunks, cancelled=st.cancelled)
+                generated=st.generated, launches=eng_stats.launches, chunks=chunks, cancelled=st.cancelled,
+                mismatches=mismatches)
 
 
 @pytest.mark.parametrize("mode,expect_iters", [(0, 50), (1, 90)])
@@ -101,7 +112,7 @@ def test_tiny_fp32_trace(mode, expect_iters, affine):
     assert r["iters"] == expect_iters
     assert r["generated"] == 155
     assert r["worst_h"] <= TOL_FP32 and r["worst_l"] <= TOL_FP32, r
-    assert r["agree"] >= 0.99, r
+    assert r["agree"] >= MIN_AGREE, r
 
 
 def test_tiny_fp32_trace_token_feedback():
@@ -121,7 +132,7 @@ def test_tiny_fp32_pipelined_two_workers():
     r = run_trace_teacher_forced(cfg, w, synth.tiny_requests(3), 4, 0, kv_slots=4 * 128, n_workers=2)
     assert r["generated"] == 155
     assert r["worst_h"] <= TOL_FP32 and r["worst_l"] <= TOL_FP32, r
-    assert r["agree"] >= 0.99, r
+    assert r["agree"] >= MIN_AGREE, r
 
 
 def test_serve_loop_tokens_independent_of_batching():
@@ -157,7 +168,7 @@ def test_tiny_fp32_chunked_prefill_and_cancellation():
                                  cancel_at={3: [1], 9: [4, 6]})
     assert r["chunks"] >= 3 and r["cancelled"] == 3
     assert r["worst_h"] <= TOL_FP32 and r["worst_l"] <= TOL_FP32, r
-    assert r["agree"] >= 0.99, r
+    assert r["agree"] >= MIN_AGREE, r
 
 
 def test_gpt2_medium_chunked_prompt():
@@ -173,6 +184,22 @@ def test_gpt2_medium_chunked_prompt():
     r = run_trace_teacher_forced(cfg, w, specs, 8, 0, kv_slots=8 * 512, max_tokens=128, chunked=True)
     assert r["chunks"] >= 2
     assert r["worst_h"] <= TOL_BF16 and r["worst_l"] <= TOL_BF16, r
+    assert r["agree"] >= MIN_AGREE, r
+
+
+@pytest.mark.parametrize("width", ["gpt2-medium", "gpt3-13b"])
+def test_bf16_teacher_forced_trace(width):
+    """A bf16 continuous-batching trace at full width and two layers, teacher
+    forced: 24 requests (Poisson arrivals, prompts U[8,64], outputs U[8,24]),
+    max_batch 8, so that more than 300 greedy tokens are compared with the
+    oracle's; every iteration within 2e-2 and >= 99 % of the tokens equal."""
+    cfg = synth.CONFIGS[width].with_layers(2)
+    w = synth.make_weights(cfg, 6, random_affine=True)
+    specs = synth.poisson_trace(6, n=24, rate=0.5, prompt_range=(8, 64), out_range=(8, 24), vocab=cfg.vocab)
+    r = run_trace_teacher_forced(cfg, w, specs, 8, 0, kv_slots=8 * 96, max_tokens=512)
+    assert r["total"] >= 300, r
+    assert r["worst_h"] <= TOL_BF16 and r["worst_l"] <= TOL_BF16, r
+    assert r["agree"] >= MIN_AGREE, r
 
 
 def run_one_batch(cfg, w, reqs, sample, seed_kv=0, max_tokens=None, pack_weights=True):
@@ -203,7 +230,8 @@ def run_one_batch(cfg, w, reqs, sample, seed_kv=0, max_tokens=None, pack_weights
     items = [BatchItem(reqs[i].rid, reqs[i].prompt, reqs[i].ctx0) for i in idx]
     ref = omodel.iteration(w, cfg.n_heads, items, store)
     res = dict(h=normwise(hid[idx], ref.hidden), l=normwise(lg[idx], ref.logits),
-               agree=np.mean([got[i] == t for i, t in zip(idx, ref.next_tokens)]), n=len(idx))
+               agree=np.mean([got[i] == t for i, t in zip(idx, ref.next_tokens)]), n=len(idx),
+               mismatches=disagreements(got[idx], lg[idx], ref.logits, ref.next_tokens))
     eng.close()
     return res
 
@@ -216,11 +244,10 @@ def test_gpt2_medium_mixed_batch(pack_weights):
     w = synth.make_weights(cfg, 0, random_affine=True)
     reqs = synth.mixed_batch(0)
     assert sum(len(r.prompt) for r in reqs) == 448 + 29
-    longest = sorted((r for r in reqs if r.ctx0), key=lambda r: -r.ctx0)[:4]
-    shortest = sorted((r for r in reqs if r.ctx0), key=lambda r: r.ctx0)[:2]
-    sample = {0, 1, 2} | {r.rid for r in longest + shortest}
-    res = run_one_batch(cfg, w, reqs, sample, pack_weights=pack_weights)
+    res = run_one_batch(cfg, w, reqs, {r.rid for r in reqs}, pack_weights=pack_weights)
+    assert res["n"] == 32
     assert res["h"] <= TOL_BF16 and res["l"] <= TOL_BF16, res
+    assert res["agree"] >= MIN_AGREE, res
 
 
 def test_gpt3_13b_width_two_layers():
@@ -230,9 +257,10 @@ def test_gpt3_13b_width_two_layers():
     cfg = synth.GPT3_13B.with_layers(2)
     w = synth.make_weights(cfg, 0, random_affine=True)
     reqs = synth.mixed_batch(3, prompt_lens=(100, 37), n_incr=62, ctx_range=(32, 1000))
-    sample = {0, 1, 2, 3, 60, 63}
-    res = run_one_batch(cfg, w, reqs, sample)
+    res = run_one_batch(cfg, w, reqs, {r.rid for r in reqs})
+    assert res["n"] == 64
     assert res["h"] <= TOL_BF16 and res["l"] <= TOL_BF16, res
+    assert res["agree"] >= MIN_AGREE, res
 
 
 @pytest.mark.parametrize("case", ["single_token", "one_long_prompt", "chunk_edges"])
@@ -247,6 +275,7 @@ def test_edge_batches(case):
         reqs = [synth.RequestSpec(i, 0.0, [i + 1], 1, c) for i, c in enumerate([1, 63, 64, 255, 256, 257, 511, 1000])]
     res = run_one_batch(cfg, w, reqs, {r.rid for r in reqs})
     assert res["h"] <= TOL_BF16 and res["l"] <= TOL_BF16, res
+    assert res["agree"] >= MIN_AGREE, res
 
 
 def test_invalid_descriptors_rejected():

@@ -212,8 +212,8 @@ def test_pins_catch_planted_mistakes(mutation, monkeypatch):
     elif mutation == "tanh_gelu":
         monkeypatch.setattr(model, "gelu", lambda x: 0.5 * x * (1 + np.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3))))
     elif mutation == "unbiased_var":
-        def ln(x, g, b, eps=1e-5):
-            x = np.asarray(x, np.float64)
+        def ln(x, g, b, eps=1e-5, dtype=np.float64):
+            x = np.asarray(x, dtype)
             m = x.mean(-1, keepdims=True)
             return (x - m) / np.sqrt(x.var(-1, ddof=1, keepdims=True) + eps) * g + b
         monkeypatch.setattr(model, "layer_norm", ln)
@@ -241,3 +241,17 @@ def test_chunked_prompt_equals_whole_prompt():
         np.testing.assert_allclose(res.hidden, whole.hidden, rtol=1e-10, atol=1e-10)
         np.testing.assert_allclose(res.logits, whole.logits, rtol=1e-10, atol=1e-10)
         assert res.next_tokens == whole.next_tokens
+
+
+def test_float32_oracle_matches_float64():
+    """The float32 form of the oracle (used only to time the CPU baseline in the
+    precision the target names) computes the same iteration: within float32
+    rounding of the float64 result, and the same greedy tokens."""
+    w = tiny_weights(9)
+    batch = [BatchItem(0, [5, 17, 300, 2], 0), BatchItem(1, [9, 511], 0)]
+    r64 = model.iteration(w, TINY.n_heads, batch, KVStore(TINY.n_layers, TINY.hidden))
+    r32 = model.iteration(w, TINY.n_heads, batch, KVStore(TINY.n_layers, TINY.hidden, np.float32), dtype=np.float32)
+    assert r32.logits.dtype == np.float32 and r32.hidden.dtype == np.float32
+    np.testing.assert_allclose(r32.hidden, r64.hidden, rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(r32.logits, r64.logits, rtol=1e-4, atol=1e-4)
+    assert r32.next_tokens == r64.next_tokens

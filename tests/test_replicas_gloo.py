@@ -53,20 +53,16 @@ def test_reduce_replicas_single():
 
 def test_iteration_work_counts():
     """Per-iteration roofline inputs: FLOPs and weight + K/V bytes of one batch."""
-    import ctypes as C
-    import numpy as np
     import bench
-    from iteration_level_scheduling_gb300 import build, synth
-    build.build()
-    from iteration_level_scheduling_gb300 import native
+    from iteration_level_scheduling_gb300 import synth
     cfg = synth.GPT3_13B
-    b = native.BatchDesc([1, 2], [0, 1], [3, 1], [0, 10], [0, 100], [5, 6, 7, 8])
-    w = bench.iteration_work(b.c, cfg)
+    w = bench.iteration_work([3, 1], [0, 10], cfg)
     H, F, V, L = cfg.hidden, cfg.ffn, cfg.vocab, cfg.n_layers
     assert w["R"] == 4 and w["B"] == 2
     pairs = 3 * 0 + 3 * 4 // 2 + 11  # prefill rows see 1, 2, 3 keys; the decode row sees 11
     assert w["flops"] == 2.0 * 4 * L * (4 * H * H + 2 * H * F) + 2.0 * 2 * H * V + 4.0 * H * pairs * L
     assert w["kv_bytes"] == (3 + 11) * L * 2 * H * 2
+    assert w["bytes"] == 2.0 * (L * (4 * H * H + 2 * H * F) + V * H) + 2.0 * 4 * H + w["kv_bytes"]
 
 
 def test_split_by_prefill():
@@ -80,9 +76,57 @@ def test_split_by_prefill():
     assert "with_prefill" not in bench.split_by_prefill(work[:1], [8.0], [0.8])
 
 
-def test_profiled_traffic_ratio_present():
-    """bench.py reads roofline.traffic's DRAM/algorithmic ratio from the committed
-    decode-GEMM ncu summary; the line must be there and near 1 (no re-reads)."""
+def test_gemm_roofline_weights_launches_per_iteration():
+    """The linear-layer family's achieved bandwidth weights each sampled-layer
+    launch by the model depth and the LM head by one: bytes per iteration over
+    GEMM time per iteration, checked against a hand-weighted sum."""
     import bench
-    r = bench.profiled_traffic_ratio()
-    assert r is not None and 0.9 < r < 1.1
+    peaks = dict(hbm=6788.3, tc_sus=1731.7)
+    L = 40
+    recs = []
+    for _ in range(2):  # two iterations, one sampled layer each
+        recs += [dict(kind="gemm_qkv", layer=3, ms=0.039, bytes=160e6, flops=1e10),
+                 dict(kind="gemm_o", layer=3, ms=0.018, bytes=55e6, flops=3e9),
+                 dict(kind="gemm_ffn1", layer=3, ms=0.050, bytes=213e6, flops=1.3e10),
+                 dict(kind="gemm_ffn2", layer=3, ms=0.043, bytes=215e6, flops=1.3e10),
+                 dict(kind="lm_head", layer=-1, ms=0.093, bytes=530e6, flops=3e10),
+                 dict(kind="layernorm", layer=3, ms=0.009, bytes=2e6, flops=0.0)]
+    tot, kinds = bench.gemm_roofline(recs, L, peaks)
+    byts = 2 * (L * (160e6 + 55e6 + 213e6 + 215e6) + 530e6)
+    ms = 2 * (L * (0.039 + 0.018 + 0.050 + 0.043) + 0.093)
+    assert abs(tot["bytes"] - byts) < 1 and abs(tot["ms"] - ms) < 1e-9
+    assert tot["launches"] == 2 * (4 * L + 1)
+    frac = byts / (ms / 1000) / 1e9 / peaks["hbm"]
+    # the unweighted pooling would give the LM head the weight of one projection
+    pooled = 2 * (160e6 + 55e6 + 213e6 + 215e6 + 530e6) / (2 * (0.039 + 0.018 + 0.050 + 0.043 + 0.093) / 1000) / 1e9
+    assert abs(tot["bytes"] / (tot["ms"] / 1000) / 1e9 / peaks["hbm"] - frac) < 1e-12
+    assert pooled / peaks["hbm"] > frac
+    assert kinds["lm_head"]["launches_per_iteration"] == 1 and kinds["gemm_qkv"]["launches_per_iteration"] == L
+    assert "layernorm" not in kinds
+
+
+def test_traffic_record_follows_the_kernel_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from a recorded ncu capture only while the GEMM
+    source is the one that was captured."""
+    import json
+    import bench
+    src = ["iteration_level_scheduling_gb300/csrc/k_gemm_tc.cu"]
+    f = tmp_path / "t.json"
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.traffic_record("gemm_decode")[0] is None
+    f.write_text(json.dumps({"gemm_decode": {"sources": src, "source_sha": bench.source_sha(src),
+                                             "dram_over_algorithmic": 1.002, "workload": "w"}}))
+    rec, why = bench.traffic_record("gemm_decode")
+    assert rec["dram_over_algorithmic"] == 1.002 and why is None
+    f.write_text(json.dumps({"gemm_decode": {"sources": src, "source_sha": "0" * 16,
+                                             "dram_over_algorithmic": 1.002, "workload": "w"}}))
+    rec, why = bench.traffic_record("gemm_decode")
+    assert rec is None and "changed" in why
+
+
+def test_trace_phases():
+    """Ramp = before the batch first fills, drain = after it is last full."""
+    import bench
+    B = bench.MAX_BATCH
+    work = [dict(B=b) for b in [1, 5, B, B, 30, B, 12, 3]]
+    assert bench.phases(work) == {"ramp": [0, 1], "steady": [2, 3, 4, 5], "drain": [6, 7]}

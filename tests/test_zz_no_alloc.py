@@ -5,8 +5,9 @@ given all device memory to its own allocator, or their serving thread may not
 call cudaMalloc) cannot create an engine; orca_attention_decode_noalloc runs
 the engine's split-K decode kernel with its scratch in a fixed device array
 inside the library.  Its output must match the engine entry point
-orca_op_attention on the same inputs, call after call (the array is shared and
-keeps the previous call's contents).  This file is collected last on purpose.
+orca_op_attention on the same inputs and the oracle's single-query attention,
+call after call (the array is shared and keeps the previous call's contents).
+This file is collected last on purpose.
 """
 
 import numpy as np
@@ -47,6 +48,21 @@ def rel(a, ref):
     return float(np.max(np.abs(a - ref)) / np.max(np.abs(ref)))
 
 
+def oracle_decode(qkv, pool, ctx, offs, n_heads, d):
+    """The oracle's attention for one query row per request: request i's row sits
+    at position ctx[i] and sees its keys 0 .. ctx[i] (slots offs[i] ..)."""
+    from oracle.model import attention_one
+    H = n_heads * d
+    q = qkv.float().cpu().numpy().astype(np.float64)[:, :H]
+    out = np.zeros((len(ctx), H))
+    for i, (c, o) in enumerate(zip(ctx, offs)):
+        kv = pool[:, :, o:o + c + 1, :].float().cpu().numpy().astype(np.float64)  # [K|V][head][key][d]
+        k = kv[0].transpose(1, 0, 2).reshape(c + 1, H)
+        v = kv[1].transpose(1, 0, 2).reshape(c + 1, H)
+        out[i] = attention_one(q[i:i + 1], k, v, np.array([c]), n_heads)[0]
+    return out
+
+
 @pytest.mark.parametrize("dtype,d,n_heads,tol", [("bf16", 128, 40, 1e-2), ("fp32", 64, 8, 1e-5)])
 def test_noalloc_matches_engine_entry_point(native, dtype, d, n_heads, tol):
     dt = native.DTYPE_BF16 if dtype == "bf16" else native.DTYPE_FP32
@@ -66,6 +82,9 @@ def test_noalloc_matches_engine_entry_point(native, dtype, d, n_heads, tol):
             torch.cuda.synchronize()
             assert torch.isfinite(got.float()).all()
             assert rel(got, ref) <= tol
+            exact = oracle_decode(qkv, pool, ctx, offs, n_heads, d)
+            g64 = got.float().cpu().numpy().astype(np.float64)
+            assert float(np.max(np.abs(g64 - exact)) / np.max(np.abs(exact))) <= tol
     finally:
         eng.close()
 
@@ -75,6 +94,9 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(native):
     with pytest.raises(native.OrcaError) as e:
         native.attention_decode_noalloc(native.DTYPE_BF16, 16, 16, 10 ** 6, n_heads, d, [5] * 257, [0] * 257, 16)
     assert e.value.code == native.ERR_LIMIT
-    with pytest.raises(native.OrcaError) as e:  # too many split-K partials: 256 requests x 64 chunks x 128 heads
+    with pytest.raises(native.OrcaError) as e:  # too many work items for the plan tables: 256 x 63 chunks
         native.attention_decode_noalloc(native.DTYPE_BF16, 16, 16, 40000, 128, 128, [32000] * 256, [0] * 256, 16)
+    assert e.value.code == native.ERR_LIMIT
+    with pytest.raises(native.OrcaError) as e:  # tables fit (1024 work items) but the partials do not (17 Mi floats)
+        native.attention_decode_noalloc(native.DTYPE_BF16, 16, 16, 40000, 128, 128, [2000] * 256, [0] * 256, 16)
     assert e.value.code == native.ERR_LIMIT
