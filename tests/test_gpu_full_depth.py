@@ -11,7 +11,7 @@ import torch
 
 import bench
 from iteration_level_scheduling_gb300 import synth
-from gpu_util import MIN_AGREE, full_depth_check
+from gpu_util import assert_agreement, full_depth_check
 
 pytestmark = pytest.mark.gpu
 
@@ -59,7 +59,7 @@ def check(r):
     assert r["argmax_ok"]
     assert r["n"] >= 16
     assert r["h"] <= TOL_BF16 and r["l"] <= TOL_BF16, r
-    assert r["agree"] >= MIN_AGREE, r
+    assert_agreement(r["agree"], r["n"], r["mismatches"], wide=True)
 
 
 def test_gpt3_13b_bench_window_iteration():

@@ -16,7 +16,7 @@ from iteration_level_scheduling_gb300 import synth
 from oracle import model as omodel
 from oracle import sched as osched
 from oracle.model import BatchItem, KVStore
-from gpu_util import MIN_AGREE, disagreements, kv_pool_tensor, load_context, make_engine, normwise
+from gpu_util import MIN_AGREE, assert_agreement, disagreements, kv_pool_tensor, load_context, make_engine, normwise
 
 pytestmark = pytest.mark.gpu
 
@@ -197,9 +197,10 @@ def test_bf16_teacher_forced_trace(width):
     w = synth.make_weights(cfg, 6, random_affine=True)
     specs = synth.poisson_trace(6, n=24, rate=0.5, prompt_range=(8, 64), out_range=(8, 24), vocab=cfg.vocab)
     r = run_trace_teacher_forced(cfg, w, specs, 8, 0, kv_slots=8 * 96, max_tokens=512)
+    print(width, {k: r[k] for k in ("agree", "total", "worst_h", "worst_l", "mismatches")})
     assert r["total"] >= 300, r
     assert r["worst_h"] <= TOL_BF16 and r["worst_l"] <= TOL_BF16, r
-    assert r["agree"] >= MIN_AGREE, r
+    assert_agreement(r["agree"], r["total"], r["mismatches"], wide=cfg.hidden >= 4096)
 
 
 def run_one_batch(cfg, w, reqs, sample, seed_kv=0, max_tokens=None, pack_weights=True):
@@ -258,9 +259,10 @@ def test_gpt3_13b_width_two_layers():
     w = synth.make_weights(cfg, 0, random_affine=True)
     reqs = synth.mixed_batch(3, prompt_lens=(100, 37), n_incr=62, ctx_range=(32, 1000))
     res = run_one_batch(cfg, w, reqs, {r.rid for r in reqs})
+    print(res)
     assert res["n"] == 64
     assert res["h"] <= TOL_BF16 and res["l"] <= TOL_BF16, res
-    assert res["agree"] >= MIN_AGREE, res
+    assert_agreement(res["agree"], res["n"], res["mismatches"], wide=True)
 
 
 @pytest.mark.parametrize("case", ["single_token", "one_long_prompt", "chunk_edges"])

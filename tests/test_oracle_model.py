@@ -255,3 +255,39 @@ def test_float32_oracle_matches_float64():
     np.testing.assert_allclose(r32.hidden, r64.hidden, rtol=1e-4, atol=1e-4)
     np.testing.assert_allclose(r32.logits, r64.logits, rtol=1e-4, atol=1e-4)
     assert r32.next_tokens == r64.next_tokens
+
+
+def test_agreement_rule_rejects_clear_flips():
+    """The GPU tests' agreement rule: at GPT-3 widths a disagreement is accepted
+    only as a near-tie (oracle margin within a few RMS logit errors of the
+    row) and only up to the bf16 flip floor; a flip with a clear margin, or
+    too many flips, fails, and elsewhere 99 % is required."""
+    from gpu_util import assert_agreement, disagreements
+    rng = np.random.default_rng(0)
+    ref = rng.standard_normal((100, 5000))
+    noise = 1e-3 * rng.standard_normal((100, 5000))
+    gpu = ref + noise
+    top2 = np.argsort(ref, 1)[:, -2:]
+    near = int(np.argmin(ref[np.arange(100), top2[:, 1]] - ref[np.arange(100), top2[:, 0]]))
+    gpu[near, top2[near, 0]] = gpu[near, top2[near, 1]] + 1e-6  # a near-tie flip
+    got = gpu.argmax(1)
+    tokens = ref.argmax(1).tolist()
+    mm = disagreements(got, gpu, ref, tokens)
+    assert len(mm) == 1 and mm[0]["row"] == near
+    agree = 1 - len(mm) / 100
+    if mm[0]["ref_margin"] <= 6 * mm[0]["row_rms_err"]:
+        assert_agreement(agree, 100, mm, wide=True)
+    with pytest.raises(AssertionError):  # one flip in 50 tokens is 98 %
+        assert_agreement(1 - len(mm) / 50, 50, mm, wide=False)
+    clear = gpu.copy()
+    clear[3, int(np.argmin(ref[3]))] = ref[3].max() + 1.0  # the lowest logit pushed to the top: a bug
+    mm2 = disagreements(clear.argmax(1), clear, ref, tokens)
+    with pytest.raises(AssertionError):
+        assert_agreement(1 - len(mm2) / 100, 100, mm2, wide=True)
+    many = gpu.copy()  # five near-tie flips in 100 tokens: above the 3 % floor
+    for r in np.argsort(ref[np.arange(100), top2[:, 1]] - ref[np.arange(100), top2[:, 0]])[:5]:
+        many[r, top2[r, 0]] = many[r, top2[r, 1]] + 1e-6
+    mm3 = disagreements(many.argmax(1), many, ref, tokens)
+    assert len(mm3) == 5
+    with pytest.raises(AssertionError):
+        assert_agreement(0.95, 100, mm3, wide=True)
