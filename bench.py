@@ -91,6 +91,10 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-full-trace", action="store_true")
+    p.add_argument("--no-request-level", action="store_true",
+                   help="skip the padded request-level baseline on the same GPU")
+    p.add_argument("--no-window", action="store_true",
+                   help="skip the headline window, its serve loop and the whole trace (measure --configs only)")
     p.add_argument("--configs", default="tiny-fp32,gpt2-medium-mixed,gpt3-6.7b-decode,gpt3-13b-prefill-heavy",
                    help="comma-separated list of the other workloads to measure ('' for none)")
     p.add_argument("--prefill-heavy-iters", type=int, default=50)
@@ -660,6 +664,89 @@ def run_full_trace(args, eng, trace, cfg, peaks):
 
 
 # --------------------------------------------------------------------------- #
+# the conventional baseline on the same GPU: request-level, padded + masked
+# --------------------------------------------------------------------------- #
+def run_request_level_padded(args, ptrs, cfg, peaks, trace):
+    """The baseline the pages compare Orca with, on the same engine, model and
+    trace: request-level batches ([0h-n0] "Request-Level vs Iteration-Level
+    Scheduling": a batch forms only when the previous one has finished and runs
+    until its longest member is done) executed as conventional padded + masked
+    batches ([houmin] 3.1.2 "问题"): prompts padded to the longest of the batch,
+    finished members kept in the batch as pad rows, increments attending over
+    the batch's longest context with the rest masked (orca_plan_build_padded).
+    Device-resident plans over `--steps` iterations from `--window-start` of its
+    own schedule; tokens/s counts the real requests' tokens only."""
+    import torch
+
+    from iteration_level_scheduling_gb300 import native
+    eng = make_engine(cfg, ptrs, MAX_BATCH * 512, MAX_BATCH, MAX_BATCH * KV_RESERVE)  # 64 prompts padded to <= 512
+    fill_kv_pool(eng, 0)
+    s = native.Scheduler(MAX_BATCH, MAX_TOKENS, kv_reserve=KV_RESERVE, mode=1, engine=eng)
+    for sp in trace:
+        s.submit(sp.rid, sp.arrival, sp.prompt, sp.out_len)
+    members, ctx, kv = [], {}, {}
+    plans, work, real_tokens, rows = [], [], [], []
+    n_it, done = args.warmup + args.steps, 0
+    while len(plans) < n_it:
+        st, b = s.next_raw()
+        if st == 2:
+            break
+        if st != 1:
+            continue
+        B = b.n_req
+        ids = np.ctypeslib.as_array(b.request_id, (B,)).tolist()
+        n = np.ctypeslib.as_array(b.n_input, (B,)).tolist()
+        c = np.ctypeslib.as_array(b.ctx_len, (B,)).tolist()
+        ph = np.ctypeslib.as_array(b.phase, (B,)).tolist()
+        if all(p == 0 for p in ph):  # a new batch
+            members = ids
+        for r, o in zip(ids, np.ctypeslib.as_array(b.kv_offset, (B,)).tolist()):
+            kv[r] = o
+        real = {r: i for i, r in enumerate(ids)}
+        if done >= args.window_start:
+            toks = np.ctypeslib.as_array(b.tokens, (sum(n),)).tolist()
+            off = np.concatenate([[0], np.cumsum(n)]).tolist()
+            d = dict(rid=[], ph=[], n=[], c=[], kv=[], tok=[])
+            for r in members:
+                i = real.get(r)
+                ghost = i is None  # finished: a pad row after its own context
+                d["rid"].append(r), d["ph"].append(1 if ghost else ph[i]), d["n"].append(1 if ghost else n[i])
+                d["c"].append(ctx[r] if ghost else c[i]), d["kv"].append(kv[r])
+                d["tok"].extend([0] if ghost else [t if t >= 0 else 0 for t in toks[off[i]:off[i + 1]]])
+            desc = native.BatchDesc(d["rid"], d["ph"], d["n"], d["c"], d["kv"], d["tok"])
+            buf = np.zeros(eng.plan_words(desc, padded=True), np.int32)
+            eng.plan_build(desc, buf, padded=True)
+            plans.append(buf)
+            work.append(iteration_work(n, c, cfg))
+            real_tokens.append(B)
+            rows.append((max(d["n"]) * len(d["rid"]), sum(n)))
+        for r in members:
+            i = real.get(r)
+            ctx[r] = (ctx[r] + 1) if i is None else c[i] + n[i]
+        s.complete(np.zeros(B, np.int32))
+        done += 1
+    s.close()
+    if len(plans) < n_it:
+        raise RuntimeError("trace too short for the request-level window")
+    dp = DevicePlans(plans)
+    timed_run(eng, dp, 0, args.warmup)
+    it_ms, launches = timed_run(eng, dp, args.warmup, args.steps)
+    eng.close()
+    del dp
+    torch.cuda.synchronize()
+    tot = sum(it_ms)
+    tokens = sum(real_tokens[args.warmup:])
+    padded = sum(r[0] for r in rows[args.warmup:])
+    useful = sum(r[1] for r in rows[args.warmup:])
+    return {"value": tokens / (tot / 1000), "unit": "tokens/s", "ms_per_iteration": tot / args.steps,
+            "iterations_timed": args.steps, "window_start_iteration": args.window_start,
+            "mean_real_batch": float(np.mean(real_tokens[args.warmup:])),
+            "rows_computed_over_real_rows": padded / useful, "gpu_launches": launches,
+            "scheduler": "request-level (a batch forms when the previous one has finished), padded + masked "
+                         "batches (orca_plan_build_padded)"}
+
+
+# --------------------------------------------------------------------------- #
 # the other workloads
 # --------------------------------------------------------------------------- #
 def cfg_block(work, it_ms, peaks, launches, extra=None):
@@ -762,6 +849,8 @@ def run_gpt2_mixed(args, peaks, do_cpu):
     w = iteration_work(b.n_input, b.ctx_len, cfg)
     out = cfg_block([w] * K, it_ms, peaks, launches, {"workload": CFG_WORKLOADS["gpt2-medium-mixed"],
                                                      "rows": int(rows), "requests": len(reqs)})
+    out["kernels"] = kernel_breakdown(per_kernel_pass(eng, dp, W, min(K, cfg.n_layers)), cfg.n_layers,
+                                      min(K, cfg.n_layers))
     release_gpu(eng)
     del dp, keep
     release_gpu()
@@ -793,6 +882,10 @@ def run_gpt3_decode(args, peaks, do_cpu):
     it_ms, launches = timed_run(eng, dp, W, K)
     work = [iteration_work(n, c, cfg) for n, c in shapes[W:]]
     out = cfg_block(work, it_ms, peaks, launches, {"workload": CFG_WORKLOADS["gpt3-6.7b-decode"]})
+    try:  # (a replayed plan must follow one of the same batch size)
+        out["kernels"] = kernel_breakdown(per_kernel_pass(eng, dp, W, cfg.n_layers), cfg.n_layers, cfg.n_layers)
+    except native.OrcaError as e:
+        out["kernels"] = {"unavailable": str(e)}
     release_gpu(eng)
     del dp, keep
     release_gpu()
@@ -804,9 +897,10 @@ def run_gpt3_decode(args, peaks, do_cpu):
     return out
 
 
-def run_gpt3_prefill_heavy(args, peaks, do_cpu, keep13, ptrs13):
+def run_gpt3_prefill_heavy(args, peaks, do_cpu, cfg, ptrs13):
+    """`cfg` is the 13B shape at the depth of the weights `ptrs13` (40 layers
+    unless --layers says otherwise, e.g. for a small profiler capture)."""
     from iteration_level_scheduling_gb300 import native
-    cfg = MODEL
     n_it = max(1, args.prefill_heavy_iters)
     W = 3
     draws = [synth.prefill_heavy_batch(seed=i % n_it, vocab=cfg.vocab) for i in range(n_it)]
@@ -833,9 +927,10 @@ def run_gpt3_prefill_heavy(args, peaks, do_cpu, keep13, ptrs13):
     timed_run(eng, dp, 0, W)
     it_ms, launches = timed_run(eng, dp, W, n_it)
     out = cfg_block(work, it_ms, peaks, launches, {"workload": CFG_WORKLOADS["gpt3-13b-prefill-heavy"],
-                                                  "mean_rows": float(np.mean(rows))})
+                                                  "mean_rows": float(np.mean(rows)), "layers": cfg.n_layers})
     # the linear layers of one iteration, event-timed per launch (tensor-pipe bound)
     recs = per_kernel_pass(eng, dp, W, min(n_it, 3))
+    out["kernels"] = kernel_breakdown(recs, cfg.n_layers, min(n_it, 3))
     tot, kinds = gemm_roofline(recs, cfg.n_layers, peaks)
     if tot["ms"]:
         ach = tot["flops"] / (tot["ms"] / 1000) / 1e12
@@ -845,7 +940,7 @@ def run_gpt3_prefill_heavy(args, peaks, do_cpu, keep13, ptrs13):
     del dp
     release_gpu()
     if do_cpu:
-        runner = OracleRunner(cfg, 0, np.float32)
+        runner = OracleRunner(MODEL, 0, np.float32)
         d = draws[0]
         batch = ([r.rid for r in d], [len(r.prompt) for r in d], [r.ctx0 for r in d], [t for r in d for t in r.prompt])
         out["cpu_baseline"] = cpu_line(runner, [batch], "the first iteration (16 prompts + 128 increments)")
@@ -855,18 +950,10 @@ def run_gpt3_prefill_heavy(args, peaks, do_cpu, keep13, ptrs13):
 # --------------------------------------------------------------------------- #
 # our arm
 # --------------------------------------------------------------------------- #
-def run_orca(args, rank, world, local_rank):
-    import torch
+def run_headline(args, eng, trace, cfg, peaks, world, local_rank):
+    """The headline window (device-resident and through the serve loop) and the
+    linear-layer roofline; returns the JSON line without the extra blocks."""
     import torch.distributed as dist
-
-    torch.cuda.set_device(local_rank)
-    cfg = MODEL.with_layers(args.layers)
-    peaks = load_peaks()
-    solo = world == 1
-    keep, ptrs = gpu_weights(cfg, seed=rank)
-    eng = make_engine(cfg, ptrs, MAX_TOKENS, MAX_BATCH, MAX_BATCH * KV_RESERVE)
-    fill_kv_pool(eng, rank)
-    trace = make_trace(rank)
 
     # ---------------- the headline window, device-resident ------------------
     s = window_scheduler(eng, trace, args.window_start)
@@ -930,7 +1017,7 @@ def run_orca(args, rank, world, local_rank):
         e2e = {"value": e2e_tokens / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": 1000 * dt / args.steps, "api": "orca_sched_run (scheduler + orca_run_iteration)"}
 
-    line = {
+    return {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -945,24 +1032,44 @@ def run_orca(args, rank, world, local_rank):
         "clocks": clk, "e2e": e2e,
     }
 
-    # ---------------- the whole trace (ramp, steady state, drain) ----------
-    if solo and not args.no_full_trace and cfg.n_layers == MODEL.n_layers:
-        line["full_trace"] = run_full_trace(args, eng, trace, cfg, peaks)
-    eng.close()
 
-    # ---------------- the CPU oracle on a bounded sample (rank 0, N=1) ------
-    if solo and not args.no_cpu:
-        runner = OracleRunner(MODEL, 0, np.float32)
-        line["cpu_baseline"] = cpu_line(runner, oracle_window_batches(args.window_start + args.warmup, 3),
-                                        "2 window iterations")
+def run_orca(args, rank, world, local_rank):
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    cfg = MODEL.with_layers(args.layers)
+    peaks = load_peaks()
+    solo = world == 1
+    keep, ptrs = gpu_weights(cfg, seed=rank)
+    line = {"metric": METRIC, "unit": "tokens/s", "n_gpus": world, "dtype": "bf16", "data": "synthetic"}
+    if not args.no_window:
+        eng = make_engine(cfg, ptrs, MAX_TOKENS, MAX_BATCH, MAX_BATCH * KV_RESERVE)
+        fill_kv_pool(eng, rank)
+        trace = make_trace(rank)
+        line = run_headline(args, eng, trace, cfg, peaks, world, local_rank)
+        # ---------------- the whole trace (ramp, steady state, drain) ------
+        if solo and not args.no_full_trace and cfg.n_layers == MODEL.n_layers:
+            line["full_trace"] = run_full_trace(args, eng, trace, cfg, peaks)
+        eng.close()
+        release_gpu()
+        # ---------------- the request-level baseline, padded + masked -------
+        if solo and not args.no_request_level:
+            rl = run_request_level_padded(args, ptrs, cfg, peaks, trace)
+            rl["iteration_level_over_request_level"] = line["value"] / rl["value"]
+            line["request_level"] = rl
+        # ---------------- the CPU oracle on a bounded sample (rank 0, N=1) --
+        if solo and not args.no_cpu:
+            runner = OracleRunner(MODEL, 0, np.float32)
+            line["cpu_baseline"] = cpu_line(runner, oracle_window_batches(args.window_start + args.warmup, 3),
+                                            "2 window iterations")
 
     # ---------------- the other workloads ------------------------------------
     if solo and args.configs:
         cfgs = {}
         names = [c for c in args.configs.split(",") if c]
         do_cpu = not args.no_cpu
-        if "gpt3-13b-prefill-heavy" in names and cfg.n_layers == MODEL.n_layers:
-            cfgs["gpt3-13b-prefill-heavy"] = run_gpt3_prefill_heavy(args, peaks, do_cpu, keep, ptrs)
+        if "gpt3-13b-prefill-heavy" in names:
+            cfgs["gpt3-13b-prefill-heavy"] = run_gpt3_prefill_heavy(args, peaks, do_cpu, cfg, ptrs)
         del keep
         release_gpu()
         if "gpt3-6.7b-decode" in names:

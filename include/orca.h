@@ -177,6 +177,25 @@ int orca_plan_build(orca_engine *eng, const orca_batch *batch, int32_t *host_buf
 int orca_run_planned(orca_engine *eng, const int32_t *host_plan, const int32_t *dev_plan, int32_t *dev_out_next);
 int orca_engine_sync(orca_engine *eng);
 
+/* The same iteration as a conventional padded + masked batch ([houmin] 3.1.2
+ * "问题" and [arcsin2] 3.2: batching needs tensors of one shape, so requests
+ * of different lengths are padded and masked; [0h-n0] "Request-Level vs
+ * Iteration-Level Scheduling": the baseline Orca is compared with).  The
+ * descriptor is the same; the engine runs every request with Lq = max
+ * n_input rows -- its own rows, then pad rows of token 0 at the positions
+ * that follow, whose K/V land inside its reservation (ctx_len + Lq must fit
+ * it and max_pos) and are overwritten by its next real row -- and, when Lq =
+ * 1, every request's attention covers the batch's longest key range
+ * Lk = max(ctx_len) + 1, its keys past ctx_len[i] masked.  The next token of
+ * request i comes from its last real row, so the results equal those of the
+ * selective batch; only the work differs (Lq * n_req rows must fit
+ * max_tokens).  A request-level scheduler keeps finished members in their
+ * batch as single-row requests on token 0, whose tokens it ignores.
+ * Errors and synchrony as orca_run_iteration / orca_plan_build. */
+int orca_run_iteration_padded(orca_engine *eng, const orca_batch *batch, int32_t *out_next_tokens);
+int64_t orca_plan_words_padded(const orca_engine *eng, const orca_batch *batch);
+int orca_plan_build_padded(orca_engine *eng, const orca_batch *batch, int32_t *host_buf, int64_t cap_words);
+
 /* Parity/debug read-back of the last iteration: the final-LayerNorm output of
  * each request's last row (n_req x hidden floats) and the logits (n_req x vocab
  * floats), copied to HOST memory.  n = number of floats the buffer holds. */
@@ -214,6 +233,22 @@ typedef struct orca_kernel_time {
 #define ORCA_K_FINAL_LN 11
 int orca_engine_timing(orca_engine *eng, int32_t enable);
 int orca_engine_timing_read(orca_engine *eng, orca_kernel_time *out, int32_t cap, int32_t *n_out);
+
+/* Failure-detection test hook (the pages describe no such facility).  Launches,
+ * on the engine stream, a kernel whose one thread waits on a barrier that
+ * nothing completes, with the same bounded wait every pipelined kernel uses
+ * but a limit of limit_ns nanoseconds (1 ns .. 10 s).  The wait gives up,
+ * records an expired wait in the engine's device error word and the kernel
+ * returns; the next orca_engine_sync (or orca_run_iteration) reports
+ * ORCA_ERR_DEVICE_FLAG, clears the word and the engine stays usable.
+ * Asynchronous.  Errors: INVALID (limit out of range), CUDA. */
+int orca_debug_expire_wait(orca_engine *eng, int64_t limit_ns);
+
+/* Host-side fault injection: when the process environment holds
+ * ORCA_FAULT=kv_alloc:N at the creation of an engine or of a scheduler without
+ * an engine, the N-th K/V reservation of that object's pool fails as if the
+ * pool were full (ORCA_ERR_KV_FULL; a scheduler then stops admitting for that
+ * iteration, as the [0h-n0] scheduler algorithm does when K/V runs out). */
 
 /* ------------------------------------------------------------------------ */
 /* operator entry points (device pointers; used by the kernel parity tests)  */

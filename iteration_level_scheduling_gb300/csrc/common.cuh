@@ -134,12 +134,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete, for at most
 // kWaitLimitNs.  On expiry the error word gets ERR_WAIT_TIMEOUT and false is
 // returned; the caller then skips its remaining work.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, unsigned *err) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, unsigned *err,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     unsigned long long t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+        if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) {
             raise_err(err, ERR_WAIT_TIMEOUT);
             return false;
         }

@@ -60,6 +60,9 @@ enum : int {
     P_PREPAIRS_LO,
     P_DECORDER,  // decode work items, longest first
     P_DECITEM,   // their 8-word records (AttnPlan::dec_items)
+    P_REQKEYS,   // keys each decode request's work items cover (AttnPlan::req_keys)
+    P_PADDED,    // 1: every request padded to the batch's longest input (a conventional batch)
+    P_FIELDS
 };
 
 struct KRec {
@@ -155,50 +158,65 @@ struct orca_engine {
 namespace {
 
 // Sizes of one plan; the same function drives both orca_plan_words and the build.
+//
+// A padded plan runs the batch the conventional way ([houmin] 3.1.2 "问题";
+// [arcsin2] 3.2): one [B, Lq] block of rows, every request padded with token 0
+// after its own rows to the batch's longest input Lq, and the single-row
+// (increment) requests attending over the batch's longest key range with the
+// keys past their own context masked.  Pad rows sit at the positions after the
+// request's real rows and append their K/V there (inside its reservation,
+// overwritten by its next real row); the next token comes from each request's
+// last real row, so the results equal the selective batch's.
 struct Layout {
     int B, R, n_dec, n_pre, n_dec_work, n_pre_tiles, chunk;
-    int64_t off[P_DECITEM + 1];
+    int padded, lq, lk;  // padded: rows per request and keys per increment request
+    int64_t off[P_FIELDS];
 };
 
-int decode_chunk(const orca_engine *E, const orca_batch *b) {
-    int64_t keys = 0, n = 0;
-    for (int i = 0; i < b->n_req; ++i)
-        if (b->n_input[i] == 1) keys += (int64_t)b->ctx_len[i] + 1, ++n;
+// Rows request i takes, and the keys its decode items cover.
+int rows_of(const Layout &lay, const orca_batch *b, int i) { return lay.padded ? lay.lq : b->n_input[i]; }
+int keys_of(const Layout &lay, const orca_batch *b, int i) { return lay.padded ? lay.lk : b->ctx_len[i] + 1; }
+
+int decode_chunk(const orca_engine *E, const orca_batch *b, const Layout &lay) {
     int chunk = 512;
     // shrink the chunk until the decode grid has a few CTAs per SM
     while (chunk > 64) {
         int64_t items = 0;
         for (int i = 0; i < b->n_req; ++i)
-            if (b->n_input[i] == 1) items += ceil_div((int64_t)b->ctx_len[i] + 1, chunk);
+            if (rows_of(lay, b, i) == 1) items += ceil_div(keys_of(lay, b, i), chunk);
         if (items * E->nh >= 4LL * E->num_sms) break;
         chunk /= 2;
     }
-    (void)keys;
-    (void)n;
     return chunk;
 }
 
-int layout(const orca_engine *E, const orca_batch *b, Layout *lay) {
+int layout(const orca_engine *E, const orca_batch *b, Layout *lay, bool padded) {
     if (!b || b->n_req < 1 || b->n_req > E->cfg.max_batch) return ORCA_ERR_INVALID;
     if (!b->request_id || !b->phase || !b->n_input || !b->ctx_len || !b->kv_offset || !b->tokens)
         return ORCA_ERR_INVALID;
     lay->B = b->n_req;
+    lay->padded = padded;
+    lay->lq = lay->lk = 0;
     int64_t R = 0;
     for (int i = 0; i < b->n_req; ++i) {
         if (b->n_input[i] < 1 || b->ctx_len[i] < 0) return ORCA_ERR_INVALID;
         R += b->n_input[i];
+        lay->lq = std::max(lay->lq, b->n_input[i]);
+        lay->lk = std::max(lay->lk, b->ctx_len[i] + 1);
     }
+    if (padded) R = (int64_t)lay->lq * b->n_req;
     if (R > E->cfg.max_tokens) return ORCA_ERR_INVALID;
     lay->R = (int)R;
-    lay->chunk = decode_chunk(E, b);
+    lay->chunk = decode_chunk(E, b, *lay);
     int nd = 0, np = 0, work = 0, tiles = 0;
     for (int i = 0; i < b->n_req; ++i) {
-        if (b->n_input[i] == 1) {
+        const int n = rows_of(*lay, b, i);
+        if (n == 1) {
             ++nd;
-            work += ceil_div((int64_t)b->ctx_len[i] + 1, lay->chunk);
+            work += ceil_div(keys_of(*lay, b, i), lay->chunk);
         } else {
             ++np;
-            tiles += ceil_div(b->n_input[i], kPrefillRowsPerTile);
+            tiles += ceil_div(n, kPrefillRowsPerTile);
         }
     }
     lay->n_dec = nd, lay->n_pre = np, lay->n_dec_work = work, lay->n_pre_tiles = tiles;
@@ -221,28 +239,30 @@ int layout(const orca_engine *E, const orca_batch *b, Layout *lay) {
     put(P_DECITEM, 8 * (int64_t)work);
     put(P_PRETILES, 2 * (int64_t)tiles);
     put(P_LASTROW, B);
+    put(P_REQKEYS, B);
     lay->off[P_TOTAL] = w;
     return ORCA_OK;
 }
 
-int build(orca_engine *E, const orca_batch *b, int32_t *buf, int64_t cap) {
+int build(orca_engine *E, const orca_batch *b, int32_t *buf, int64_t cap, bool padded) {
     Layout lay;
-    int rc = layout(E, b, &lay);
+    int rc = layout(E, b, &lay, padded);
     if (rc != ORCA_OK) return rc;
     if (!buf || cap < lay.off[P_TOTAL]) return ORCA_ERR_INVALID;
     const int B = lay.B;
-    // validation against the model limits and the K/V reservations
+    // validation against the model limits and the K/V reservations (a
+    // padded request's pad rows must fit them too)
     std::unordered_set<int64_t> seen;
     int64_t tok_i = 0;
     for (int i = 0; i < B; ++i) {
         const int64_t id = b->request_id[i];
         if (!seen.insert(id).second) return ORCA_ERR_INVALID;
-        const int n = b->n_input[i], ctx = b->ctx_len[i];
+        const int n = b->n_input[i], ctx = b->ctx_len[i], rows = rows_of(lay, b, i);
         if (b->phase[i] != (ctx > 0 ? 1 : 0)) return ORCA_ERR_INVALID;
-        if ((int64_t)ctx + n > E->cfg.max_pos) return ORCA_ERR_INVALID;
+        if ((int64_t)ctx + rows > E->cfg.max_pos) return ORCA_ERR_INVALID;
         int64_t off = 0, len = 0;
         if (!E->pool.lookup(id, &off, &len)) return ORCA_ERR_INVALID;
-        if (b->kv_offset[i] != off || (int64_t)ctx + n > len) return ORCA_ERR_INVALID;
+        if (b->kv_offset[i] != off || (int64_t)ctx + rows > len) return ORCA_ERR_INVALID;
         for (int j = 0; j < n; ++j, ++tok_i) {
             const int32_t t = b->tokens[tok_i];
             if (t >= E->V || (t < 0 && -1 - (int64_t)t >= E->built_prev_n)) return ORCA_ERR_INVALID;
@@ -253,26 +273,28 @@ int build(orca_engine *E, const orca_batch *b, int32_t *buf, int64_t cap) {
     int32_t *tokens = buf + lay.off[P_TOKENS], *row_pos = buf + lay.off[P_ROWPOS], *row_slot = buf + lay.off[P_ROWSLOT];
     int32_t *dec_wb = buf + lay.off[P_DECWB], *dec_nch = buf + lay.off[P_DECNCH];
     int32_t *dec_work = buf + lay.off[P_DECWORK], *pre_tiles = buf + lay.off[P_PRETILES];
-    int32_t *last_row = buf + lay.off[P_LASTROW];
+    int32_t *last_row = buf + lay.off[P_LASTROW], *req_keys = buf + lay.off[P_REQKEYS];
     int r = 0, work = 0, tiles = 0;
-    int64_t dec_keys = 0, pre_keys = 0, pre_pairs = 0;
+    int64_t dec_keys = 0, pre_keys = 0, pre_pairs = 0, src = 0;
     for (int i = 0; i < B; ++i) {
-        const int n = b->n_input[i], ctx = b->ctx_len[i];
+        const int n = rows_of(lay, b, i), real = b->n_input[i], ctx = b->ctx_len[i];
         req_off[i] = r;
         req_ctx[i] = ctx;
         req_kv[i] = (int32_t)b->kv_offset[i];
+        req_keys[i] = keys_of(lay, b, i);
         for (int j = 0; j < n; ++j, ++r) {
-            tokens[r] = b->tokens[r];
+            tokens[r] = j < real ? b->tokens[src + j] : 0;  // pad rows: token 0
             row_pos[r] = ctx + j;
             row_slot[r] = (int32_t)(b->kv_offset[i] + ctx + j);
         }
-        last_row[i] = r - 1;
+        src += real;
+        last_row[i] = req_off[i] + real - 1;
         if (n == 1) {
-            const int nch = ceil_div((int64_t)ctx + 1, lay.chunk);
+            const int nch = ceil_div(req_keys[i], lay.chunk);
             dec_wb[i] = work;
             dec_nch[i] = nch;
             for (int c = 0; c < nch; ++c, ++work) dec_work[2 * work] = i, dec_work[2 * work + 1] = c;
-            dec_keys += ctx + 1;
+            dec_keys += req_keys[i];
         } else {
             dec_wb[i] = -1;
             dec_nch[i] = 0;
@@ -282,8 +304,8 @@ int build(orca_engine *E, const orca_batch *b, int32_t *buf, int64_t cap) {
         }
     }
     req_off[B] = r;
-    decode_order(dec_work, lay.n_dec_work, req_ctx, lay.chunk, buf + lay.off[P_DECORDER]);
-    decode_items(buf + lay.off[P_DECORDER], dec_work, lay.n_dec_work, req_off, req_ctx, req_kv, dec_wb, dec_nch,
+    decode_order(dec_work, lay.n_dec_work, req_keys, lay.chunk, buf + lay.off[P_DECORDER]);
+    decode_items(buf + lay.off[P_DECORDER], dec_work, lay.n_dec_work, req_off, req_keys, req_kv, dec_wb, dec_nch,
                  lay.chunk, buf + lay.off[P_DECITEM]);
     buf[P_MAGIC] = kPlanMagic;
     buf[P_NREQ] = B;
@@ -301,6 +323,8 @@ int build(orca_engine *E, const orca_batch *b, int32_t *buf, int64_t cap) {
     buf[P_PREPAIRS_LO] = (int32_t)(pre_pairs & 0x7FFFFFFF);
     buf[P_DECORDER] = (int32_t)lay.off[P_DECORDER];
     buf[P_DECITEM] = (int32_t)lay.off[P_DECITEM];
+    buf[P_REQKEYS] = (int32_t)lay.off[P_REQKEYS];
+    buf[P_PADDED] = lay.padded;
     E->built_prev_n = B;
     return ORCA_OK;
 }
@@ -338,6 +362,7 @@ int run_plan(orca_engine *E, const int32_t *hp, const int32_t *dp, int32_t *dev_
     ap.dec_order = dp + hp[P_DECORDER];
     ap.dec_items = dp + hp[P_DECITEM];
     ap.pre_tiles = dp + hp[P_PRETILES];
+    ap.req_keys = dp + hp[P_REQKEYS];
     ap.n_dec_work = hp[P_NDECWORK];
     ap.n_pre_tiles = hp[P_NPRETILES];
     ap.chunk = hp[P_CHUNK];
@@ -673,13 +698,25 @@ int orca_kv_layout_get(orca_engine *E, orca_kv_layout *out) {
 int64_t orca_plan_words(const orca_engine *E, const orca_batch *b) {
     if (!E) return ORCA_ERR_INVALID;
     Layout lay;
-    const int rc = layout(E, b, &lay);
+    const int rc = layout(E, b, &lay, false);
     return rc == ORCA_OK ? lay.off[P_TOTAL] : rc;
 }
 
 int orca_plan_build(orca_engine *E, const orca_batch *b, int32_t *host_buf, int64_t cap_words) {
     if (!E) return ORCA_ERR_INVALID;
-    return build(E, b, host_buf, cap_words);
+    return build(E, b, host_buf, cap_words, false);
+}
+
+int64_t orca_plan_words_padded(const orca_engine *E, const orca_batch *b) {
+    if (!E) return ORCA_ERR_INVALID;
+    Layout lay;
+    const int rc = layout(E, b, &lay, true);
+    return rc == ORCA_OK ? lay.off[P_TOTAL] : rc;
+}
+
+int orca_plan_build_padded(orca_engine *E, const orca_batch *b, int32_t *host_buf, int64_t cap_words) {
+    if (!E) return ORCA_ERR_INVALID;
+    return build(E, b, host_buf, cap_words, true);
 }
 
 int orca_run_planned(orca_engine *E, const int32_t *host_plan, const int32_t *dev_plan, int32_t *dev_out_next) {
@@ -697,11 +734,12 @@ int orca_engine_sync(orca_engine *E) {
     return check_flag(E);
 }
 
-int orca_run_iteration(orca_engine *E, const orca_batch *b, int32_t *out_next) {
+namespace {
+int run_iteration_impl(orca_engine *E, const orca_batch *b, int32_t *out_next, bool padded) {
     if (!E || !out_next || !E->has_weights) return ORCA_ERR_INVALID;
     const int saved_prev = E->built_prev_n;
     E->built_prev_n = E->run_prev_n;  // feedback refers to the last iteration actually run
-    int rc = build(E, b, E->h_plan, E->plan_cap);
+    int rc = build(E, b, E->h_plan, E->plan_cap, padded);
     if (rc != ORCA_OK) {
         E->built_prev_n = saved_prev;
         return rc;
@@ -724,6 +762,15 @@ int orca_run_iteration(orca_engine *E, const orca_batch *b, int32_t *out_next) {
     if (rc != ORCA_OK) return rc;
     std::memcpy(out_next, E->h_next, (size_t)B * 4);
     return ORCA_OK;
+}
+}  // namespace
+
+int orca_run_iteration(orca_engine *E, const orca_batch *b, int32_t *out_next) {
+    return run_iteration_impl(E, b, out_next, false);
+}
+
+int orca_run_iteration_padded(orca_engine *E, const orca_batch *b, int32_t *out_next) {
+    return run_iteration_impl(E, b, out_next, true);
 }
 
 int orca_get_last_hidden(orca_engine *E, float *host_out, int64_t n) {
@@ -790,6 +837,16 @@ int orca_engine_timing_read(orca_engine *E, orca_kernel_time *out, int32_t cap, 
     return ORCA_OK;
 }
 
+int orca_debug_expire_wait(orca_engine *E, int64_t limit_ns) {
+    if (!E || limit_ns < 1 || limit_ns > 10000000000LL) return ORCA_ERR_INVALID;
+    if (expire_wait((unsigned long long)limit_ns, E->d_err, E->st) != cudaSuccess) {
+        cudaGetLastError();
+        return ORCA_ERR_CUDA;
+    }
+    E->launches++;
+    return ORCA_OK;
+}
+
 int orca_op_attention(orca_engine *E, int32_t dtype, const void *qkv, const void *kv_layer, int64_t kv_slots,
                       int32_t n_heads, int32_t head_dim, int32_t n_req, const int32_t *n_input,
                       const int32_t *ctx_len, const int64_t *kv_offset, void *out) {
@@ -814,7 +871,7 @@ int orca_op_attention(orca_engine *E, int32_t dtype, const void *qkv, const void
     std::vector<int32_t> toks((size_t)rows, 0);
     orca_batch b{n_req, ids.data(), phase.data(), n_input, ctx_len, kv_offset, toks.data()};
     Layout lay;
-    int rc = layout(E, &b, &lay);
+    int rc = layout(E, &b, &lay, false);
     if (rc != ORCA_OK) return rc;
     if (lay.off[P_TOTAL] > E->plan_cap ||
         (int64_t)lay.n_dec_work * n_heads * (head_dim + 2) > E->attn_part_work * E->nh * (E->d + 2))
@@ -828,11 +885,13 @@ int orca_op_attention(orca_engine *E, int32_t dtype, const void *qkv, const void
     int32_t *req_off = buf + lay.off[P_REQOFF], *req_ctx = buf + lay.off[P_REQCTX], *req_kv = buf + lay.off[P_REQKV];
     int32_t *dec_wb = buf + lay.off[P_DECWB], *dec_nch = buf + lay.off[P_DECNCH];
     int32_t *dec_work = buf + lay.off[P_DECWORK], *pre_tiles = buf + lay.off[P_PRETILES];
+    int32_t *req_keys = buf + lay.off[P_REQKEYS];
     int r = 0, work = 0, tiles = 0;
     for (int i = 0; i < n_req; ++i) {
         req_off[i] = r;
         req_ctx[i] = ctx_len[i];
         req_kv[i] = (int32_t)kv_offset[i];
+        req_keys[i] = ctx_len[i] + 1;
         if (n_input[i] == 1) {
             const int nch = ceil_div((int64_t)ctx_len[i] + 1, lay.chunk);
             dec_wb[i] = work;
@@ -847,8 +906,8 @@ int orca_op_attention(orca_engine *E, int32_t dtype, const void *qkv, const void
         r += n_input[i];
     }
     req_off[n_req] = r;
-    decode_order(dec_work, lay.n_dec_work, req_ctx, lay.chunk, buf + lay.off[P_DECORDER]);
-    decode_items(buf + lay.off[P_DECORDER], dec_work, lay.n_dec_work, req_off, req_ctx, req_kv, dec_wb, dec_nch,
+    decode_order(dec_work, lay.n_dec_work, req_keys, lay.chunk, buf + lay.off[P_DECORDER]);
+    decode_items(buf + lay.off[P_DECORDER], dec_work, lay.n_dec_work, req_off, req_keys, req_kv, dec_wb, dec_nch,
                  lay.chunk, buf + lay.off[P_DECITEM]);
     if (cudaMemcpyAsync(E->d_plan, E->h_plan, (size_t)lay.off[P_TOTAL] * 4, cudaMemcpyHostToDevice, E->st) !=
         cudaSuccess) {
@@ -866,6 +925,7 @@ int orca_op_attention(orca_engine *E, int32_t dtype, const void *qkv, const void
     ap.dec_order = dp + lay.off[P_DECORDER];
     ap.dec_items = dp + lay.off[P_DECITEM];
     ap.pre_tiles = dp + lay.off[P_PRETILES];
+    ap.req_keys = dp + lay.off[P_REQKEYS];
     ap.n_dec_work = lay.n_dec_work;
     ap.n_pre_tiles = lay.n_pre_tiles;
     ap.chunk = lay.chunk;

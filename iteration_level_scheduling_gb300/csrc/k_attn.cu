@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const AttnArgs
             for (int q = blockIdx.x; q < total && ok; q += G) {
                 int i, c, h;
                 item(q, i, c, h);
-                const int n_keys = a.p.req_ctx[i] + 1;
+                const int n_keys = a.p.req_keys ? a.p.req_keys[i] : a.p.req_ctx[i] + 1;
                 const int t0 = c * a.p.chunk, t1 = min(n_keys, t0 + a.p.chunk);
                 const size_t head_base = ((size_t)h * a.kv_slots + a.p.req_kvoff[i]) * D;
                 for (int t = t0; t < t1; t += kDecTok, ++g) {
@@ -257,7 +257,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const AttnArgs
         int i, c, h;
         item(q, i, c, h);
         const int row = a.p.req_off[i];
-        const int n_keys = a.p.req_ctx[i] + 1;
+        const int n_keys = a.p.req_keys ? a.p.req_keys[i] : a.p.req_ctx[i] + 1;
+        const int n_valid = a.p.req_ctx[i] + 1;  // keys past the context (a padded batch's) are masked
         const int t0 = c * a.p.chunk, t1 = min(n_keys, t0 + a.p.chunk);
         float qv[VEC];
 #pragma unroll
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const AttnArgs
                 ok = false;
                 break;
             }
-            const int ntok = min(kDecTok, t1 - t);
+            const int ntok = min(kDecTok, min(t1, n_valid) - t);  // (<= 0: a stage of masked keys only)
             float sc[STEPS], vv[STEPS][VEC];
 #pragma unroll
             for (int st = 0; st < STEPS; ++st) {
@@ -889,6 +890,10 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
         int4 r0, r1;
         rec(q, r0, r1);
         const int t0 = 0, t1 = r0.y;  // keys of this item, from its first
+        // keys of the item within the request's context (fewer than t1 in a
+        // padded batch: the rest are loaded but masked; <= 0 for an item of
+        // padding only)
+        const int t_valid = a.p.req_ctx[r0.w] + 1 - r1.w;
         uint32_t qb[KS][2];
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qn[ks][0], qb[ks][1] = qn[ks][1];
@@ -903,7 +908,7 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
                 return;
             }
             const uint32_t kb = smem_u32(ring + s * kStage), vb = kb + NB * kBox;
-            const int ntok = min(kMdTok, t1 - t);
+            const int ntok = min(kMdTok, min(t1, t_valid) - t);  // rows to use (past them: masked, V zeroed)
             if (j0 < ntok) {
                 // S^T = K q^T for tokens j0 .. j0 + 15: lane (g8, t4) gets tokens j0 + g8 and j0 + g8 + 8
                 float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1045,7 +1050,7 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
 
 }  // namespace
 
-void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_ctx, int chunk, int32_t *order) {
+void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_keys, int chunk, int32_t *order) {
     if (chunk < 1 || chunk > 512) {  // (the engine's chunks are 64 .. 512) keep the given order
         for (int w = 0; w < n_work; ++w) order[w] = w;
         return;
@@ -1054,7 +1059,7 @@ void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_ctx, i
     int start[513 + 1] = {0};
     auto keys = [&](int w) {
         const int i = dec_work[2 * w], c = dec_work[2 * w + 1];
-        return std::min(chunk, req_ctx[i] + 1 - c * chunk);
+        return std::min(chunk, req_keys[i] - c * chunk);
     };
     for (int w = 0; w < n_work; ++w) ++start[chunk - keys(w) + 1];
     for (int b = 1; b <= chunk; ++b) start[b] += start[b - 1];
@@ -1062,11 +1067,11 @@ void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_ctx, i
 }
 
 void decode_items(const int32_t *order, const int32_t *dec_work, int n_work, const int32_t *req_off,
-                  const int32_t *req_ctx, const int32_t *req_kvoff, const int32_t *dec_wbegin, const int32_t *dec_nch,
+                  const int32_t *req_keys, const int32_t *req_kvoff, const int32_t *dec_wbegin, const int32_t *dec_nch,
                   int chunk, int32_t *items) {
     for (int k = 0; k < n_work; ++k) {
         const int w = order[k], i = dec_work[2 * w], c = dec_work[2 * w + 1];
-        const int t0 = c * chunk, t1 = std::min(req_ctx[i] + 1, t0 + chunk);
+        const int t0 = c * chunk, t1 = std::min(req_keys[i], t0 + chunk);
         int32_t *r = items + 8 * (size_t)k;
         r[0] = req_kvoff[i] + t0, r[1] = t1 - t0, r[2] = req_off[i], r[3] = i;
         r[4] = c, r[5] = dec_nch[i], r[6] = dec_wbegin[i], r[7] = t0;
@@ -1175,13 +1180,14 @@ extern "C" int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, con
     }
     int64_t n_work = 0;
     for (int i = 0; i < n_req; ++i) n_work += ((int64_t)ctx_len[i] + chunk) / chunk;
-    const size_t items_at = (6 * (size_t)n_req + 1 + 3 * (size_t)n_work + 3) & ~size_t(3);  // 16-byte aligned
+    const size_t items_at = (7 * (size_t)n_req + 1 + 3 * (size_t)n_work + 3) & ~size_t(3);  // 16-byte aligned
     const size_t words = items_at + 8 * (size_t)n_work;
     if (words > kNaPlanWords || (size_t)n_work * n_heads * (head_dim + 2) > kNaPartFloats) return kLimit;
 
     // tables: req_off, req_ctx, req_kvoff, dec_wbegin, dec_nch, dec_work
     int32_t *req_off = g_na_plan, *req_ctx = req_off + n_req + 1, *req_kv = req_ctx + n_req;
-    int32_t *dec_wb = req_kv + n_req, *dec_nch = dec_wb + n_req, *dec_work = dec_nch + n_req;
+    int32_t *dec_wb = req_kv + n_req, *dec_nch = dec_wb + n_req, *req_keys = dec_nch + n_req;
+    int32_t *dec_work = req_keys + n_req;
     int32_t *dec_ord = dec_work + 2 * n_work;
     int w = 0;
     for (int i = 0; i < n_req; ++i) {
@@ -1189,13 +1195,14 @@ extern "C" int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, con
         req_off[i] = i;
         req_ctx[i] = ctx_len[i];
         req_kv[i] = (int32_t)kv_offset[i];
+        req_keys[i] = ctx_len[i] + 1;
         dec_wb[i] = w;
         dec_nch[i] = nch;
         for (int c = 0; c < nch; ++c, ++w) dec_work[2 * w] = i, dec_work[2 * w + 1] = c;
     }
     req_off[n_req] = n_req;
-    decode_order(dec_work, (int)n_work, req_ctx, chunk, dec_ord);
-    decode_items(dec_ord, dec_work, (int)n_work, req_off, req_ctx, req_kv, dec_wb, dec_nch, chunk, g_na_plan + items_at);
+    decode_order(dec_work, (int)n_work, req_keys, chunk, dec_ord);
+    decode_items(dec_ord, dec_work, (int)n_work, req_off, req_keys, req_kv, dec_wb, dec_nch, chunk, g_na_plan + items_at);
 
     float *part = reinterpret_cast<float *>(nd.scratch);
     int32_t *counters = reinterpret_cast<int32_t *>(part + kNaPartFloats);
@@ -1215,6 +1222,7 @@ extern "C" int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, con
     ap.dec_work = plan + (dec_work - g_na_plan);
     ap.dec_order = plan + (dec_ord - g_na_plan);
     ap.dec_items = plan + items_at;
+    ap.req_keys = plan + (req_keys - g_na_plan);
     ap.pre_tiles = nullptr;
     ap.n_dec_work = (int)n_work;
     ap.n_pre_tiles = 0;

@@ -295,6 +295,26 @@ template cudaError_t layernorm<bf16>(float *, const int32_t *, const float *, co
 template cudaError_t kv_append<float>(const float *, const int32_t *, float *, int64_t, int, int, int, cudaStream_t);
 template cudaError_t kv_append<bf16>(const bf16 *, const int32_t *, bf16 *, int64_t, int, int, int, cudaStream_t);
 
+namespace {
+// One thread waits, bounded, on an mbarrier nothing arrives on: the wait runs
+// out after limit_ns and records ERR_WAIT_TIMEOUT, as an expired wait in any
+// kernel would.
+__global__ void expire_wait_kernel(unsigned long long limit_ns, unsigned *err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0u, err, limit_ns);
+}
+}  // namespace
+
+cudaError_t expire_wait(unsigned long long limit_ns, unsigned *err, cudaStream_t st) {
+    expire_wait_kernel<<<1, 32, 0, st>>>(limit_ns, err);
+    return cudaGetLastError();
+}
+
 cudaError_t max_smem_once(const void *kernel, int bytes) {
     static std::mutex mu;
     static std::set<std::pair<int, const void *>> done;

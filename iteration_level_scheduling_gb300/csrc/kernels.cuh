@@ -80,6 +80,7 @@ bool gemm_uses_sk(int m_tok, int n_out, int k, const GemmScratch &s);
 size_t gemm_sk_part_floats(int num_sms);
 int gemm_sk_counters(int max_rows, int max_n);
 
+
 // cuTensorMapEncodeTiled, reached through the runtime's driver entry point;
 // dims/strides/box innermost first (strides in bytes, rank - 1 of them).
 bool encode_tensor_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t rank, const void *base, const uint64_t *dims,
@@ -112,6 +113,9 @@ cudaError_t kv_append(const T *qkv, const int32_t *row_slot, T *pool_layer, int6
 
 struct AttnPlan {
     const int32_t *req_off, *req_ctx, *req_kvoff;
+    // keys each decode request's work items cover: ctx + 1, or in a padded
+    // batch the batch's longest (keys past ctx + 1 are loaded and masked); null = ctx + 1
+    const int32_t *req_keys;
     const int32_t *dec_work, *dec_wbegin, *dec_nch;  // decode split-K work items
     const int32_t *dec_order;                        // work items, longest first
     // per entry of dec_order, 8 words (16-byte aligned): kv_offset + first key,
@@ -130,16 +134,21 @@ cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *ou
 
 // Order of the decode work items (request, chunk) by number of keys, longest
 // first (stable), for the persistent decode kernel's load balance.
-void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_ctx, int chunk, int32_t *order);
+// req_keys[i]: the keys request i's items cover (AttnPlan::req_keys).
+void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_keys, int chunk, int32_t *order);
 // The 8-word records of AttnPlan::dec_items, in the order of `order`.
 void decode_items(const int32_t *order, const int32_t *dec_work, int n_work, const int32_t *req_off,
-                  const int32_t *req_ctx, const int32_t *req_kvoff, const int32_t *dec_wbegin, const int32_t *dec_nch,
+                  const int32_t *req_keys, const int32_t *req_kvoff, const int32_t *dec_wbegin, const int32_t *dec_nch,
                   int chunk, int32_t *items);
 
 // next[b] = argmax_j logits[b, j] (lowest j on ties); also to out2 if non-null.
 cudaError_t argmax_rows(const float *logits, int n_rows, int V, int32_t *next, int32_t *out2, cudaStream_t st);
 
 constexpr int kPrefillRowsPerTile = 64;
+
+// A bounded wait that nothing satisfies, given up after limit_ns (failure-
+// detection tests of the device error word).
+cudaError_t expire_wait(unsigned long long limit_ns, unsigned *err, cudaStream_t st);
 
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current
 // device.  The attribute belongs to the device that was current when it was

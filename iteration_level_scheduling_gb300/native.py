@@ -28,10 +28,11 @@ KERNEL_KINDS = ["embed", "layernorm", "gemm_qkv", "kv_append", "attn_decode", "a
 EXPORTS = [
     "orca_strerror", "orca_engine_create", "orca_engine_destroy", "orca_kv_alloc", "orca_kv_free",
     "orca_kv_layout_get", "orca_run_iteration", "orca_plan_words", "orca_plan_build", "orca_run_planned",
+    "orca_run_iteration_padded", "orca_plan_words_padded", "orca_plan_build_padded",
     "orca_engine_sync", "orca_get_last_hidden", "orca_get_last_logits", "orca_engine_stats_get",
     "orca_engine_timing", "orca_engine_timing_read", "orca_op_linear", "orca_op_attention", "orca_packed_weight_elems",
     "orca_pack_weight",
-    "orca_attention_decode_noalloc", "orca_sched_create", "orca_sched_destroy",
+    "orca_attention_decode_noalloc", "orca_debug_expire_wait", "orca_sched_create", "orca_sched_destroy",
     "orca_sched_submit", "orca_sched_set_token_feedback", "orca_sched_next", "orca_sched_complete", "orca_sched_cancel",
     "orca_sched_stats_get", "orca_sched_request_get",
     "orca_sched_request_tokens", "orca_sched_run",
@@ -108,6 +109,9 @@ _sig = {
     "orca_plan_words": (C.c_int64, [P, C.POINTER(Batch)]),
     "orca_plan_build": (C.c_int, [P, C.POINTER(Batch), P, C.c_int64]),
     "orca_run_planned": (C.c_int, [P, P, P, P]),
+    "orca_run_iteration_padded": (C.c_int, [P, C.POINTER(Batch), P]),
+    "orca_plan_words_padded": (C.c_int64, [P, C.POINTER(Batch)]),
+    "orca_plan_build_padded": (C.c_int, [P, C.POINTER(Batch), P, C.c_int64]),
     "orca_engine_sync": (C.c_int, [P]),
     "orca_get_last_hidden": (C.c_int, [P, P, C.c_int64]),
     "orca_get_last_logits": (C.c_int, [P, P, C.c_int64]),
@@ -121,6 +125,7 @@ _sig = {
     "orca_op_attention": (C.c_int, [P, C.c_int32, P, P, C.c_int64, C.c_int32, C.c_int32, C.c_int32, P, P, P, P]),
     "orca_attention_decode_noalloc": (C.c_int, [C.c_int32, P, P, C.c_int64, C.c_int32, C.c_int32, C.c_int32, P, P,
                                                 P, P]),
+    "orca_debug_expire_wait": (C.c_int, [P, C.c_int64]),
     "orca_sched_create": (C.c_int, [C.POINTER(SchedConfig), P, C.POINTER(P)]),
     "orca_sched_destroy": (C.c_int, [P]),
     "orca_sched_submit": (C.c_int, [P, C.c_int64, C.c_double, P, C.c_int32, C.c_int32, C.c_int32,
@@ -232,11 +237,19 @@ class Engine:
         check(lib.orca_run_iteration(self._h, C.byref(batch.c), _ptr(out)), "orca_run_iteration")
         return out
 
-    def plan_words(self, batch: BatchDesc) -> int:
-        return check(lib.orca_plan_words(self._h, C.byref(batch.c)), "orca_plan_words")
+    def plan_words(self, batch: BatchDesc, padded: bool = False) -> int:
+        f = lib.orca_plan_words_padded if padded else lib.orca_plan_words
+        return check(f(self._h, C.byref(batch.c)), "orca_plan_words")
 
-    def plan_build(self, batch: BatchDesc, buf: np.ndarray) -> None:
-        check(lib.orca_plan_build(self._h, C.byref(batch.c), _ptr(buf), buf.size), "orca_plan_build")
+    def plan_build(self, batch: BatchDesc, buf: np.ndarray, padded: bool = False) -> None:
+        f = lib.orca_plan_build_padded if padded else lib.orca_plan_build
+        check(f(self._h, C.byref(batch.c), _ptr(buf), buf.size), "orca_plan_build")
+
+    def run_iteration_padded(self, batch: BatchDesc) -> np.ndarray:
+        """The iteration as a conventional padded + masked batch (see orca.h)."""
+        out = np.zeros(batch.n_req, np.int32)
+        check(lib.orca_run_iteration_padded(self._h, C.byref(batch.c), _ptr(out)), "orca_run_iteration_padded")
+        return out
 
     def run_planned(self, host_plan: np.ndarray, dev_plan_ptr: int, dev_out_ptr: int = 0) -> None:
         check(lib.orca_run_planned(self._h, _ptr(host_plan), P(dev_plan_ptr), P(dev_out_ptr or None)),
@@ -278,6 +291,10 @@ class Engine:
               "orca_op_linear")
         if sync:
             self.sync()
+
+    def debug_expire_wait(self, limit_ns: int) -> None:
+        """Make a bounded device wait run out (see orca.h); asynchronous."""
+        check(lib.orca_debug_expire_wait(self._h, int(limit_ns)), "orca_debug_expire_wait")
 
     @staticmethod
     def packed_weight_elems(n_out: int, k: int) -> int:

@@ -49,6 +49,9 @@ SHAPES = [
     # stream-K over several token tiles: feature-tile major with cut tiles (2
     # token tiles), token-tile major with cut tiles (5 token tiles)
     (300, 12800, 320), (1100, 5120, 512),
+    # more output tiles than SMs at decode sizes (two CTAs on some SMs),
+    # 1..128 rows, the vocabulary-sized tail
+    (64, 20480, 256), (7, 50257, 192), (128, 19584, 128), (100, 25600, 320), (1, 50257, 64),
 ]
 
 

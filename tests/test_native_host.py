@@ -294,3 +294,54 @@ def test_pipelined_protocol(native):
     for bad in (dict(mode=1), dict(token_feedback=True)):
         with pytest.raises(native.OrcaError):
             native.Scheduler(2, 4096, kv_slots=100, n_workers=2, **bad)
+
+
+def faulty_oracle_pool(monkeypatch, n):
+    """The oracle's pool with its n-th reservation failing as if full (the
+    oracle side of ORCA_FAULT=kv_alloc:n)."""
+    from oracle import kv as okv
+    orig = okv.KVPool.alloc
+
+    def alloc(self, rid, n_tokens):
+        if n_tokens <= 0 or rid in self.owned:
+            return orig(self, rid, n_tokens)
+        self._calls = getattr(self, "_calls", 0) + 1
+        return None if self._calls == n else orig(self, rid, n_tokens)
+
+    monkeypatch.setattr(okv.KVPool, "alloc", alloc)
+
+
+@pytest.mark.parametrize("nth", [1, 3, 9, 25])
+def test_injected_kv_alloc_failure_keeps_scheduler_consistent(native, monkeypatch, nth):
+    """ORCA_FAULT=kv_alloc:N makes the N-th K/V reservation fail as if the pool
+    were full ([0h-n0] scheduler algorithm: admission stops when K/V runs out).
+    The scheduler must stall that admission and retry it later exactly as the
+    oracle does under the same failure: identical batches, offsets and slots,
+    every request finished, every reservation returned."""
+    trace = synth.poisson_trace(40 + nth, n=60, rate=1.5, prompt_range=(1, 40), out_range=(1, 20), vocab=1000)
+    clean_native = drive_native(native, trace, 6, 200, 6 * 64, kv_reserve=64)[1]
+    monkeypatch.setenv("ORCA_FAULT", f"kv_alloc:{nth}")
+    s, recs = drive_native(native, trace, 6, 200, 6 * 64, kv_reserve=64)
+    monkeypatch.delenv("ORCA_FAULT")
+    faulty_oracle_pool(monkeypatch, nth)
+    _, orecs = drive_oracle(trace, 6, 200, 6 * 64, kv_reserve=64)
+    assert_same(recs, orecs)
+    # the fault changed the schedule (the failed admission waited)
+    assert [(k, b.request_id.tolist()) for k, b in recs] != [(k, b.request_id.tolist()) for k, b in clean_native]
+    st = s.stats()
+    assert st.finished == len(trace) and st.kv_reserved == 0
+    for sp in trace:
+        assert s.request(sp.rid).n_generated == sp.out_len
+
+
+def test_fault_injection_reads_only_its_point(native, monkeypatch):
+    """Other entries in ORCA_FAULT, or none, leave the pool alone."""
+    monkeypatch.setenv("ORCA_FAULT", "plan_h2d:1,kv_allocx:1")
+    s = native.Scheduler(2, 100, kv_slots=100)
+    assert s.submit(0, 0.0, [1], 5, ctx0=3) == 0
+    monkeypatch.setenv("ORCA_FAULT", "other:4,kv_alloc:1")
+    s2 = native.Scheduler(2, 100, kv_slots=100)
+    with pytest.raises(native.OrcaError) as e:
+        s2.submit(0, 0.0, [1], 5, ctx0=3)
+    assert e.value.code == native.ERR_KV_FULL
+    assert s2.submit(1, 0.0, [1], 5, ctx0=3) == 0  # only the first call fails
