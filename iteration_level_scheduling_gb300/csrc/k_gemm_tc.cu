@@ -86,6 +86,7 @@ struct TcArgs {
     Epilogue e;
     int vec_out;  // output / residual rows allow 16-byte (fp32) or 8-byte (bf16) vector access
     int mode;     // kDirect, or kPartial (split-K slabs to e.part)
+    int w_policy; // L2 policy of the weight loads: 0 evict-first (read once), 1 normal, 2 evict-last (reused)
     const bf16 *w_packed;  // weights in the tile-contiguous layout of pack_weight_bf16, or null (tensor map)
     unsigned *err;
 };
@@ -171,9 +172,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The whole warp runs the loop (so addresses and coordinates stay warp-
         // uniform) and one elected lane issues the copies.
         const bool leader = elect_one();
-        // with one token tile the weights are read exactly once: stream them past L2
+        // with one token tile the weights are read exactly once: stream them past
+        // L2; with several, the CTAs of a raster group reuse them from L2
         const bool stream_w = a.n_tok_tiles == 1;
-        const uint64_t pol_w = l2_policy_evict_first();
+        const uint64_t pol_w = a.w_policy == 0   ? l2_policy_evict_first()
+                               : a.w_policy == 1 ? l2_policy_evict_normal()
+                                                 : l2_policy_evict_last();
         // packed weights: tile (ft, kb) is one contiguous 16 KiB block, already in
         // the swizzled shared-memory image, so one bulk copy moves it
         const bf16 *wp = a.w_packed ? a.w_packed + (size_t)ft * a.num_kb * (BM * BK) : nullptr;
@@ -181,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *sa = smem + (size_t)s * stage_bytes;
             if (wp)
                 bulk_load(sa, wp + (size_t)(kb0 + i) * (BM * BK), kStageA, &full[s], pol_w);
-            else if (stream_w)
+            else if (stream_w || a.w_policy != 1)
                 tma_load_2d_hint(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM, pol_w);
             else
                 tma_load_2d(sa, &tmw, &full[s], (kb0 + i) * BK, ft * BM);
@@ -896,6 +900,12 @@ int override_stages() {
     static int v = env_int("ORCA_GEMM_STAGES");
     return v;
 }
+// ORCA_GEMM_WPOL: L2 policy of the weights, 1 normal, 2 evict-last, 3
+// evict-first; unset = by token tiles (tuning).
+int override_wpol() {
+    static int v = env_int("ORCA_GEMM_WPOL");
+    return v;
+}
 
 // ORCA_GEMM_SK: 1 = stream-K whenever the workspace allows, -1 = never,
 // unset / 0 = by token rows (kSkMinRows).
@@ -1136,6 +1146,15 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_pa
                 !(reinterpret_cast<uintptr_t>(e.resid) & 15);
     if (e.kv_pool && !a.vec_out) return cudaErrorInvalidValue;
     a.mode = t.splits == 1 ? kDirect : kPartial;
+    // Weights stream past L2 (evict-first) unless many token tiles reuse them
+    // long after their first read: up to 8 token tiles the tiles that share a
+    // weight block run at about the same time and hit it in L2 anyway, and
+    // evict-first leaves L2 to the activations (13B QKV at 572 rows 866 ->
+    // 927 TFLOP/s); with 101 token tiles (25777 rows) evict-first made every
+    // token tile re-read the weights from DRAM (13.1 GB read, against 2.3 GB
+    // with the normal policy; 1210 -> 1354 TFLOP/s).
+    a.w_policy = override_wpol() == 1 ? 1 : override_wpol() == 2 ? 2 : override_wpol() == 3 ? 0
+                 : t.n_tok_tiles > 8 ? 1 : 0;
     a.w_packed = w_packed ? w : nullptr;
     a.err = s.err;
     if (a.mode == kPartial && n_partials) *n_partials = t.splits;
