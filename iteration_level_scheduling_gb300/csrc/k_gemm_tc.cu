@@ -442,7 +442,10 @@ constexpr size_t kSkSmemExtra = 1024 + kSkTail;
 struct SkArgs {
     int m_tok, n_out, num_kb, bn, stages;
     int n_tok_tiles, n_feat_tiles, n_units, chunk;
-    int tt_major;  // tile order: token-tile major (tile = tt * nft + ft) or feature-tile major (ft * ntt + tt)
+    // tile order: kSkFeatMajor (tile = ft * ntt + tt), kSkTokMajor (tt * nft + ft),
+    // or kSkWhole: CTA b takes whole tiles b, b + G, b + 2G, ... of the one-tile
+    // kernel's raster order (no tile is cut; n_units and chunk are unused)
+    int order;
     uint32_t idesc, tmem_cols;
     Epilogue e;
     const bf16 *w_packed;  // tile-contiguous weights (pack_weight_bf16), or null (tensor map)
@@ -454,7 +457,22 @@ struct SkArgs {
     unsigned *err;
 };
 
+enum { kSkFeatMajor = 0, kSkTokMajor = 1, kSkWhole = 2 };
+
 __device__ __forceinline__ int sk_unit_begin(int b, const SkArgs &a) { return min(b * a.chunk, a.n_units); }
+// Raster order of the whole-tile walk: groups of kGroup feature tiles, the
+// token tiles inside a group, a group's feature tiles innermost.  The tiles
+// that all CTAs hold at one time (consecutive in this order) then span a few
+// token tiles of one group: its weights and those activations stay in L2.
+__device__ __forceinline__ void sk_raster(int lin, int nft, int ntt, int &ft, int &tt) {
+    const int per_group = kGroup * ntt;
+    const int g = lin / per_group;
+    const int first = g * kGroup;
+    const int gsize = min(nft - first, kGroup);
+    const int r = lin - g * per_group;
+    ft = first + r % gsize;
+    tt = r / gsize;
+}
 __device__ __forceinline__ int sk_part_slot(int b, int tile, const SkArgs &a) {
     return 2 * b + (sk_unit_begin(b, a) / a.num_kb == tile ? 0 : 1);
 }
@@ -488,15 +506,26 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     int *tile_slot = reinterpret_cast<int *>(tail + 256);                  // [bn] K/V pool slot of each token
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int u_begin = sk_unit_begin(blockIdx.x, a), u_end = sk_unit_begin(blockIdx.x + 1, a);
     // Tile order.  Feature-tile major, a CTA takes a feature tile's token
     // tiles one after the other, re-reading its weights.  Token-tile major
     // (chosen with four or more token tiles), the CTAs holding the token tiles
     // of one feature tile are nft * nkb units apart: they walk the same weight
-    // blocks at about the same time and share them in L2.
+    // blocks at about the same time and share them in L2.  Whole tiles: this
+    // CTA's units are numbered 0.. over its own tiles (tile index j of the
+    // walk = raster tile blockIdx.x + j * gridDim.x), so no unit range cuts a tile.
     const int nkb = a.num_kb, ntt = a.n_tok_tiles, nft = a.n_feat_tiles;
-    auto ft_of = [&](int tile) { return a.tt_major ? tile % nft : tile / ntt; };
-    auto tt_of = [&](int tile) { return a.tt_major ? tile / nft : tile % ntt; };
+    const bool whole = a.order == kSkWhole;
+    const int n_whole = whole ? max(0, (nft * ntt - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) : 0;
+    const int u_begin = whole ? 0 : sk_unit_begin(blockIdx.x, a);
+    const int u_end = whole ? n_whole * nkb : sk_unit_begin(blockIdx.x + 1, a);
+    auto coords = [&](int tile, int &ft, int &tt) {
+        if (whole) {
+            sk_raster((int)blockIdx.x + tile * (int)gridDim.x, nft, ntt, ft, tt);
+        } else {
+            ft = a.order == kSkTokMajor ? tile % nft : tile / ntt;
+            tt = a.order == kSkTokMajor ? tile / nft : tile % ntt;
+        }
+    };
 
     pdl_trigger();
     if (threadIdx.x == 0) {
@@ -529,7 +558,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         // loop (warp-uniform control) and one elected lane issues the copies.
         const bool leader = elect_one();
         // weights are streamed past L2 unless token tiles share them there
-        const uint64_t pol_w = a.tt_major ? l2_policy_evict_normal() : l2_policy_evict_first();
+        const uint64_t pol_w = a.order != kSkFeatMajor ? l2_policy_evict_normal() : l2_policy_evict_first();
         // A unit's tile and K block are tracked as running counters, and the
         // ring slot and phase too: no division per stage on this path.
         struct Cursor {
@@ -539,16 +568,14 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             Cursor c;
             c.tile = u / nkb;
             c.kb = u - c.tile * nkb;
-            c.ft = ft_of(c.tile);
-            c.tt = tt_of(c.tile);
+            coords(c.tile, c.ft, c.tt);
             return c;
         };
         auto step = [&](Cursor &c) {
             if (++c.kb == nkb) {
                 c.kb = 0;
                 ++c.tile;
-                c.ft = ft_of(c.tile);
-                c.tt = tt_of(c.tile);
+                coords(c.tile, c.ft, c.tt);
             }
         };
         auto load_w = [&](const Cursor &c, int s) {
@@ -668,7 +695,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             const int tile = u / nkb, k0 = u - tile * nkb, k1 = min(nkb, k0 + (u_end - u));
             u += k1 - k0;
             const int buf = p & 1;
-            const int ft = ft_of(tile), tt = tt_of(tile);
+            int ft, tt;
+            coords(tile, ft, tt);
             const int t_base = tt * a.bn, t_lim = min(a.bn, a.m_tok - t_base);
             const int f = ft * BM + row;
             const bool f_ok = f < a.n_out;
@@ -920,6 +948,13 @@ constexpr int kSkMinRows = 129;
 // whole weight once per token tile.  Measured on the 13B FFN1 at 25777 rows:
 // stream-K 7.99 ms with 55 GB of DRAM reads, one-tile about 1.4x faster.
 constexpr int kSkMaxRows = 1024;
+// ORCA_GEMM_WHOLE: 1 = the whole-tile persistent walk whenever the one-tile
+// launch needs two waves or more, -1 = never; unset = from kWholeMinRows rows.
+int override_whole() {
+    static int v = env_int("ORCA_GEMM_WHOLE");
+    return v;
+}
+constexpr int kWholeMinRows = 1025;
 
 }  // namespace
 
@@ -1050,6 +1085,18 @@ int gemm_sk_counters(int max_rows, int max_n) {
     return std::max(1 << 16, ceil_div(std::max(max_rows, 1), kSkMaxBn) * ceil_div(std::max(max_n, 1), BM));
 }
 
+// The whole-tile persistent walk (SkArgs::order == kSkWhole) for layers whose
+// one-tile launch needs several waves: one CTA per SM keeps its ring streaming
+// across tiles and drains each accumulator while the next tile's MMAs run,
+// where every one-tile CTA pays its own pipeline fill and an epilogue nothing
+// overlaps.  It cuts no tile, so it needs no workspace.
+bool gemm_uses_whole(int m_tok, int n_out, int k, const GemmScratch &s) {
+    if (m_tok <= 0 || k % BK != 0 || k <= 0 || n_out <= 0 || override_whole() < 0) return false;
+    const SkShape t = gemm_sk_shape(m_tok, n_out, k, s.num_sms);
+    if (t.stages < 2 || t.tiles < 2 * s.num_sms) return false;
+    return override_whole() > 0 || m_tok >= kWholeMinRows;
+}
+
 bool gemm_uses_sk(int m_tok, int n_out, int k, const GemmScratch &s) {
     if (!s.sk_part || !s.sk_cnt || m_tok <= 0 || k % BK != 0 || k <= 0 || n_out <= 0) return false;
     if (override_sk() < 0) return false;
@@ -1063,8 +1110,9 @@ bool gemm_uses_sk(int m_tok, int n_out, int k, const GemmScratch &s) {
 
 namespace {
 cudaError_t launch_sk(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_packed, int m_tok, int n_out, int k,
-                      const Epilogue &e, const GemmScratch &s, cudaStream_t st) {
-    const SkShape t = gemm_sk_shape(m_tok, n_out, k, s.num_sms);
+                      const Epilogue &e, const GemmScratch &s, cudaStream_t st, bool whole) {
+    SkShape t = gemm_sk_shape(m_tok, n_out, k, s.num_sms);
+    if (whole) t.grid = std::min(t.tiles, s.num_sms);
     {
         cudaError_t ae = max_smem_once((const void *)gemm_sk_kernel, (int)kSmemMaxCta);
         if (ae != cudaSuccess) return ae;
@@ -1080,15 +1128,15 @@ cudaError_t launch_sk(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_packe
     a.stages = t.stages;
     a.n_tok_tiles = t.n_tok_tiles;
     a.n_feat_tiles = t.n_feat_tiles;
-    a.tt_major = t.n_tok_tiles >= 4;
+    a.order = whole ? kSkWhole : t.n_tok_tiles >= 4 ? kSkTokMajor : kSkFeatMajor;
     a.n_units = t.units;
     a.chunk = t.chunk;
     a.idesc = idesc_bf16_f32(BM, t.bn);
     a.tmem_cols = (uint32_t)t.tmem_cols;
     a.e = e;
     a.w_packed = w_packed ? w : nullptr;
-    a.part = s.sk_part;
-    a.cnt = s.sk_cnt;
+    a.part = whole ? nullptr : s.sk_part;
+    a.cnt = whole ? nullptr : s.sk_cnt;
     a.err = s.err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(t.grid);
@@ -1111,7 +1159,8 @@ cudaError_t gemm_tc_bf16(const bf16 *x, int x_rows_cap, const bf16 *w, bool w_pa
     if (k % BK != 0 || k <= 0 || n_out <= 0 || x_rows_cap < m_tok) return cudaErrorInvalidValue;
     if (e.kv_pool && (e.kv_hd % 4 != 0 || !e.row_slot || !e.out_bf16)) return cudaErrorInvalidValue;
     if (w_packed && (reinterpret_cast<uintptr_t>(w) & 15)) return cudaErrorInvalidValue;
-    if (gemm_uses_sk(m_tok, n_out, k, s)) return launch_sk(x, x_rows_cap, w, w_packed, m_tok, n_out, k, e, s, st);
+    if (gemm_uses_whole(m_tok, n_out, k, s)) return launch_sk(x, x_rows_cap, w, w_packed, m_tok, n_out, k, e, s, st, true);
+    if (gemm_uses_sk(m_tok, n_out, k, s)) return launch_sk(x, x_rows_cap, w, w_packed, m_tok, n_out, k, e, s, st, false);
     const bool allow_partial = e.part != nullptr && !(reinterpret_cast<uintptr_t>(e.part) & 15);
     const TcShape t = gemm_tc_shape(m_tok, n_out, k, s, allow_partial, e.part_cap);
     if (t.stages < 2 || (size_t)t.stages * (kStageA + t.bn * BK * 2) < (size_t)std::min(t.bn, 256) * BM * 4)

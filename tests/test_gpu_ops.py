@@ -52,6 +52,10 @@ SHAPES = [
     # more output tiles than SMs at decode sizes (two CTAs on some SMs),
     # 1..128 rows, the vocabulary-sized tail
     (64, 20480, 256), (7, 50257, 192), (128, 19584, 128), (100, 25600, 320), (1, 50257, 64),
+    # the persistent whole-tile walk (1025+ rows, two waves of tiles or more):
+    # several tiles per CTA through both accumulator buffers, a partial raster
+    # group (63 feature tiles, the last one ragged), ragged token tiles
+    (1100, 12800, 128), (2100, 8000, 192), (4097, 5120, 64),
 ]
 
 
