@@ -950,11 +950,15 @@ constexpr int kSkMinRows = 129;
 constexpr int kSkMaxRows = 1024;
 // ORCA_GEMM_WHOLE: 1 = the whole-tile persistent walk whenever the one-tile
 // launch needs two waves or more, -1 = never; unset = from kWholeMinRows rows.
+// Measured on the 13B shapes (stand-alone): QKV at 572 rows 98.5 -> 82.6 us,
+// FFN1 at 1024 rows 229 -> 161 us, at 25777 rows 4621 -> 3101 us; inside the
+// 13B trace's window 6656 -> 6713 tok/s; at 64 rows the LM head (393 tiles)
+// is 2.4 us slower, hence the row floor.
 int override_whole() {
     static int v = env_int("ORCA_GEMM_WHOLE");
     return v;
 }
-constexpr int kWholeMinRows = 1025;
+constexpr int kWholeMinRows = 129;
 
 }  // namespace
 
