@@ -412,6 +412,25 @@ def kernel_breakdown(recs, n_layers, steps):
             for k, d in sorted(kinds.items(), key=lambda kv: -kv[1]["est"])}
 
 
+def kernel_breakdown_by_kind(recs, work, n_layers):
+    """kernel_breakdown for decode-only and prompt-carrying iterations apart: the
+    records split into iterations at each embedding launch (the first of an
+    iteration), `work` giving each iteration's rows."""
+    its, cur = [], None
+    for r in recs:
+        if r["kind"] == "embed":
+            cur = []
+            its.append(cur)
+        if cur is not None:
+            cur.append(r)
+    out = {}
+    for name, sel in (("decode_only", lambda w: w["R"] == w["B"]), ("with_prefill", lambda w: w["R"] > w["B"])):
+        idx = [i for i, w in enumerate(work[:len(its)]) if sel(w)]
+        if idx:
+            out[name] = kernel_breakdown([r for i in idx for r in its[i]], n_layers, len(idx))
+    return out
+
+
 def per_kernel_pass(eng, dp, first, count):
     """The same plans again with CUDA events around every launch of one sampled
     layer per iteration and the per-iteration kernels (events between launches
@@ -1003,6 +1022,7 @@ def run_headline(args, eng, trace, cfg, peaks, world, local_rank):
                  "weighting": "per-launch bytes and times weighted by launches per iteration "
                               f"({cfg.n_layers} per projection, 1 LM head)"})
     breakdown = kernel_breakdown(recs, cfg.n_layers, args.steps)
+    breakdown_by_kind = kernel_breakdown_by_kind(recs, work[args.warmup:], cfg.n_layers)
     del dp
 
     # ---------------- the same window through the public serve loop --------
@@ -1028,7 +1048,8 @@ def run_headline(args, eng, trace, cfg, peaks, world, local_rank):
                                    mean_batch=float(np.mean([w["B"] for w in work[args.warmup:]])),
                                    mean_rows=float(np.mean([w["R"] for w in work[args.warmup:]])),
                                    by_kind=split_by_prefill(work[args.warmup:], it_ms, fr)),
-        "roofline": roof, "kernels": breakdown, "gemm_by_kind": gemm_kinds, "gpu_launches": launches,
+        "roofline": roof, "kernels": breakdown, "kernels_by_kind": breakdown_by_kind, "gemm_by_kind": gemm_kinds,
+        "gpu_launches": launches,
         "clocks": clk, "e2e": e2e,
     }
 

@@ -76,6 +76,27 @@ def test_split_by_prefill():
     assert "with_prefill" not in bench.split_by_prefill(work[:1], [8.0], [0.8])
 
 
+def test_kernel_breakdown_by_kind_splits_at_embed():
+    """Records of three iterations (decode-only, prompt-carrying, decode-only):
+    split at each embedding launch and grouped by the iterations' kind."""
+    import bench
+    def it(prefill):
+        r = [dict(kind="embed", layer=-1, ms=0.01, bytes=1.0, flops=0.0),
+             dict(kind="gemm_qkv", layer=0, ms=0.04, bytes=1e6, flops=1e9),
+             dict(kind="attn_decode", layer=0, ms=0.10, bytes=1e6, flops=0.0)]
+        if prefill:
+            r.append(dict(kind="attn_prefill", layer=0, ms=0.02, bytes=1e5, flops=1e8))
+        return r + [dict(kind="lm_head", layer=-1, ms=0.09, bytes=5e8, flops=1e10)]
+    recs = it(False) + it(True) + it(False)
+    work = [dict(R=64, B=64), dict(R=400, B=64), dict(R=64, B=64)]
+    out = bench.kernel_breakdown_by_kind(recs, work, 40)
+    assert set(out) == {"decode_only", "with_prefill"}
+    assert "attn_prefill" in out["with_prefill"] and "attn_prefill" not in out["decode_only"]
+    assert out["decode_only"]["attn_decode"]["launches_timed"] == 2
+    assert abs(out["decode_only"]["attn_decode"]["est_ms_per_iteration"] - 40 * 0.10) < 1e-9
+    assert out["with_prefill"]["gemm (all linear layers)"]["launches_timed"] == 2  # QKV and the LM head
+
+
 def test_gemm_roofline_weights_launches_per_iteration():
     """The linear-layer family's achieved bandwidth weights each sampled-layer
     launch by the model depth and the LM head by one: bytes per iteration over
