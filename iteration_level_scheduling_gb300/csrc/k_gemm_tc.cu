@@ -67,7 +67,7 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 9;
 constexpr int kMaxSplits = 8;  // split-K ways (partial slabs)
 constexpr int kStageA = BM * BK * 2;  // 16 KiB
 constexpr int kGroup = 16;            // feature tiles per raster group
@@ -949,7 +949,9 @@ constexpr int kSkMinRows = 129;
 // stream-K 7.99 ms with 55 GB of DRAM reads, one-tile about 1.4x faster.
 constexpr int kSkMaxRows = 1024;
 // ORCA_GEMM_WHOLE: 1 = the whole-tile persistent walk whenever the one-tile
-// launch needs two waves or more, -1 = never; unset = from kWholeMinRows rows.
+// launch needs two waves or more (more than one without a stream-K
+// workspace), 2 = more than one wave in any case, -1 = never; unset = the
+// same as 1 from kWholeMinRows rows (tuning, tests).
 // Measured on the 13B shapes (stand-alone): QKV at 572 rows 98.5 -> 82.6 us,
 // FFN1 at 1024 rows 229 -> 161 us, at 25777 rows 4621 -> 3101 us; inside the
 // 13B trace's window 6656 -> 6713 tok/s; at 64 rows the LM head (393 tiles)
@@ -1097,7 +1099,11 @@ int gemm_sk_counters(int max_rows, int max_n) {
 bool gemm_uses_whole(int m_tok, int n_out, int k, const GemmScratch &s) {
     if (m_tok <= 0 || k % BK != 0 || k <= 0 || n_out <= 0 || override_whole() < 0) return false;
     const SkShape t = gemm_sk_shape(m_tok, n_out, k, s.num_sms);
-    if (t.stages < 2 || t.tiles < 2 * s.num_sms) return false;
+    // from two waves of tiles; from more than one where the caller gives no
+    // stream-K workspace (stream-K balances one to two waves better, where
+    // it may run: FFN1 at 200 rows 67 us against 81 us on the walk)
+    const bool one_wave = override_whole() == 2 || !s.sk_part;
+    if (t.stages < 2 || t.tiles < (one_wave ? s.num_sms + 1 : 2 * s.num_sms)) return false;
     return override_whole() > 0 || m_tok >= kWholeMinRows;
 }
 

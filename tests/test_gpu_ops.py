@@ -161,6 +161,29 @@ def test_linear_sk_repeatable(eng):
         assert torch.equal(outs[0], o)
 
 
+def run_child(env_extra):
+    import json
+    import os
+    import subprocess
+    import sys
+    env = dict(os.environ, **env_extra)
+    child = os.path.join(os.path.dirname(__file__), "wide_tile_child.py")
+    out = subprocess.run([sys.executable, child], env=env, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    return [json.loads(line) for line in out.stdout.splitlines() if line.startswith("{")]
+
+
+def test_linear_whole_walk_one_to_two_waves(eng):
+    """The whole-tile walk between one and two waves of tiles (as QKV takes it
+    inside an iteration at 257..512 rows): CTAs holding one tile beside CTAs
+    holding two, every epilogue, packed and unpacked weights, ragged rows."""
+    rows = run_child({"ORCA_GEMM_WHOLE": "2"})
+    assert len(rows) == 4 * 3 * 2
+    for r in rows:
+        tol = 1e-5 * max(1.0, np.sqrt(r["k"] / 1024)) if r["mode"] == "bias_resid_f32" else 8e-3
+        assert r["rel"] < tol, r
+
+
 def test_linear_wide_token_tile(eng):
     """257..448 rows in one token tile (two MMAs per K step, the epilogue in two
     256-column halves), in a process where stand-alone calls may not take the

@@ -1,7 +1,10 @@
-"""Run by test_gpu_ops.test_linear_wide_token_tile in a process with
-ORCA_GEMM_SK=-1 (read once per process), so that stand-alone linear calls take
-the one-tile-per-CTA kernel: shapes with 257..448 rows whose launch model picks
-one wide token tile (two MMAs per K step).  Prints one JSON line per case."""
+"""Run by test_gpu_ops in a process of its own (the kernel-choice overrides are
+read once per process).  With ORCA_GEMM_SK=-1 (test_linear_wide_token_tile)
+stand-alone linear calls take the one-tile-per-CTA kernel: shapes with
+257..448 rows whose launch model picks one wide token tile (two MMAs per K
+step).  With ORCA_GEMM_WHOLE=2 (test_linear_whole_walk_one_to_two_waves) the
+same shapes, 160..240 tiles, take the whole-tile walk with one or two tiles
+per CTA.  Prints one JSON line per case."""
 
 import json
 import sys
