@@ -10,6 +10,9 @@ kernel chosen is the engine's own choice for a stand-alone call (stream-K
 from 129 rows when every SM gets a tile); ORCA_GEMM_SK=-1 in the
 environment keeps the one-tile kernel, as an iteration does for every layer
 but FFN1.
+
+``--library`` times the vendor library instead (``torch.matmul``, bf16, no
+epilogue), the same way, for calibration only: nothing in the engine calls it.
 """
 
 from __future__ import annotations
@@ -32,7 +35,11 @@ def main() -> None:
     p.add_argument("--epilogue", default="bias_gelu_bf16", choices=["bf16", "bias_gelu_bf16", "bias_resid_f32"])
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--reps", type=int, default=10)
+    p.add_argument("--library", action="store_true", help="time torch.matmul on the same shape instead")
     a = p.parse_args()
+    if a.library:
+        library(a)
+        return
 
     torch.manual_seed(0)
     stream = torch.cuda.current_stream().cuda_stream
@@ -74,6 +81,34 @@ def main() -> None:
     print(json.dumps({"m": a.m, "n": a.n, "k": a.k, "epilogue": a.epilogue, "us": t * 1e6,
                       "TFLOP/s": flops / t / 1e12, "GB/s": byts / t / 1e9}), flush=True)
     eng.close()
+
+
+def library(a) -> None:
+    """torch.matmul (cuBLAS) on x [m, k] @ w[n, k]^T in bf16, timed as above."""
+    import torch
+
+    torch.manual_seed(0)
+    x = torch.randn(a.m, a.k, device="cuda").to(torch.bfloat16)
+    w = (torch.randn(a.n, a.k, device="cuda") * 0.02).to(torch.bfloat16)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(a.warmup):
+        y = x @ w.t()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    total = 0.0
+    for _ in range(a.reps):
+        flush.zero_()
+        s.record()
+        y = x @ w.t()
+        e.record()
+        e.synchronize()
+        total += s.elapsed_time(e)
+    t = total / a.reps / 1000.0
+    flops = 2.0 * a.m * a.n * a.k
+    byts = 2.0 * (a.n * a.k + a.m * a.k + a.m * a.n)
+    print(json.dumps({"m": a.m, "n": a.n, "k": a.k, "library": "torch.matmul", "us": t * 1e6,
+                      "TFLOP/s": flops / t / 1e12, "GB/s": byts / t / 1e9}), flush=True)
+    del y
 
 
 if __name__ == "__main__":
