@@ -322,8 +322,8 @@ int orca_op_attention(orca_engine *eng, int32_t dtype, const void *qkv, const vo
  * returns ORCA_ERR_LIMIT and does nothing.
  * It calls no cudaMalloc, cudaFree or other allocating routine.  The first call
  * on a device looks up the array's device address (once per device, with that
- * device current), so make it before any stream capture.  The host tables are
- * copied from pageable memory, which waits for the stream's earlier work.
+ * device current).  The host tables are copied from pageable memory, which
+ * waits for the stream's earlier work.
  * Every call shares the one array and it keeps the last call's contents (the
  * counters are cleared at each call): calls that overlap on the GPU -- on
  * different streams, or from different threads -- race and must not be made.
