@@ -151,3 +151,26 @@ def test_trace_phases():
     B = bench.MAX_BATCH
     work = [dict(B=b) for b in [1, 5, B, B, 30, B, 12, 3]]
     assert bench.phases(work) == {"ramp": [0, 1], "steady": [2, 3, 4, 5], "drain": [6, 7]}
+
+
+def test_reference_arm_never_loads_the_engine_library():
+    """bench.py's reference arm (the oracle on the host) takes its batches from
+    the oracle's own scheduler and times the oracle's model: the process never
+    maps liborca.so."""
+    import subprocess
+    import sys
+    code = (
+        "import bench, numpy as np\n"
+        "from iteration_level_scheduling_gb300 import synth\n"
+        "b = bench.oracle_window_batches(256, 2)\n"
+        "assert len(b) == 2 and all(len(r[0]) == 64 for r in b)\n"
+        "cfg = synth.ModelConfig(n_layers=2, hidden=64, n_heads=4, ffn=256, vocab=512, max_pos=2048, dtype='bf16')\n"
+        "r = bench.OracleRunner(cfg, 0, np.float32)\n"
+        "t, B, m = r.step([1, 2], [3, 1], [0, 5], [7, 8, 9, 10])\n"
+        "assert B == 2 and t > 0\n"
+        "maps = open('/proc/self/maps').read()\n"
+        "print('liborca' in maps)\n")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300,
+                         cwd=__file__.rsplit("/", 2)[0])
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert out.stdout.strip().splitlines()[-1] == "False"
