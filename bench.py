@@ -500,6 +500,26 @@ def cpu_line(runner, batches, what):
                        f"{runner.cfg.n_layers} layers")}
 
 
+def one_thread_sample(window_start: int):
+    """tokens/s of the same oracle sample with one BLAS thread: a child process
+    started with single-thread BLAS (the thread count is fixed when NumPy
+    loads), timing the second of two window iterations; None if it fails."""
+    code = ("import json, numpy as np, bench\n"
+            f"b = bench.oracle_window_batches({window_start}, 2)\n"
+            "r = bench.OracleRunner(bench.MODEL, 0, np.float32)\n"
+            "r.step(*b[0])\n"
+            "t, B, m = r.step(*b[1])\n"
+            "print(json.dumps({'value': B / t, 'measured_ms_per_sample': 1000 * m}))\n")
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    try:
+        out = subprocess.run([sys.executable, "-c", code], env=env, cwd=ROOT, capture_output=True, text=True,
+                             timeout=600)
+        return json.loads(out.stdout.strip().splitlines()[-1]) if out.returncode == 0 else None
+    except (subprocess.TimeoutExpired, ValueError, IndexError):
+        return None
+
+
 def oracle_window_batches(window_start: int, n: int):
     """Batches of the headline window, scheduled by the oracle's scheduler."""
     from oracle import sched as osched
@@ -1083,6 +1103,7 @@ def run_orca(args, rank, world, local_rank):
             runner = OracleRunner(MODEL, 0, np.float32)
             line["cpu_baseline"] = cpu_line(runner, oracle_window_batches(args.window_start + args.warmup, 3),
                                             "2 window iterations")
+            line["cpu_baseline"]["one_thread"] = one_thread_sample(args.window_start + args.warmup)
 
     # ---------------- the other workloads ------------------------------------
     if solo and args.configs:
