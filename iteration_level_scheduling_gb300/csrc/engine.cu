@@ -99,11 +99,12 @@ struct orca_engine {
     int32_t *h_next = nullptr;
     int32_t *h_plan = nullptr, *d_plan = nullptr;
     int64_t plan_cap = 0;
-    // GEMM launch contexts: `gs` without a stream-K workspace (one-tile-per-CTA
-    // kernel only), `gs_op` with one (stream-K allowed: stand-alone
-    // orca_op_linear calls and FFN1).  Inside an iteration the stream-K kernel,
-    // which fills every SM, is mostly slower end to end: the one-tile kernel's
-    // idle SMs let the next launch start early under programmatic launch.
+    // GEMM launch contexts: `gs` without a stream-K workspace (the one-tile
+    // kernel, and the whole-tile walk for layers of more than one wave of
+    // tiles), `gs_op` with one (stream-K allowed: stand-alone orca_op_linear
+    // calls and FFN1).  Inside an iteration stream-K proper, which fills every
+    // SM, is mostly slower end to end: the one-tile kernel's idle SMs let the
+    // next launch start early under programmatic launch.
     GemmScratch gs, gs_op;
     float *part = nullptr;  // split-K partial slabs of the residual projections
     size_t part_cap = 0;

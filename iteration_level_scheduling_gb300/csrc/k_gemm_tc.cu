@@ -29,12 +29,16 @@
 // partial tile to a slab; no CTA waits on another.  Otherwise one CTA per tile
 // with a deep stage ring, one CTA per SM when the tiles fit in one wave.
 //
-// With 129+ token rows and at least one output tile per SM the stream-K
-// kernel further below takes the layer instead (gemm_uses_sk), when the
-// caller's launch context carries a stream-K workspace.  The engine gives one
-// to stand-alone linear calls and to FFN1 only: elsewhere in an iteration the
-// one-tile kernel is faster end to end, because its idle SMs let the next
-// launch start early.
+// With 129+ token rows two more launch shapes run on the stream-K kernel
+// further below.  When the one-tile launch would need more than one wave of
+// tiles (two waves where a stream-K workspace is given), the whole-tile walk
+// (gemm_uses_whole): one persistent CTA per SM takes whole tiles in this
+// kernel's raster order, its ring and a double-buffered accumulator carried
+// across tiles.  Below that, with at least one output tile per SM and a
+// stream-K workspace in the caller's launch context, stream-K proper
+// (gemm_uses_sk).  The engine gives the workspace to stand-alone linear calls
+// and to FFN1 only: elsewhere in an iteration the one-tile kernel is faster
+// end to end, because its idle SMs let the next launch start early.
 //
 // Weights can be pre-packed (pack_weight_bf16) so each 128 x 64 stage tile is
 // one contiguous, already swizzled 16 KiB block read by a single bulk copy:
