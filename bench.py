@@ -633,6 +633,36 @@ def phases(work):
     return {"ramp": list(range(0, a)), "steady": list(range(a, b + 1)), "drain": list(range(b + 1, len(work)))}
 
 
+def request_latency(arrival, out_len, ids_per_it, sel_clock, it_ms):
+    """Per-request latency on the device timeline of a run whose iterations took
+    it_ms back to back: from the start of the first iteration selected at or
+    after the request's arrival (logical clock; sel_clock[i] is iteration i's,
+    nondecreasing) to the end of the iteration that made its last token;
+    queueing until the start of its own first iteration; and latency per output
+    token.  Mean and 50/90/99th percentiles, in ms."""
+    t = np.concatenate([[0.0], np.cumsum(np.asarray(it_ms, np.float64))])
+    first, last = {}, {}
+    for i, ids in enumerate(ids_per_it):
+        for r in ids:
+            first.setdefault(int(r), i)
+            last[int(r)] = i
+    sel = np.asarray(sel_clock)
+    lat, queue, per_tok = [], [], []
+    for r, a in arrival.items():
+        if r not in last:
+            continue
+        k = int(np.searchsorted(sel, a, side="left"))
+        lat.append(t[last[r] + 1] - t[k])
+        queue.append(t[first[r]] - t[k])
+        per_tok.append(lat[-1] / out_len[r])
+
+    def pct(v):
+        return {"mean": float(np.mean(v)), "p50": float(np.percentile(v, 50)), "p90": float(np.percentile(v, 90)),
+                "p99": float(np.percentile(v, 99))}
+    return {"requests": len(lat), "latency_ms": pct(lat), "queue_ms": pct(queue),
+            "ms_per_output_token": pct(per_tok)}
+
+
 def run_full_trace(args, eng, trace, cfg, peaks):
     import torch
 
@@ -644,7 +674,9 @@ def run_full_trace(args, eng, trace, cfg, peaks):
 
     def rec(sched, b):
         st = sched.stats()
-        meta.append(dict(clock=st.clock, waiting=st.waiting, kv_reserved=st.kv_reserved))
+        # (the clock has already advanced past this iteration's selection)
+        meta.append(dict(clock=st.clock, waiting=st.waiting, kv_reserved=st.kv_reserved,
+                         ids=np.ctypeslib.as_array(b.request_id, (b.n_req,)).copy()))
 
     t0 = time.perf_counter()
     plans, shapes = build_plans(eng, s, record=rec)
@@ -670,7 +702,10 @@ def run_full_trace(args, eng, trace, cfg, peaks):
              "ms_per_iteration": total_ms / len(plans), "total_s": total_ms / 1000, "gpu_launches": launches,
              "iteration_roofline": dict(roof, by_phase=by_phase, by_kind=split_by_prefill(work, it_ms, fr)),
              "slots_busy": tokens / (len(plans) * MAX_BATCH), "clocks": clk,
-             "host_plan_build_us_per_iteration": 1e6 * host_plan_s / len(plans)}
+             "host_plan_build_us_per_iteration": 1e6 * host_plan_s / len(plans),
+             "request_latency": request_latency({sp.rid: sp.arrival for sp in trace},
+                                                {sp.rid: sp.out_len for sp in trace},
+                                                [m["ids"] for m in meta], [m["clock"] - 1 for m in meta], it_ms)}
     if args.metrics:
         with open(args.metrics, "w") as f:
             for i, (w, m) in enumerate(zip(work, meta)):

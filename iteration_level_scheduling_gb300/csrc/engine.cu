@@ -22,6 +22,10 @@
 #include <unordered_set>
 #include <vector>
 
+#include <cstdlib>
+
+#include <nvtx3/nvToolsExt.h>  // header-only; inert unless a profiler attaches
+
 #include "../../include/orca.h"
 #include "kernels.cuh"
 #include "kvpool.h"
@@ -64,6 +68,22 @@ enum : int {
     P_PADDED,    // 1: every request padded to the batch's longest input (a conventional batch)
     P_FIELDS
 };
+
+// NVTX ranges around every iteration and every kernel launch, named by kind,
+// when ORCA_NVTX=1 (read once): a timeline tool then shows the iteration's
+// structure.  Off by default.
+bool nvtx_on() {
+    static const bool on = [] {
+        const char *v = getenv("ORCA_NVTX");
+        return v && v[0] == '1';
+    }();
+    return on;
+}
+const char *kind_name(int kind) {
+    static const char *names[] = {"embed",     "layernorm", "gemm_qkv",  "kv_append", "attn_decode", "attn_prefill",
+                                  "gemm_o",    "gemm_ffn1", "gemm_ffn2", "lm_head",   "argmax",      "final_ln"};
+    return kind >= 0 && kind < (int)(sizeof(names) / sizeof(names[0])) ? names[kind] : "kernel";
+}
 
 struct KRec {
     int32_t kind, layer;
@@ -146,7 +166,10 @@ struct orca_engine {
             a = (int)ev_next;
             cudaEventRecord(events[ev_next++], st);
         }
+        const bool nvtx = nvtx_on();
+        if (nvtx) nvtxRangePushA(kind_name(kind));
         cudaError_t e = fn();
+        if (nvtx) nvtxRangePop();
         ++launches;
         if (rec) {
             cudaEventRecord(events[ev_next++], st);
@@ -488,7 +511,11 @@ int run_plan(orca_engine *E, const int32_t *hp, const int32_t *dp, int32_t *dev_
 int run_planned_impl(orca_engine *E, const int32_t *hp, const int32_t *dp, int32_t *dev_out) {
     if (!E->has_weights || !hp || !dp || hp[P_MAGIC] != kPlanMagic) return ORCA_ERR_INVALID;
     if (hp[P_PREVN] != E->run_prev_n) return ORCA_ERR_INVALID;  // plans must run in build order
-    return E->bf ? run_plan<bf16>(E, hp, dp, dev_out) : run_plan<float>(E, hp, dp, dev_out);
+    const bool nvtx = nvtx_on();
+    if (nvtx) nvtxRangePushA("iteration");
+    const int rc = E->bf ? run_plan<bf16>(E, hp, dp, dev_out) : run_plan<float>(E, hp, dp, dev_out);
+    if (nvtx) nvtxRangePop();
+    return rc;
 }
 
 int check_flag(orca_engine *E) {

@@ -174,3 +174,19 @@ def test_reference_arm_never_loads_the_engine_library():
                          cwd=__file__.rsplit("/", 2)[0])
     assert out.returncode == 0, out.stderr[-2000:]
     assert out.stdout.strip().splitlines()[-1] == "False"
+
+
+def test_request_latency_on_the_device_timeline():
+    """Three iterations of 2, 3 and 5 ms selected at logical clocks 0, 1, 3 (an
+    idle tick at 2): request 0 arrives at 0 and runs in iterations 0-1; request
+    1 arrives at 1 and runs in 1-2; request 2 arrives at 2 (runs first at clock
+    3, iteration 2) and runs in 2 only."""
+    import bench
+    out = bench.request_latency({0: 0, 1: 1, 2: 2}, {0: 2, 1: 2, 2: 1}, [[0], [0, 1], [1, 2]], [0, 1, 3],
+                                [2.0, 3.0, 5.0])
+    assert out["requests"] == 3
+    lat = sorted([5.0, 8.0, 5.0])  # 0: [0, 5); 1: [2, 10); 2: [5, 10)
+    assert abs(out["latency_ms"]["mean"] - sum(lat) / 3) < 1e-12
+    assert out["latency_ms"]["p50"] == 5.0
+    assert abs(out["queue_ms"]["mean"] - 0.0) < 1e-12  # each runs in the first iteration it may
+    assert abs(out["ms_per_output_token"]["mean"] - (2.5 + 4.0 + 5.0) / 3) < 1e-12
