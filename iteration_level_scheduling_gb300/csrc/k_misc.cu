@@ -64,6 +64,9 @@ __global__ void __launch_bounds__(kRowThreads) embed_kernel(const int32_t *token
 
 constexpr int kLnThreads = 512;
 constexpr int kLnMaxVec = 4;  // H <= kLnThreads * 4 * kLnMaxVec = 8192
+// the many-rows shape (layernorm_rows_kernel): 256 threads, three CTAs per SM
+constexpr int kLnRowsThreads = 256, kLnRowsVec = 8, kLnRowsCtas = 3;
+constexpr int kLnRowsFrom = 256;  // rows from which it runs
 
 __device__ __forceinline__ float block_sum(float v, float *red) {
     v = warp_sum(v);
@@ -192,6 +195,78 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(float *x, const i
     }
 }
 
+// The same LayerNorm (and split-K completion, the partials summed in the same
+// order; the row statistics sum in a different fixed order) for launches of
+// hundreds of rows and more: the
+// 512-thread kernel above fills an SM's registers with one row, so only one
+// row per SM is in flight (13B, 25777 rows: 382 us per launch, 0.3 of HBM).
+// Here 256 threads take a row and hold only the completed row (8 float4 at
+// most), so three CTAs share an SM.
+template <typename T>
+__global__ void __launch_bounds__(kLnRowsThreads, kLnRowsCtas)
+    layernorm_rows_kernel(float *x, const int32_t *row_map, const float *g, const float *b, T *y, float *y32, int H,
+                          const float *part, int n_part, int part_rows, const float *add_bias) {
+    __shared__ float red[33];
+    pdl_trigger();
+#pragma unroll
+    for (int i = 0; i < kLnRowsVec; ++i) {
+        const int e = (threadIdx.x + i * kLnRowsThreads) * 4;
+        if (e < H) {
+            prefetch_l1(g + e);
+            prefetch_l1(b + e);
+        }
+    }
+    pdl_wait();
+    const int r = blockIdx.x;
+    const int src = row_map ? row_map[r] : r;
+    float *xr = x + (size_t)src * H;
+    float4 q[kLnRowsVec];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kLnRowsVec; ++i) {
+        const int e = (threadIdx.x + i * kLnRowsThreads) * 4;
+        q[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < H) {
+            q[i] = *reinterpret_cast<const float4 *>(xr + e);
+            if (n_part > 0) {
+                // complete the residual row: x + (bias + the split-K partials, in split order)
+                float4 acc = add_bias ? *reinterpret_cast<const float4 *>(add_bias + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int sp = 0; sp < n_part; ++sp) {
+                    const float4 p = *reinterpret_cast<const float4 *>(part + ((size_t)sp * part_rows + src) * H + e);
+                    acc.x += p.x, acc.y += p.y, acc.z += p.z, acc.w += p.w;
+                }
+                q[i].x += acc.x, q[i].y += acc.y, q[i].z += acc.z, q[i].w += acc.w;
+                *reinterpret_cast<float4 *>(xr + e) = q[i];
+            }
+            s += q[i].x + q[i].y + q[i].z + q[i].w;
+        }
+    }
+    const float mean = block_sum(s, red) / (float)H;
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kLnRowsVec; ++i) {
+        const int e = (threadIdx.x + i * kLnRowsThreads) * 4;
+        if (e < H) {
+            const float d0 = q[i].x - mean, d1 = q[i].y - mean, d2 = q[i].z - mean, d3 = q[i].w - mean;
+            ss += d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3;
+        }
+    }
+    const float var = block_sum(ss, red) / (float)H;
+    const float rstd = rsqrtf(var + 1e-5f);
+#pragma unroll
+    for (int i = 0; i < kLnRowsVec; ++i) {
+        const int e = (threadIdx.x + i * kLnRowsThreads) * 4;
+        if (e < H) {
+            const float4 gg = *reinterpret_cast<const float4 *>(g + e);
+            const float4 bb = *reinterpret_cast<const float4 *>(b + e);
+            float o[4] = {(q[i].x - mean) * rstd * gg.x + bb.x, (q[i].y - mean) * rstd * gg.y + bb.y,
+                          (q[i].z - mean) * rstd * gg.z + bb.z, (q[i].w - mean) * rstd * gg.w + bb.w};
+            store_vec4<T>(y + (size_t)r * H + e, o);
+            if (y32) store16(y32 + (size_t)r * H + e, o);
+        }
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) kv_append_kernel(const T *qkv, const int32_t *row_slot,
                                                                 T *pool_layer, int64_t kv_slots, int H, int d,
@@ -267,6 +342,10 @@ cudaError_t layernorm(float *x, const int32_t *row_map, const float *g, const fl
                       int H, cudaStream_t st, const float *part, int n_part, int part_rows, const float *add_bias) {
     if (n_rows <= 0) return cudaSuccess;
     if (H % 4 != 0 || H > kLnThreads * 4 * kLnMaxVec || n_part > 8) return cudaErrorInvalidValue;
+    static_assert(kLnRowsThreads * 4 * kLnRowsVec >= kLnThreads * 4 * kLnMaxVec, "same H limit for both shapes");
+    if (n_rows >= kLnRowsFrom)
+        return launch_pdl(layernorm_rows_kernel<T>, dim3(n_rows), dim3(kLnRowsThreads), 0, st, x, row_map, g, b, y, y32,
+                          H, part, n_part, part_rows, add_bias);
     return launch_pdl(layernorm_kernel<T>, dim3(n_rows), dim3(kLnThreads), 0, st, x, row_map, g, b, y, y32, H, part,
                       n_part, part_rows, add_bias);
 }
