@@ -390,6 +390,7 @@ int run_plan(orca_engine *E, const int32_t *hp, const int32_t *dp, int32_t *dev_
     ap.n_dec_work = hp[P_NDECWORK];
     ap.n_pre_tiles = hp[P_NPRETILES];
     ap.chunk = hp[P_CHUNK];
+    ap.n_rows = hp[P_NROWS];
     const int32_t *tokens = dp + hp[P_TOKENS], *row_pos = dp + hp[P_ROWPOS], *row_slot = dp + hp[P_ROWSLOT];
     const int32_t *last_row = dp + hp[P_LASTROW];
     const double dec_keys = hp[P_DECKEYS], pre_keys = hp[P_PREKEYS];
@@ -957,6 +958,7 @@ int orca_op_attention(orca_engine *E, int32_t dtype, const void *qkv, const void
     ap.n_dec_work = lay.n_dec_work;
     ap.n_pre_tiles = lay.n_pre_tiles;
     ap.chunk = lay.chunk;
+    ap.n_rows = (int)rows;
     const int H = n_heads * head_dim;
     cudaError_t ce;
     if (dtype == ORCA_DTYPE_BF16)

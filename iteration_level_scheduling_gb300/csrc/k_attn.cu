@@ -21,13 +21,16 @@
 //           head_dim 64/128: TMA-loaded stages scored and accumulated on the
 //           tensor cores (below); otherwise bulk copies and SIMT dot products.
 // prefill : requests with several input rows (initiation phase, or any
-//           multi-row request).  Work item = (request, 64 query rows) x head.
-//           bf16 with head_dim 64/128: flash-attention tiles on the tensor
-//           cores (below).  Otherwise each warp owns one query row at a time
-//           and attends causally over keys 0..pos of its request.
+//           multi-row request).  Work item = (request, 128 query rows) x head.
+//           bf16 with head_dim 64/128: flash-attention tiles on the tcgen05
+//           tensor cores, S and O in tensor memory (below; an mma.sync
+//           version is kept for comparisons).  Otherwise each warp owns one
+//           query row at a time and attends causally over keys 0..pos of its
+//           request.
 // Scores use exp2 with log2(e)/sqrt(head_dim) folded into q; the softmax is
 // the online (running max / running sum) form, exact up to rounding.
 #include <algorithm>
+#include <cstdlib>
 #include <type_traits>
 
 #include "common.cuh"
@@ -40,6 +43,16 @@ namespace {
 constexpr int kAttnThreads = 128;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr float kNegBig = -1e30f;
+
+// ORCA_ATTN_PREFILL_TC=-1: bf16 prefill on the mma.sync kernel instead of the
+// tcgen05 one (read once; comparisons).
+int override_prefill_tc() {
+    static const int v = [] {
+        const char *e = getenv("ORCA_ATTN_PREFILL_TC");
+        return e && *e ? atoi(e) : 0;
+    }();
+    return v;
+}
 
 template <typename T>
 struct AttnArgs {
@@ -420,14 +433,15 @@ __global__ void __launch_bounds__(kAttnThreads) attn_prefill_kernel(const AttnAr
 
 // ---------------------------------------------------------------------------
 // Prefill on tensor cores (bf16, head_dim 64 or 128): flash-attention tiling.
-// CTA = (request, 64 query rows, head), 4 warps x 16 rows.  K/V tiles of 64
+// CTA = (request, 64 query rows, head), 4 warps x 16 rows; blockIdx.z picks
+// the half of the plan's 128-row tile.  K/V tiles of 64
 // keys are double-buffered in shared memory (cp.async, 16-byte chunks stored
 // XOR-swizzled by row so ldmatrix reads are conflict-free); S = Q K^T and
 // O += P V run on mma.sync m16n8k16 with fp32 accumulators; the softmax is the
 // online form, rows held in registers.  Causal: row r of the request sits at
 // position ctx + r and sees keys 0 .. ctx + r.
 // ---------------------------------------------------------------------------
-constexpr int kPreRows = 64;  // query rows per CTA (== kPrefillRowsPerTile)
+constexpr int kPreRows = 64;  // query rows per CTA (half of kPrefillRowsPerTile)
 constexpr int kPreKeys = 64;  // keys per tile
 
 template <int D>
@@ -487,9 +501,10 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const AttnArgs<bf
     pdl_wait();
 
     const int tile = blockIdx.x, h = blockIdx.y;
-    const int i = a.p.pre_tiles[2 * tile], q0 = a.p.pre_tiles[2 * tile + 1];
+    const int i = a.p.pre_tiles[2 * tile], q0 = a.p.pre_tiles[2 * tile + 1] + kPreRows * (int)blockIdx.z;
     const int off = a.p.req_off[i];
     const int n = a.p.req_off[i + 1] - off;
+    if (q0 >= n) return;  // the tile's second half is past the request
     const int ctx = a.p.req_ctx[i];
     const int rows = min(kPreRows, n - q0);
     const int n_keys = ctx + q0 + rows;  // keys any row of this tile may see
@@ -631,6 +646,394 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const AttnArgs<bf
     for (int j = 0; j < NT; ++j) {
         if (row_lo < rows) *reinterpret_cast<uint32_t *>(out_lo + j * 8) = pack_bf16(o[j][0] * inv_lo, o[j][1] * inv_lo);
         if (row_hi < rows) *reinterpret_cast<uint32_t *>(out_hi + j * 8) = pack_bf16(o[j][2] * inv_hi, o[j][3] * inv_hi);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Prefill on the fifth-generation tensor cores (bf16, head_dim 64 or 128).
+// CTA = (request, 128 query rows, head), the tiles launched longest first.
+// Both contractions are tcgen05 MMAs with M = 128 query rows, one TMEM lane
+// per row, fp32 accumulators in tensor memory:
+//   S  = Q K^T   A = Q (K-major), B = a tile of 128 keys of K (K-major)
+//   O += P V     A = P (K-major, written by the softmax warps), B = the V tile
+//                read MN-major straight from its [key][dim] TMA image
+// Warp 0 streams Q and 128-key tiles of K and of V by TMA (two stages each,
+// on separate barriers, so S can start before V has landed).  Warp 1 issues
+// S_{j+1} while the softmax warps work on S_j, then O += P_j V_j.  Warps 2-5
+// hold one query row per thread: the scale, the causal mask (row r at
+// position ctx + q0 + r sees keys 0 .. ctx + q0 + r, masked by index), the
+// running max m and sum l in fp32, and P_j = exp2(S_j - m) rounded to bf16
+// (l sums the rounded weights).  O is rescaled in TMEM (read, scaled, written
+// back) only when a row's max has grown by more than 2^8 since m was last
+// set: every P is formed against the m that O and l carry, so the result is
+// the same up to rounding, and P stays below 2^8.  The last tile may reach
+// past the tile's keys into slots of other requests or slots never written:
+// those scores are masked by index and those V rows zeroed in shared memory
+// before P V reads them.
+// ---------------------------------------------------------------------------
+constexpr int kPtRows = 128;         // query rows per CTA (== kPrefillRowsPerTile)
+constexpr int kPtKeys = 128;         // keys per tile
+constexpr int kPtThreads = 192;      // TMA warp, MMA warp, four softmax warps
+constexpr uint32_t kPtAtom = 16384;  // 128 rows x 128 bytes: one 128-byte-swizzled block
+constexpr float kPtRescale = 8.f;    // log2 growth of a row's max that triggers a rescale of O
+constexpr uint32_t kPtTmemCols = 512;
+constexpr uint32_t kPtTmemO = 256;   // O's columns; S_0 and S_1 take 0 .. 255
+
+template <int D>
+struct PtLayout {  // byte offsets from the 1024-aligned base of dynamic shared memory
+    static constexpr int kAtoms = D / 64;  // 64-dim blocks of a row of Q, K, V
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kK = kQ + kAtoms * kPtAtom;      // 2 stages
+    static constexpr uint32_t kV = kK + 2 * kAtoms * kPtAtom;  // 2 stages
+    static constexpr uint32_t kP = kV + 2 * kAtoms * kPtAtom;  // 2 buffers of 2 blocks (keys 0-63, 64-127)
+    static constexpr uint32_t kBars = kP + 4 * kPtAtom;
+    static constexpr uint32_t kBytes = kBars + 256 + 1024;     // barriers, alignment slack
+};
+
+struct PtBars {
+    uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], drain;
+    uint32_t tmem;
+    int abort;
+};
+
+// Shared-memory matrix descriptor for an MN-major operand written by TMA with
+// 128-byte swizzling as blocks of [K rows][64 MN elements]: rows 128 B apart,
+// 8-row groups 1024 B apart (stride byte offset), 64-element MN blocks
+// `mn_block` bytes apart (leading byte offset); version 1, swizzle mode 2.
+__device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr, uint32_t mn_block) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((mn_block >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+                 "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+                   "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+}
+// Waits for this thread's TMEM loads; the registers are operands, so no use
+// of them is placed before the wait.
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t *r) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+                   "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+                 "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+                 :
+                 : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                   "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+                   "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+                   "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPtThreads, 1)
+    attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmkv,
+                           const AttnArgs<bf16> a) {
+    using L = PtLayout<D>;
+    extern __shared__ uint8_t pt_smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(pt_smem_raw) + 1023) & ~uintptr_t(1023));
+    PtBars &bar = *reinterpret_cast<PtBars *>(sm + L::kBars);
+    volatile int *abort = &bar.abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // longest first: a request's later query tiles see more keys
+    const int tile = (int)gridDim.x - 1 - (int)blockIdx.x, h = (int)blockIdx.y;
+
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+        mbar_init(&bar.q_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bar.k_full[b], 1);
+            mbar_init(&bar.k_empty[b], 1);
+            mbar_init(&bar.v_full[b], 1);
+            mbar_init(&bar.v_empty[b], 1);
+            mbar_init(&bar.s_full[b], 1);
+            mbar_init(&bar.p_full[b], 4);  // one arrival per softmax warp
+            mbar_init(&bar.pv_done[b], 1);
+        }
+        mbar_init(&bar.drain, 1);
+        *abort = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmq);
+        prefetch_tmap(&tmkv);
+    }
+    if (warp == 1) {
+        tmem_alloc(&bar.tmem, kPtTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar.tmem;
+    pdl_wait();  // q and this iteration's K/V rows come from the kernels before
+
+    const int i = a.p.pre_tiles[2 * tile], q0 = a.p.pre_tiles[2 * tile + 1];
+    const int off = a.p.req_off[i], n = a.p.req_off[i + 1] - off, ctx = a.p.req_ctx[i];
+    const int kv0 = a.p.req_kvoff[i];
+    const int rows = min(kPtRows, n - q0);
+    const int n_keys = ctx + q0 + rows;  // keys any row of this tile may see
+    const int n_kt = (n_keys + kPtKeys - 1) / kPtKeys;
+    constexpr unsigned kFull = 0xffffffffu;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        const bool leader = elect_one();
+        const uint64_t pol = l2_policy_evict_normal();  // every query tile of the request reads them
+        if (leader) {
+            mbar_arrive_expect_tx(&bar.q_full, L::kAtoms * kPtAtom);
+            for (int c = 0; c < L::kAtoms; ++c)
+                tma_load_2d(sm + L::kQ + c * kPtAtom, &tmq, &bar.q_full, h * D + 64 * c, off + q0);
+        }
+        __syncwarp();
+        int issued_k = 0, issued_v = 0;  // key tiles whose K / V loads were issued
+        bool ok = true;
+        for (int j = 0; j < n_kt; ++j) {
+            const int b = j & 1;
+            const uint32_t ep = (uint32_t)((j - 2) >> 1) & 1u;  // parity of the release of tile j - 2
+            if (j >= 2 && !__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.k_empty[b], ep, a.err))) {
+                ok = false;
+                break;
+            }
+            if (leader) {
+                mbar_arrive_expect_tx(&bar.k_full[b], L::kAtoms * kPtAtom);
+                for (int c = 0; c < L::kAtoms; ++c)
+                    tma_load_3d_hint(sm + L::kK + (b * L::kAtoms + c) * kPtAtom, &tmkv, &bar.k_full[b], 64 * c,
+                                     kv0 + j * kPtKeys, h, pol);
+            }
+            __syncwarp();
+            issued_k = j + 1;
+            if (j >= 2 && !__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.v_empty[b], ep, a.err))) {
+                ok = false;
+                break;
+            }
+            if (leader) {
+                mbar_arrive_expect_tx(&bar.v_full[b], L::kAtoms * kPtAtom);
+                for (int c = 0; c < L::kAtoms; ++c)
+                    tma_load_3d_hint(sm + L::kV + (b * L::kAtoms + c) * kPtAtom, &tmkv, &bar.v_full[b], 64 * c,
+                                     kv0 + j * kPtKeys, a.n_heads + h, pol);
+            }
+            __syncwarp();
+            issued_v = j + 1;
+        }
+        if (!ok) {
+            *abort = 1;
+            // let the copies in flight (each barrier's latest tile at most) land before the CTA exits
+            if (leader) {
+                for (int j = max(0, issued_k - 2); j < issued_k; ++j)
+                    mbar_wait_bounded(&bar.k_full[j & 1], (uint32_t)(j >> 1) & 1u, a.err);
+                for (int j = max(0, issued_v - 2); j < issued_v; ++j)
+                    mbar_wait_bounded(&bar.v_full[j & 1], (uint32_t)(j >> 1) & 1u, a.err);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        const bool leader = elect_one();
+        const uint32_t idesc_s = idesc_bf16_f32(kPtRows, kPtKeys);
+        const uint32_t idesc_pv = idesc_bf16_f32(kPtRows, D) | (1u << 16);  // B (V) MN-major
+        const uint32_t q_s = smem_u32(sm + L::kQ);
+        auto issue_s = [&](int j) {
+            const int b = j & 1;
+            if (!__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.k_full[b], (uint32_t)(j >> 1) & 1u, a.err)))
+                return false;
+            tc_fence_after();
+            const uint32_t k_s = smem_u32(sm + L::kK + b * L::kAtoms * kPtAtom);
+            if (leader) {
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {  // 16 dims per MMA: 32 B within a 64-dim block
+                    const uint32_t o = (uint32_t)(ks >> 2) * kPtAtom + (uint32_t)(ks & 3) * 32u;
+                    tc_mma_f16(tmem + (uint32_t)(b * kPtKeys), smem_desc_k128(q_s + o), smem_desc_k128(k_s + o),
+                               idesc_s, (uint32_t)(ks != 0));
+                }
+                tc_commit(&bar.k_empty[b]);
+                tc_commit(&bar.s_full[b]);
+            }
+            __syncwarp();
+            return true;
+        };
+        auto issue_pv = [&](int j) {
+            const int b = j & 1;
+            const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+            if (!__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.p_full[b], ph, a.err) &&
+                                       mbar_wait_bounded(&bar.v_full[b], ph, a.err)))
+                return false;
+            tc_fence_after();
+            const uint32_t p_s = smem_u32(sm + L::kP + b * 2 * kPtAtom);
+            const uint32_t v_s = smem_u32(sm + L::kV + b * L::kAtoms * kPtAtom);
+            if (leader) {
+#pragma unroll
+                for (int ks = 0; ks < kPtKeys / 16; ++ks)  // 16 keys per MMA: two 8-row groups of V
+                    tc_mma_f16(tmem + kPtTmemO,
+                               smem_desc_k128(p_s + (uint32_t)(ks >> 2) * kPtAtom + (uint32_t)(ks & 3) * 32u),
+                               smem_desc_mn128(v_s + (uint32_t)ks * 2048u, kPtAtom), idesc_pv,
+                               (uint32_t)(j != 0 || ks != 0));
+                tc_commit(&bar.v_empty[b]);
+                tc_commit(&bar.pv_done[b]);
+            }
+            __syncwarp();
+            return true;
+        };
+        bool ok = __all_sync(kFull, mbar_wait_bounded(&bar.q_full, 0u, a.err)) && issue_s(0);
+        for (int j = 0; ok && j < n_kt; ++j) {
+            if (j + 1 < n_kt) ok = issue_s(j + 1);  // S_{j+1} runs while the softmax warps work on S_j
+            if (ok) ok = issue_pv(j);
+        }
+        if (!ok) *abort = 1;
+        // every MMA issued has completed before the stages and TMEM are released
+        if (leader) tc_commit(&bar.drain);
+        __syncwarp();
+        mbar_wait_bounded(&bar.drain, 0u, a.err);
+    } else {
+        // ------------------------------ softmax ------------------------------
+        const int quarter = warp & 3;  // TMEM lanes 32 * (warp % 4) ..
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_t = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int row_keys = min(ctx + q0 + r + 1, n_keys);  // keys 0 .. row_keys - 1 are this row's
+        float m = kNegBig, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_kt; ++j) {
+            const int b = j & 1, kbase = j * kPtKeys;
+            if (!__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.s_full[b], (uint32_t)(j >> 1) & 1u, a.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t s[kPtKeys];
+#pragma unroll
+            for (int c = 0; c < kPtKeys / 32; ++c) tmem_ld32(lane_t + (uint32_t)(b * kPtKeys + 32 * c), s + 32 * c);
+#pragma unroll
+            for (int c = 0; c < kPtKeys / 32; ++c) tmem_wait_ld32(s + 32 * c);
+            const int valid = min(max(row_keys - kbase, 0), kPtKeys);
+            float mx = kNegBig;
+#pragma unroll
+            for (int c = 0; c < kPtKeys; ++c) {
+                const float v = c < valid ? __uint_as_float(s[c]) * a.scale_log2 : kNegBig;
+                s[c] = __float_as_uint(v);
+                mx = fmaxf(mx, v);
+            }
+            float alpha = 1.f;
+            if (j == 0) {
+                m = mx;
+            } else if (mx > m + kPtRescale) {
+                alpha = exp2f(m - mx);
+                m = mx;
+                l *= alpha;
+            }
+            // P buffer b was read by P_{j-2} V_{j-2}
+            if (j >= 2 &&
+                !__all_sync(kFull, mbar_wait_bounded(&bar.pv_done[b], (uint32_t)((j - 2) >> 1) & 1u, a.err))) {
+                ok = false;
+                break;
+            }
+            if (__any_sync(kFull, alpha != 1.f)) {
+                // O = P_0 V_0 + .. + P_{j-1} V_{j-1}: once the last of them is done, scale it
+                if (!__all_sync(kFull, mbar_wait_bounded(&bar.pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u,
+                                                         a.err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_t + kPtTmemO + 32 * c, o);
+                    tmem_wait_ld32(o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(lane_t + kPtTmemO + 32 * c, o);
+                }
+                tmem_wait_st();
+            }
+            // P_j: row r of two 64-key blocks, 16-byte chunk c at position c ^ (r % 8)
+            const uint32_t p_row = smem_u32(sm + L::kP + b * 2 * kPtAtom) + (uint32_t)r * 128u;
+            float ls = 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < kPtKeys / 8; ++c8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat162 pv = __floats2bfloat162_rn(exp2f(__uint_as_float(s[8 * c8 + 2 * e]) - m),
+                                                                    exp2f(__uint_as_float(s[8 * c8 + 2 * e + 1]) - m));
+                    ls += __low2float(pv) + __high2float(pv);
+                    w[e] = *reinterpret_cast<const uint32_t *>(&pv);
+                }
+                st_shared_v4(p_row + (uint32_t)(c8 >> 3) * kPtAtom + ((uint32_t)((c8 & 7) ^ (r & 7)) << 4), w[0], w[1],
+                             w[2], w[3]);
+            }
+            l += ls;
+            // the tile's V rows past its keys: zero (once they have landed) before P V reads them
+            const int tile_keys = min(n_keys - kbase, kPtKeys);
+            if (tile_keys < kPtKeys) {
+                if (!__all_sync(kFull, mbar_wait_bounded(&bar.v_full[b], (uint32_t)(j >> 1) & 1u, a.err))) {
+                    ok = false;
+                    break;
+                }
+                if (r >= tile_keys)
+#pragma unroll
+                    for (int c = 0; c < L::kAtoms; ++c)
+#pragma unroll
+                        for (int x = 0; x < 8; ++x)
+                            st_shared_v4(smem_u32(sm + L::kV + (b * L::kAtoms + c) * kPtAtom) + (uint32_t)r * 128u +
+                                             16u * x,
+                                         0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();  // P (and the zeroed rows) before the tensor core reads them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.p_full[b]);
+        }
+        if (ok)
+            ok = __all_sync(kFull, !*abort && mbar_wait_bounded(&bar.pv_done[(n_kt - 1) & 1],
+                                                                (uint32_t)((n_kt - 1) >> 1) & 1u, a.err));
+        if (ok) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            bf16 *dst = a.out + (size_t)(off + q0 + r) * a.H + h * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(lane_t + kPtTmemO + 32 * c, o);
+                tmem_wait_ld32(o);
+                if (r < rows) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * inv,
+                                                                       __uint_as_float(o[2 * e + 1]) * inv);
+                        w[e] = *reinterpret_cast<const uint32_t *>(&v);
+                    }
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) d4[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+                }
+            }
+        } else {
+            *abort = 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kPtTmemCols);
     }
 }
 
@@ -1034,8 +1437,29 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
                 cudaError_t e = max_smem_once((const void *)attn_prefill_mma_kernel<D>, (int)sizeof(PrefillSmem<D>));
                 if (e != cudaSuccess) return e;
             }
-            cudaError_t e = launch_pdl(attn_prefill_mma_kernel<D>, dim3(a.p.n_pre_tiles, a.n_heads), dim3(128),
-                                       sizeof(PrefillSmem<D>), st, a);
+            cudaError_t e = cudaSuccess;
+            if (a.p.n_rows > 0 && override_prefill_tc() >= 0) {
+                // q as [rows][3H] (boxes of 64 dims x 128 rows), the pool as [K|V][head] planes of [slot][D]
+                CUtensorMap tmq, tmkv;
+                const uint64_t qdims[2] = {(uint64_t)3 * a.H, (uint64_t)a.p.n_rows};
+                const uint64_t qstrides[1] = {(uint64_t)3 * a.H * 2};
+                const uint32_t qbox[2] = {64, kPtRows};
+                const uint64_t kdims[3] = {(uint64_t)D, (uint64_t)a.kv_slots, (uint64_t)2 * a.n_heads};
+                const uint64_t kstrides[2] = {(uint64_t)D * 2, (uint64_t)a.kv_slots * D * 2};
+                const uint32_t kbox[3] = {64, kPtKeys, 1};
+                if (!encode_tensor_map(&tmq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.qkv, qdims, qstrides, qbox,
+                                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+                    !encode_tensor_map(&tmkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.kpool, kdims, kstrides, kbox,
+                                       CU_TENSOR_MAP_SWIZZLE_128B))
+                    return cudaErrorInvalidValue;
+                e = max_smem_once((const void *)attn_prefill_tc_kernel<D>, (int)PtLayout<D>::kBytes);
+                if (e != cudaSuccess) return e;
+                e = launch_pdl(attn_prefill_tc_kernel<D>, dim3(a.p.n_pre_tiles, a.n_heads), dim3(kPtThreads),
+                               PtLayout<D>::kBytes, st, tmq, tmkv, a);
+            } else {
+                e = launch_pdl(attn_prefill_mma_kernel<D>, dim3(a.p.n_pre_tiles, a.n_heads, 2), dim3(128),
+                               sizeof(PrefillSmem<D>), st, a);
+            }
             if (e != cudaSuccess) return e;
         } else {
             cudaError_t e = launch_pdl(attn_prefill_kernel<T, D>, dim3(a.p.n_pre_tiles, a.n_heads),
@@ -1227,6 +1651,7 @@ extern "C" int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, con
     ap.n_dec_work = (int)n_work;
     ap.n_pre_tiles = 0;
     ap.chunk = chunk;
+    ap.n_rows = 0;
     const int H = n_heads * head_dim;
     cudaError_t ce =
         dtype == 1 ? attention<bf16>((const bf16 *)qkv, (const bf16 *)kv_layer, kv_slots, (bf16 *)out, ap, H, n_heads,

@@ -123,6 +123,7 @@ struct AttnPlan {
     const int32_t *dec_items;
     const int32_t *pre_tiles;                        // prefill (request, first row) tiles
     int n_dec_work, n_pre_tiles, chunk;
+    int n_rows;  // rows of the qkv matrix (bounds the tcgen05 prefill's q loads; 0: that kernel is not used)
 };
 
 // Attention for one layer.  Decode: requests with one input row, split-K over
@@ -144,7 +145,7 @@ void decode_items(const int32_t *order, const int32_t *dec_work, int n_work, con
 // next[b] = argmax_j logits[b, j] (lowest j on ties); also to out2 if non-null.
 cudaError_t argmax_rows(const float *logits, int n_rows, int V, int32_t *next, int32_t *out2, cudaStream_t st);
 
-constexpr int kPrefillRowsPerTile = 64;
+constexpr int kPrefillRowsPerTile = 128;  // query rows per prefill tile (the tcgen05 kernel's M)
 
 // A bounded wait that nothing satisfies, given up after limit_ns (failure-
 // detection tests of the device error word).

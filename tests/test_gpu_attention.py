@@ -103,3 +103,75 @@ def test_attention_13b_head_shape(eng):
     got = run_op(eng, "bf16", reqs, offs, kv_slots, pool, qkv, n_heads, d)
     ref = oracle_out(reqs, offs, pool, qkv, n_heads, d)
     assert rel(got, ref) < 2e-2
+
+
+def used_slots(reqs, offs, kv_slots):
+    used = np.zeros(kv_slots, bool)
+    for (n, c), off in zip(reqs, offs):
+        used[off:off + c + n] = True
+    return used
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_prefill_tc_multi_tile(eng, d):
+    """The tcgen05 prefill at the prompt lengths of the traces: several 128-key
+    tiles per query tile, ragged query tiles (127 rows; 513 and 129 rows leave one),
+    cached context before the prompt (chunked prefill) and the causal diagonal
+    inside a key tile (the test engine takes up to 1024 rows)."""
+    n_heads = 2
+    reqs = [(513, 0), (127, 300), (129, 0), (1, 5), (128, 128), (100, 77)]
+    offs, kv_slots, pool, qkv = make_case(4, n_heads, d, reqs, "bf16")
+    got = run_op(eng, "bf16", reqs, offs, kv_slots, pool, qkv, n_heads, d)
+    ref = oracle_out(reqs, offs, pool, qkv, n_heads, d)
+    assert rel(got, ref) < 2e-2
+
+
+def test_prefill_tc_rescale(eng):
+    """Keys whose scale grows along the sequence, so a row's max keeps growing by
+    more than 2^8 from tile to tile and O is rescaled in tensor memory many
+    times."""
+    n_heads, d = 2, 128
+    reqs = [(600, 0), (300, 400), (60, 0)]
+    offs, kv_slots, pool, qkv = make_case(5, n_heads, d, reqs, "bf16")
+    for (n, c), off in zip(reqs, offs):
+        t = np.arange(c + n, dtype=np.float32)
+        pool[0, :, off:off + c + n, :] *= (1.0 + t / 48.0)[None, :, None]
+    pool = synth.bf16_round(pool)
+    got = run_op(eng, "bf16", reqs, offs, kv_slots, pool, qkv, n_heads, d)
+    ref = oracle_out(reqs, offs, pool, qkv, n_heads, d)
+    assert np.isfinite(got).all()
+    assert rel(got, ref) < 2e-2
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_attention_ignores_foreign_slots(eng, d):
+    """Every pool slot that holds none of the batch's keys is NaN (slots between
+    reservations and after the last): the prefill tile that reaches past its
+    keys and the decode items must neither read them into a score nor let P V
+    carry them into a row."""
+    n_heads = 2
+    reqs = [(200, 0), (1, 77), (130, 10), (1, 300), (3, 0), (64, 64)]
+    offs, kv_slots, pool, qkv = make_case(6, n_heads, d, reqs, "bf16")
+    pool[:, :, ~used_slots(reqs, offs, kv_slots), :] = np.nan
+    got = run_op(eng, "bf16", reqs, offs, kv_slots, pool, qkv, n_heads, d)
+    clean = np.where(np.isnan(pool), 0.0, pool).astype(np.float32)
+    ref = oracle_out(reqs, offs, clean, qkv, n_heads, d)
+    assert np.isfinite(got).all()
+    assert rel(got, ref) < 2e-2
+
+
+def test_prefill_mma_sync_kernel_when_chosen(eng):
+    """The mma.sync prefill kernel (kept for comparisons, ORCA_ATTN_PREFILL_TC=-1,
+    read once per process): the 128-row plan tiles as two 64-row halves."""
+    import json
+    import os
+    import subprocess
+    import sys
+    child = os.path.join(os.path.dirname(__file__), "prefill_kernel_child.py")
+    env = dict(os.environ, ORCA_ATTN_PREFILL_TC="-1")
+    out = subprocess.run([sys.executable, child], env=env, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    rows = [json.loads(line) for line in out.stdout.splitlines() if line.startswith("{")]
+    assert len(rows) == 2
+    for r in rows:
+        assert r["rel"] < 2e-2, r
