@@ -659,25 +659,30 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const AttnArgs<bf
 //                read MN-major straight from its [key][dim] TMA image
 // Warp 0 streams Q and 128-key tiles of K and of V by TMA (two stages each,
 // on separate barriers, so S can start before V has landed).  Warp 1 issues
-// S_{j+1} while the softmax warps work on S_j, then O += P_j V_j.  Warps 2-5
-// hold one query row per thread: the scale, the causal mask (row r at
-// position ctx + q0 + r sees keys 0 .. ctx + q0 + r, masked by index), the
-// running max m and sum l in fp32, and P_j = exp2(S_j - m) rounded to bf16
-// (l sums the rounded weights).  O is rescaled in TMEM (read, scaled, written
-// back) only when a row's max has grown by more than 2^8 since m was last
-// set: every P is formed against the m that O and l carry, so the result is
-// the same up to rounding, and P stays below 2^8.  The last tile may reach
-// past the tile's keys into slots of other requests or slots never written:
-// those scores are masked by index and those V rows zeroed in shared memory
-// before P V reads them.
+// S_{j+1} while the softmax warps work on S_j, then O += P_j V_j.  Warps 2-9
+// hold half a query row per thread (two warps per TMEM lane quarter, 64 keys
+// of each tile and half of O's columns; a row's two halves meet in shared
+// memory for its max and its sum): the scale, the causal mask (row r at
+// position ctx + q0 + r sees keys 0 .. ctx + q0 + r, masked by index where a
+// tile reaches past some row's last key), the running max m and sum l in
+// fp32, and P_j = exp2(S_j - m) rounded to bf16 for the MMA.  O is rescaled
+// in TMEM (read, scaled, written back) only when a row's max has grown by
+// more than 2^8 since m was last set: every P is formed against the m that
+// O and l carry, so the result is the same up to rounding, and P stays below
+// 2^8.  The last tile may reach past the tile's keys into slots of other
+// requests or slots never written: those scores are masked by index and
+// those V rows zeroed in shared memory before P V reads them.
 // ---------------------------------------------------------------------------
 constexpr int kPtRows = 128;         // query rows per CTA (== kPrefillRowsPerTile)
 constexpr int kPtKeys = 128;         // keys per tile
-constexpr int kPtThreads = 192;      // TMA warp, MMA warp, four softmax warps
+constexpr int kPtThreads = 320;      // TMA warp, MMA warp, eight softmax warps (two per TMEM lane quarter)
 constexpr uint32_t kPtAtom = 16384;  // 128 rows x 128 bytes: one 128-byte-swizzled block
 constexpr float kPtRescale = 8.f;    // log2 growth of a row's max that triggers a rescale of O
 constexpr uint32_t kPtTmemCols = 512;
 constexpr uint32_t kPtTmemO = 256;   // O's columns; S_0 and S_1 take 0 .. 255
+// Device error bit: a kernel's dynamic shared memory did not start 1024-byte
+// aligned (its swizzled tiles need it); the kernel did nothing.
+constexpr unsigned kErrSmemAlign = 8u;
 
 template <int D>
 struct PtLayout {  // byte offsets from the 1024-aligned base of dynamic shared memory
@@ -687,11 +692,13 @@ struct PtLayout {  // byte offsets from the 1024-aligned base of dynamic shared 
     static constexpr uint32_t kV = kK + 2 * kAtoms * kPtAtom;  // 2 stages
     static constexpr uint32_t kP = kV + 2 * kAtoms * kPtAtom;  // 2 buffers of 2 blocks (keys 0-63, 64-127)
     static constexpr uint32_t kBars = kP + 4 * kPtAtom;
-    static constexpr uint32_t kBytes = kBars + 256 + 1024;     // barriers, alignment slack
+    static constexpr uint32_t kRed = kBars + 256;              // [2 tiles][2 halves][128 rows] floats
+    static constexpr uint32_t kBytes = kRed + 2048;            // (the base must be 1024-aligned: checked)
 };
 
 struct PtBars {
     uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], drain;
+    uint64_t pair[4];  // the two softmax warps of each TMEM lane quarter
     uint32_t tmem;
     int abort;
 };
@@ -741,6 +748,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
                  : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 2^x by the SFU's approximation (flush-to-zero; 2^-inf = +0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -750,8 +763,12 @@ __global__ void __launch_bounds__(kPtThreads, 1)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmkv,
                            const AttnArgs<bf16> a) {
     using L = PtLayout<D>;
-    extern __shared__ uint8_t pt_smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(pt_smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t pt_smem_raw[];
+    if (smem_u32(pt_smem_raw) & 1023u) {  // uniform: every thread leaves before any barrier
+        if (threadIdx.x == 0) raise_err(a.err, kErrSmemAlign);
+        return;
+    }
+    uint8_t *sm = pt_smem_raw;
     PtBars &bar = *reinterpret_cast<PtBars *>(sm + L::kBars);
     volatile int *abort = &bar.abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -767,10 +784,11 @@ __global__ void __launch_bounds__(kPtThreads, 1)
             mbar_init(&bar.v_full[b], 1);
             mbar_init(&bar.v_empty[b], 1);
             mbar_init(&bar.s_full[b], 1);
-            mbar_init(&bar.p_full[b], 4);  // one arrival per softmax warp
+            mbar_init(&bar.p_full[b], 8);  // one arrival per softmax warp
             mbar_init(&bar.pv_done[b], 1);
         }
         mbar_init(&bar.drain, 1);
+        for (int q = 0; q < 4; ++q) mbar_init(&bar.pair[q], 2);
         *abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tmq);
@@ -903,10 +921,28 @@ __global__ void __launch_bounds__(kPtThreads, 1)
         mbar_wait_bounded(&bar.drain, 0u, a.err);
     } else {
         // ------------------------------ softmax ------------------------------
-        const int quarter = warp & 3;  // TMEM lanes 32 * (warp % 4) ..
+        // Two warps per TMEM lane quarter: warps 2-5 take keys 0-63 of their
+        // rows, warps 6-9 keys 64-127 (and the matching halves of O's
+        // columns); the two halves of a row meet in shared memory for its max
+        // and, at the end, its sum.
+        const int quarter = warp & 3;      // TMEM lanes 32 * (warp % 4) ..
+        const int half = (warp - 2) >> 2;  // which 64 keys of a tile, which half of O's columns
         const int r = quarter * 32 + lane;
         const uint32_t lane_t = tmem + ((uint32_t)(quarter * 32) << 16);
+        float *red = reinterpret_cast<float *>(sm + L::kRed);  // [tile parity][half][row]
+        auto red_at = [&](int parity, int hf) { return red + (parity * 2 + hf) * kPtRows + r; };
+        // the two warps of a quarter meet on its mbarrier (one arrival each, a bounded wait)
+        int n_pair = 0;
+        auto pair_sync = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.pair[quarter]);
+            const bool met = __all_sync(kFull, mbar_wait_bounded(&bar.pair[quarter], (uint32_t)(n_pair & 1), a.err));
+            ++n_pair;
+            return met;
+        };
+        constexpr int kOc = D / 2;  // O columns of this half
         const int row_keys = min(ctx + q0 + r + 1, n_keys);  // keys 0 .. row_keys - 1 are this row's
+        const int first_keys = min(ctx + q0 + 1, n_keys);    // the fewest any row of the tile sees
         float m = kNegBig, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kt; ++j) {
@@ -916,24 +952,35 @@ __global__ void __launch_bounds__(kPtThreads, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t s[kPtKeys];
+            uint32_t s[64];
+            tmem_ld32(lane_t + (uint32_t)(b * kPtKeys + 64 * half), s);
+            tmem_ld32(lane_t + (uint32_t)(b * kPtKeys + 64 * half + 32), s + 32);
+            tmem_wait_ld32(s);
+            tmem_wait_ld32(s + 32);
+            // every row sees all of this tile's keys, or a prefix of them (masked by index)
+            const bool whole = kbase + kPtKeys <= first_keys;
+            const int valid = whole ? 64 : min(max(row_keys - kbase - 64 * half, 0), 64);
+            if (!whole) {
 #pragma unroll
-            for (int c = 0; c < kPtKeys / 32; ++c) tmem_ld32(lane_t + (uint32_t)(b * kPtKeys + 32 * c), s + 32 * c);
-#pragma unroll
-            for (int c = 0; c < kPtKeys / 32; ++c) tmem_wait_ld32(s + 32 * c);
-            const int valid = min(max(row_keys - kbase, 0), kPtKeys);
+                for (int c = 0; c < 64; ++c)
+                    if (c >= valid) s[c] = __float_as_uint(kNegBig);
+            }
             float mx = kNegBig;
 #pragma unroll
-            for (int c = 0; c < kPtKeys; ++c) {
-                const float v = c < valid ? __uint_as_float(s[c]) * a.scale_log2 : kNegBig;
-                s[c] = __float_as_uint(v);
-                mx = fmaxf(mx, v);
+            for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+            // (a slot of parity j & 1 is written again at tile j + 2, after the partner
+            // has read it: it reads before arriving at tile j + 1's meeting)
+            *red_at(j & 1, half) = mx;
+            if (!pair_sync()) {
+                ok = false;
+                break;
             }
+            mx = fmaxf(mx, *red_at(j & 1, half ^ 1)) * a.scale_log2;  // (scale > 0)
             float alpha = 1.f;
             if (j == 0) {
                 m = mx;
             } else if (mx > m + kPtRescale) {
-                alpha = exp2f(m - mx);
+                alpha = ex2_approx(m - mx);
                 m = mx;
                 l *= alpha;
             }
@@ -944,7 +991,7 @@ __global__ void __launch_bounds__(kPtThreads, 1)
                 break;
             }
             if (__any_sync(kFull, alpha != 1.f)) {
-                // O = P_0 V_0 + .. + P_{j-1} V_{j-1}: once the last of them is done, scale it
+                // O = P_0 V_0 + .. + P_{j-1} V_{j-1}: once the last of them is done, scale this half of it
                 if (!__all_sync(kFull, mbar_wait_bounded(&bar.pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u,
                                                          a.err))) {
                     ok = false;
@@ -952,48 +999,49 @@ __global__ void __launch_bounds__(kPtThreads, 1)
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < kOc / 32; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(lane_t + kPtTmemO + 32 * c, o);
+                    const uint32_t ta = lane_t + kPtTmemO + (uint32_t)(kOc * half + 32 * c);
+                    tmem_ld32(ta, o);
                     tmem_wait_ld32(o);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(lane_t + kPtTmemO + 32 * c, o);
+                    tmem_st32(ta, o);
                 }
                 tmem_wait_st();
             }
-            // P_j: row r of two 64-key blocks, 16-byte chunk c at position c ^ (r % 8)
-            const uint32_t p_row = smem_u32(sm + L::kP + b * 2 * kPtAtom) + (uint32_t)r * 128u;
+            // P_j, this half: row r of 64-key block `half`, 16-byte chunk c at position c ^ (r % 8);
+            // masked keys hold kNegBig, whose exp2 is 0
+            const uint32_t p_row = smem_u32(sm + L::kP + (b * 2 + half) * kPtAtom) + (uint32_t)r * 128u;
+            const float neg_m = -m;
             float ls = 0.f;
 #pragma unroll
-            for (int c8 = 0; c8 < kPtKeys / 8; ++c8) {
+            for (int c8 = 0; c8 < 8; ++c8) {
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const __nv_bfloat162 pv = __floats2bfloat162_rn(exp2f(__uint_as_float(s[8 * c8 + 2 * e]) - m),
-                                                                    exp2f(__uint_as_float(s[8 * c8 + 2 * e + 1]) - m));
-                    ls += __low2float(pv) + __high2float(pv);
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(s[8 * c8 + 2 * e]), a.scale_log2, neg_m));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(s[8 * c8 + 2 * e + 1]), a.scale_log2, neg_m));
+                    ls += p0 + p1;
+                    const __nv_bfloat162 pv = __floats2bfloat162_rn(p0, p1);
                     w[e] = *reinterpret_cast<const uint32_t *>(&pv);
                 }
-                st_shared_v4(p_row + (uint32_t)(c8 >> 3) * kPtAtom + ((uint32_t)((c8 & 7) ^ (r & 7)) << 4), w[0], w[1],
-                             w[2], w[3]);
+                st_shared_v4(p_row + ((uint32_t)(c8 ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
             }
             l += ls;
-            // the tile's V rows past its keys: zero (once they have landed) before P V reads them
+            // the tile's V rows past its keys: zeroed (once they have landed) before P V reads them
             const int tile_keys = min(n_keys - kbase, kPtKeys);
             if (tile_keys < kPtKeys) {
                 if (!__all_sync(kFull, mbar_wait_bounded(&bar.v_full[b], (uint32_t)(j >> 1) & 1u, a.err))) {
                     ok = false;
                     break;
                 }
-                if (r >= tile_keys)
+                if (half < L::kAtoms && r >= tile_keys)
 #pragma unroll
-                    for (int c = 0; c < L::kAtoms; ++c)
-#pragma unroll
-                        for (int x = 0; x < 8; ++x)
-                            st_shared_v4(smem_u32(sm + L::kV + (b * L::kAtoms + c) * kPtAtom) + (uint32_t)r * 128u +
-                                             16u * x,
-                                         0u, 0u, 0u, 0u);
+                    for (int x = 0; x < 8; ++x)
+                        st_shared_v4(smem_u32(sm + L::kV + (b * L::kAtoms + half) * kPtAtom) + (uint32_t)r * 128u +
+                                         16u * x,
+                                     0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();  // P (and the zeroed rows) before the tensor core reads them
             tc_fence_before();
@@ -1003,14 +1051,20 @@ __global__ void __launch_bounds__(kPtThreads, 1)
         if (ok)
             ok = __all_sync(kFull, !*abort && mbar_wait_bounded(&bar.pv_done[(n_kt - 1) & 1],
                                                                 (uint32_t)((n_kt - 1) >> 1) & 1u, a.err));
+        // the row's sum: both halves (in the slots of the parity the last tile did not use)
+        if (ok) {
+            *red_at(n_kt & 1, half) = l;
+            ok = pair_sync();
+            l += *red_at(n_kt & 1, half ^ 1);
+        }
         if (ok) {
             tc_fence_after();
             const float inv = 1.f / l;
-            bf16 *dst = a.out + (size_t)(off + q0 + r) * a.H + h * D;
+            bf16 *dst = a.out + (size_t)(off + q0 + r) * a.H + h * D + kOc * half;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < kOc / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld32(lane_t + kPtTmemO + 32 * c, o);
+                tmem_ld32(lane_t + kPtTmemO + (uint32_t)(kOc * half + 32 * c), o);
                 tmem_wait_ld32(o);
                 if (r < rows) {
                     uint32_t w[16];
