@@ -328,6 +328,7 @@ int build(orca_engine *E, const orca_batch *b, int32_t *buf, int64_t cap, bool p
         }
     }
     req_off[B] = r;
+    prefill_order(pre_tiles, tiles, req_off, req_ctx);
     decode_order(dec_work, lay.n_dec_work, req_keys, lay.chunk, buf + lay.off[P_DECORDER]);
     decode_items(buf + lay.off[P_DECORDER], dec_work, lay.n_dec_work, req_off, req_keys, req_kv, dec_wb, dec_nch,
                  lay.chunk, buf + lay.off[P_DECITEM]);
@@ -935,6 +936,7 @@ int orca_op_attention(orca_engine *E, int32_t dtype, const void *qkv, const void
         r += n_input[i];
     }
     req_off[n_req] = r;
+    prefill_order(pre_tiles, tiles, req_off, req_ctx);
     decode_order(dec_work, lay.n_dec_work, req_keys, lay.chunk, buf + lay.off[P_DECORDER]);
     decode_items(buf + lay.off[P_DECORDER], dec_work, lay.n_dec_work, req_off, req_keys, req_kv, dec_wb, dec_nch,
                  lay.chunk, buf + lay.off[P_DECITEM]);

@@ -651,7 +651,10 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const AttnArgs<bf
 
 // ---------------------------------------------------------------------------
 // Prefill on the fifth-generation tensor cores (bf16, head_dim 64 or 128).
-// CTA = (request, 128 query rows, head), the tiles launched longest first.
+// Persistent: one CTA per SM walks items (head, 128 query rows of a request),
+// TMEM and barriers set up once; the next item's Q and first keys load and
+// its first S runs while this item finishes, and O has two TMEM buffers so
+// that an item's P V can start while the last item's O is written out.
 // Both contractions are tcgen05 MMAs with M = 128 query rows, one TMEM lane
 // per row, fp32 accumulators in tensor memory:
 //   S  = Q K^T   A = Q (K-major), B = a tile of 128 keys of K (K-major)
@@ -679,7 +682,8 @@ constexpr int kPtThreads = 320;      // TMA warp, MMA warp, eight softmax warps 
 constexpr uint32_t kPtAtom = 16384;  // 128 rows x 128 bytes: one 128-byte-swizzled block
 constexpr float kPtRescale = 8.f;    // log2 growth of a row's max that triggers a rescale of O
 constexpr uint32_t kPtTmemCols = 512;
-constexpr uint32_t kPtTmemO = 256;   // O's columns; S_0 and S_1 take 0 .. 255
+constexpr uint32_t kPtTmemO = 256;   // O's two buffers; S_0 and S_1 take columns 0 .. 255
+constexpr uint32_t kPtOCols = 128;   // columns per O buffer (head_dim <= 128)
 // Device error bit: a kernel's dynamic shared memory did not start 1024-byte
 // aligned (its swizzled tiles need it); the kernel did nothing.
 constexpr unsigned kErrSmemAlign = 8u;
@@ -697,7 +701,8 @@ struct PtLayout {  // byte offsets from the 1024-aligned base of dynamic shared 
 };
 
 struct PtBars {
-    uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], drain;
+    uint64_t q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2];
+    uint64_t o_free[2], drain;
     uint64_t pair[4];  // the two softmax warps of each TMEM lane quarter
     uint32_t tmem;
     int abort;
@@ -772,12 +777,12 @@ __global__ void __launch_bounds__(kPtThreads, 1)
     PtBars &bar = *reinterpret_cast<PtBars *>(sm + L::kBars);
     volatile int *abort = &bar.abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // longest first: a request's later query tiles see more keys
-    const int tile = (int)gridDim.x - 1 - (int)blockIdx.x, h = (int)blockIdx.y;
+    constexpr unsigned kFull = 0xffffffffu;
 
     pdl_trigger();
     if (threadIdx.x == 0) {
         mbar_init(&bar.q_full, 1);
+        mbar_init(&bar.q_empty, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bar.k_full[b], 1);
             mbar_init(&bar.k_empty[b], 1);
@@ -786,6 +791,7 @@ __global__ void __launch_bounds__(kPtThreads, 1)
             mbar_init(&bar.s_full[b], 1);
             mbar_init(&bar.p_full[b], 8);  // one arrival per softmax warp
             mbar_init(&bar.pv_done[b], 1);
+            mbar_init(&bar.o_free[b], 8);
         }
         mbar_init(&bar.drain, 1);
         for (int q = 0; q < 4; ++q) mbar_init(&bar.pair[q], 2);
@@ -804,62 +810,92 @@ __global__ void __launch_bounds__(kPtThreads, 1)
     const uint32_t tmem = bar.tmem;
     pdl_wait();  // q and this iteration's K/V rows come from the kernels before
 
-    const int i = a.p.pre_tiles[2 * tile], q0 = a.p.pre_tiles[2 * tile + 1];
-    const int off = a.p.req_off[i], n = a.p.req_off[i + 1] - off, ctx = a.p.req_ctx[i];
-    const int kv0 = a.p.req_kvoff[i];
-    const int rows = min(kPtRows, n - q0);
-    const int n_keys = ctx + q0 + rows;  // keys any row of this tile may see
-    const int n_kt = (n_keys + kPtKeys - 1) / kPtKeys;
-    constexpr unsigned kFull = 0xffffffffu;
+    // This CTA's items: b, b + G, ... of (head, tile) with the tiles of a head
+    // innermost (the query tiles of one request, which read the same keys,
+    // run at about the same time), each head's tiles in the plan's order
+    // (longest first).
+    const int n_items = a.p.n_pre_tiles * a.n_heads;
+    struct Item {
+        int h, off, q0, ctx, kv0, rows, n_keys, n_kt;
+    };
+    auto item_at = [&](int k) {
+        Item it;
+        const int idx = (int)blockIdx.x + k * (int)gridDim.x;
+        it.h = idx / a.p.n_pre_tiles;
+        const int t = idx - it.h * a.p.n_pre_tiles;
+        const int i = a.p.pre_tiles[2 * t];
+        it.q0 = a.p.pre_tiles[2 * t + 1];
+        it.off = a.p.req_off[i];
+        it.ctx = a.p.req_ctx[i];
+        it.kv0 = a.p.req_kvoff[i];
+        it.rows = min(kPtRows, a.p.req_off[i + 1] - it.off - it.q0);
+        it.n_keys = it.ctx + it.q0 + it.rows;  // keys any row of the tile may see
+        it.n_kt = (it.n_keys + kPtKeys - 1) / kPtKeys;
+        return it;
+    };
+    const int n_mine = n_items > (int)blockIdx.x ? (n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    // Phases: key tiles are numbered g = 0, 1, .. across this CTA's items (K/V
+    // stage, S buffer, P buffer: g & 1; the barrier's use: g >> 1), items k =
+    // 0, 1, .. (Q: k; O buffer k & 1, its use k >> 1).
 
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         const bool leader = elect_one();
         const uint64_t pol = l2_policy_evict_normal();  // every query tile of the request reads them
-        if (leader) {
-            mbar_arrive_expect_tx(&bar.q_full, L::kAtoms * kPtAtom);
-            for (int c = 0; c < L::kAtoms; ++c)
-                tma_load_2d(sm + L::kQ + c * kPtAtom, &tmq, &bar.q_full, h * D + 64 * c, off + q0);
-        }
-        __syncwarp();
-        int issued_k = 0, issued_v = 0;  // key tiles whose K / V loads were issued
+        int g = 0, q_issued = 0, k_issued = 0, v_issued = 0;
         bool ok = true;
-        for (int j = 0; j < n_kt; ++j) {
-            const int b = j & 1;
-            const uint32_t ep = (uint32_t)((j - 2) >> 1) & 1u;  // parity of the release of tile j - 2
-            if (j >= 2 && !__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.k_empty[b], ep, a.err))) {
+        for (int k = 0; k < n_mine && ok; ++k) {
+            const Item it = item_at(k);
+            // Q of item k - 1 has been read by its last S
+            if (k >= 1 && !__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.q_empty, (uint32_t)(k - 1) & 1u, a.err))) {
                 ok = false;
                 break;
             }
             if (leader) {
-                mbar_arrive_expect_tx(&bar.k_full[b], L::kAtoms * kPtAtom);
+                mbar_arrive_expect_tx(&bar.q_full, L::kAtoms * kPtAtom);
                 for (int c = 0; c < L::kAtoms; ++c)
-                    tma_load_3d_hint(sm + L::kK + (b * L::kAtoms + c) * kPtAtom, &tmkv, &bar.k_full[b], 64 * c,
-                                     kv0 + j * kPtKeys, h, pol);
+                    tma_load_2d(sm + L::kQ + c * kPtAtom, &tmq, &bar.q_full, it.h * D + 64 * c, it.off + it.q0);
             }
             __syncwarp();
-            issued_k = j + 1;
-            if (j >= 2 && !__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.v_empty[b], ep, a.err))) {
-                ok = false;
-                break;
+            q_issued = k + 1;
+            for (int j = 0; j < it.n_kt; ++j, ++g) {
+                const int b = g & 1;
+                const uint32_t ep = (uint32_t)((g - 2) >> 1) & 1u;  // the release of tile g - 2
+                if (g >= 2 && !__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.k_empty[b], ep, a.err))) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    mbar_arrive_expect_tx(&bar.k_full[b], L::kAtoms * kPtAtom);
+                    for (int c = 0; c < L::kAtoms; ++c)
+                        tma_load_3d_hint(sm + L::kK + (b * L::kAtoms + c) * kPtAtom, &tmkv, &bar.k_full[b], 64 * c,
+                                         it.kv0 + j * kPtKeys, it.h, pol);
+                }
+                __syncwarp();
+                k_issued = g + 1;
+                if (g >= 2 && !__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.v_empty[b], ep, a.err))) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    mbar_arrive_expect_tx(&bar.v_full[b], L::kAtoms * kPtAtom);
+                    for (int c = 0; c < L::kAtoms; ++c)
+                        tma_load_3d_hint(sm + L::kV + (b * L::kAtoms + c) * kPtAtom, &tmkv, &bar.v_full[b], 64 * c,
+                                         it.kv0 + j * kPtKeys, a.n_heads + it.h, pol);
+                }
+                __syncwarp();
+                v_issued = g + 1;
             }
-            if (leader) {
-                mbar_arrive_expect_tx(&bar.v_full[b], L::kAtoms * kPtAtom);
-                for (int c = 0; c < L::kAtoms; ++c)
-                    tma_load_3d_hint(sm + L::kV + (b * L::kAtoms + c) * kPtAtom, &tmkv, &bar.v_full[b], 64 * c,
-                                     kv0 + j * kPtKeys, a.n_heads + h, pol);
-            }
-            __syncwarp();
-            issued_v = j + 1;
         }
         if (!ok) {
             *abort = 1;
-            // let the copies in flight (each barrier's latest tile at most) land before the CTA exits
+            // let the copies in flight (each barrier's latest use at most) land before the CTA exits
             if (leader) {
-                for (int j = max(0, issued_k - 2); j < issued_k; ++j)
-                    mbar_wait_bounded(&bar.k_full[j & 1], (uint32_t)(j >> 1) & 1u, a.err);
-                for (int j = max(0, issued_v - 2); j < issued_v; ++j)
-                    mbar_wait_bounded(&bar.v_full[j & 1], (uint32_t)(j >> 1) & 1u, a.err);
+                if (q_issued > 0) mbar_wait_bounded(&bar.q_full, (uint32_t)(q_issued - 1) & 1u, a.err);
+                for (int x = max(0, k_issued - 2); x < k_issued; ++x)
+                    mbar_wait_bounded(&bar.k_full[x & 1], (uint32_t)(x >> 1) & 1u, a.err);
+                for (int x = max(0, v_issued - 2); x < v_issued; ++x)
+                    mbar_wait_bounded(&bar.v_full[x & 1], (uint32_t)(x >> 1) & 1u, a.err);
             }
         }
     } else if (warp == 1) {
@@ -868,9 +904,11 @@ __global__ void __launch_bounds__(kPtThreads, 1)
         const uint32_t idesc_s = idesc_bf16_f32(kPtRows, kPtKeys);
         const uint32_t idesc_pv = idesc_bf16_f32(kPtRows, D) | (1u << 16);  // B (V) MN-major
         const uint32_t q_s = smem_u32(sm + L::kQ);
-        auto issue_s = [&](int j) {
-            const int b = j & 1;
-            if (!__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.k_full[b], (uint32_t)(j >> 1) & 1u, a.err)))
+        // S of key tile g (the item's j-th): Q K_g^T into S buffer g & 1; the item's
+        // last S also releases Q
+        auto issue_s = [&](int g, bool last) {
+            const int b = g & 1;
+            if (!__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.k_full[b], (uint32_t)(g >> 1) & 1u, a.err)))
                 return false;
             tc_fence_after();
             const uint32_t k_s = smem_u32(sm + L::kK + b * L::kAtoms * kPtAtom);
@@ -883,13 +921,15 @@ __global__ void __launch_bounds__(kPtThreads, 1)
                 }
                 tc_commit(&bar.k_empty[b]);
                 tc_commit(&bar.s_full[b]);
+                if (last) tc_commit(&bar.q_empty);
             }
             __syncwarp();
             return true;
         };
-        auto issue_pv = [&](int j) {
-            const int b = j & 1;
-            const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+        // O (buffer ob) += P_g V_g; the item's first overwrites O
+        auto issue_pv = [&](int g, int ob, bool first) {
+            const int b = g & 1;
+            const uint32_t ph = (uint32_t)(g >> 1) & 1u;
             if (!__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.p_full[b], ph, a.err) &&
                                        mbar_wait_bounded(&bar.v_full[b], ph, a.err)))
                 return false;
@@ -899,20 +939,44 @@ __global__ void __launch_bounds__(kPtThreads, 1)
             if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < kPtKeys / 16; ++ks)  // 16 keys per MMA: two 8-row groups of V
-                    tc_mma_f16(tmem + kPtTmemO,
+                    tc_mma_f16(tmem + kPtTmemO + (uint32_t)(ob * kPtOCols),
                                smem_desc_k128(p_s + (uint32_t)(ks >> 2) * kPtAtom + (uint32_t)(ks & 3) * 32u),
                                smem_desc_mn128(v_s + (uint32_t)ks * 2048u, kPtAtom), idesc_pv,
-                               (uint32_t)(j != 0 || ks != 0));
+                               (uint32_t)(!first || ks != 0));
                 tc_commit(&bar.v_empty[b]);
                 tc_commit(&bar.pv_done[b]);
             }
             __syncwarp();
             return true;
         };
-        bool ok = __all_sync(kFull, mbar_wait_bounded(&bar.q_full, 0u, a.err)) && issue_s(0);
-        for (int j = 0; ok && j < n_kt; ++j) {
-            if (j + 1 < n_kt) ok = issue_s(j + 1);  // S_{j+1} runs while the softmax warps work on S_j
-            if (ok) ok = issue_pv(j);
+        // S runs one key tile ahead of P V across item boundaries, so the next
+        // item's first S is done while the softmax warps finish this item
+        int k_next = 0, j_next = 0, g_next = 0;  // the next S: item k_next, its tile j_next
+        int nkt_next = n_mine > 0 ? item_at(0).n_kt : 0;
+        auto issue_next_s = [&]() {
+            if (j_next == 0 &&
+                !__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.q_full, (uint32_t)k_next & 1u, a.err)))
+                return false;
+            if (!issue_s(g_next, j_next + 1 == nkt_next)) return false;
+            ++g_next;
+            if (++j_next == nkt_next) {
+                j_next = 0;
+                if (++k_next < n_mine) nkt_next = item_at(k_next).n_kt;
+            }
+            return true;
+        };
+        bool ok = n_mine == 0 || issue_next_s();
+        int g = 0;
+        for (int k = 0; ok && k < n_mine; ++k) {
+            const int n_kt = item_at(k).n_kt, ob = k & 1;
+            for (int j = 0; ok && j < n_kt; ++j, ++g) {
+                if (k_next < n_mine) ok = issue_next_s();
+                // O buffer ob was read out by the softmax warps at the end of item k - 2
+                if (ok && j == 0 && k >= 2)
+                    ok = __all_sync(kFull, !*abort && mbar_wait_bounded(&bar.o_free[ob],
+                                                                        (uint32_t)((k - 2) >> 1) & 1u, a.err));
+                if (ok) ok = issue_pv(g, ob, j == 0);
+            }
         }
         if (!ok) *abort = 1;
         // every MMA issued has completed before the stages and TMEM are released
@@ -924,149 +988,155 @@ __global__ void __launch_bounds__(kPtThreads, 1)
         // Two warps per TMEM lane quarter: warps 2-5 take keys 0-63 of their
         // rows, warps 6-9 keys 64-127 (and the matching halves of O's
         // columns); the two halves of a row meet in shared memory for its max
-        // and, at the end, its sum.
+        // and, at the end of an item, its sum.
         const int quarter = warp & 3;      // TMEM lanes 32 * (warp % 4) ..
         const int half = (warp - 2) >> 2;  // which 64 keys of a tile, which half of O's columns
         const int r = quarter * 32 + lane;
         const uint32_t lane_t = tmem + ((uint32_t)(quarter * 32) << 16);
-        float *red = reinterpret_cast<float *>(sm + L::kRed);  // [tile parity][half][row]
-        auto red_at = [&](int parity, int hf) { return red + (parity * 2 + hf) * kPtRows + r; };
-        // the two warps of a quarter meet on its mbarrier (one arrival each, a bounded wait)
+        float *red = reinterpret_cast<float *>(sm + L::kRed);  // [meeting parity][half][row]
+        // the two warps of a quarter meet on its mbarrier (one arrival each, a bounded wait);
+        // meeting z exchanges through the slots of parity z & 1, which are written
+        // again at meeting z + 2, after the partner has read them (it reads before
+        // arriving at meeting z + 1)
         int n_pair = 0;
-        auto pair_sync = [&]() {
+        auto exchange = [&](float v, bool &met) {
+            float *slot = red + ((n_pair & 1) * 2 + half) * kPtRows + r;
+            *slot = v;
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.pair[quarter]);
-            const bool met = __all_sync(kFull, mbar_wait_bounded(&bar.pair[quarter], (uint32_t)(n_pair & 1), a.err));
+            met = __all_sync(kFull, mbar_wait_bounded(&bar.pair[quarter], (uint32_t)(n_pair & 1), a.err));
+            const float other = slot[(1 - 2 * half) * kPtRows];  // the same row's other half
             ++n_pair;
-            return met;
+            return other;
         };
         constexpr int kOc = D / 2;  // O columns of this half
-        const int row_keys = min(ctx + q0 + r + 1, n_keys);  // keys 0 .. row_keys - 1 are this row's
-        const int first_keys = min(ctx + q0 + 1, n_keys);    // the fewest any row of the tile sees
-        float m = kNegBig, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_kt; ++j) {
-            const int b = j & 1, kbase = j * kPtKeys;
-            if (!__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.s_full[b], (uint32_t)(j >> 1) & 1u, a.err))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t s[64];
-            tmem_ld32(lane_t + (uint32_t)(b * kPtKeys + 64 * half), s);
-            tmem_ld32(lane_t + (uint32_t)(b * kPtKeys + 64 * half + 32), s + 32);
-            tmem_wait_ld32(s);
-            tmem_wait_ld32(s + 32);
-            // every row sees all of this tile's keys, or a prefix of them (masked by index)
-            const bool whole = kbase + kPtKeys <= first_keys;
-            const int valid = whole ? 64 : min(max(row_keys - kbase - 64 * half, 0), 64);
-            if (!whole) {
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (c >= valid) s[c] = __float_as_uint(kNegBig);
-            }
-            float mx = kNegBig;
-#pragma unroll
-            for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
-            // (a slot of parity j & 1 is written again at tile j + 2, after the partner
-            // has read it: it reads before arriving at tile j + 1's meeting)
-            *red_at(j & 1, half) = mx;
-            if (!pair_sync()) {
-                ok = false;
-                break;
-            }
-            mx = fmaxf(mx, *red_at(j & 1, half ^ 1)) * a.scale_log2;  // (scale > 0)
-            float alpha = 1.f;
-            if (j == 0) {
-                m = mx;
-            } else if (mx > m + kPtRescale) {
-                alpha = ex2_approx(m - mx);
-                m = mx;
-                l *= alpha;
-            }
-            // P buffer b was read by P_{j-2} V_{j-2}
-            if (j >= 2 &&
-                !__all_sync(kFull, mbar_wait_bounded(&bar.pv_done[b], (uint32_t)((j - 2) >> 1) & 1u, a.err))) {
-                ok = false;
-                break;
-            }
-            if (__any_sync(kFull, alpha != 1.f)) {
-                // O = P_0 V_0 + .. + P_{j-1} V_{j-1}: once the last of them is done, scale this half of it
-                if (!__all_sync(kFull, mbar_wait_bounded(&bar.pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u,
-                                                         a.err))) {
+        int g = 0;
+        for (int k = 0; k < n_mine && ok; ++k) {
+            const Item it = item_at(k);
+            const int ob = k & 1;
+            const uint32_t o_t = lane_t + kPtTmemO + (uint32_t)(ob * kPtOCols + kOc * half);  // this half of O
+            const int row_keys = min(it.ctx + it.q0 + r + 1, it.n_keys);  // keys 0 .. row_keys - 1 are this row's
+            const int first_keys = min(it.ctx + it.q0 + 1, it.n_keys);    // the fewest any row of the tile sees
+            float m = kNegBig, l = 0.f;
+            for (int j = 0; j < it.n_kt; ++j, ++g) {
+                const int b = g & 1, kbase = j * kPtKeys;
+                if (!__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.s_full[b], (uint32_t)(g >> 1) & 1u, a.err))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                uint32_t s[64];
+                tmem_ld32(lane_t + (uint32_t)(b * kPtKeys + 64 * half), s);
+                tmem_ld32(lane_t + (uint32_t)(b * kPtKeys + 64 * half + 32), s + 32);
+                tmem_wait_ld32(s);
+                tmem_wait_ld32(s + 32);
+                // every row sees all of this tile's keys, or a prefix of them (masked by index)
+                const bool whole = kbase + kPtKeys <= first_keys;
+                if (!whole) {
+                    const int valid = min(max(row_keys - kbase - 64 * half, 0), 64);
 #pragma unroll
-                for (int c = 0; c < kOc / 32; ++c) {
-                    uint32_t o[32];
-                    const uint32_t ta = lane_t + kPtTmemO + (uint32_t)(kOc * half + 32 * c);
-                    tmem_ld32(ta, o);
-                    tmem_wait_ld32(o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(ta, o);
+                    for (int c = 0; c < 64; ++c)
+                        if (c >= valid) s[c] = __float_as_uint(kNegBig);
                 }
-                tmem_wait_st();
-            }
-            // P_j, this half: row r of 64-key block `half`, 16-byte chunk c at position c ^ (r % 8);
-            // masked keys hold kNegBig, whose exp2 is 0
-            const uint32_t p_row = smem_u32(sm + L::kP + (b * 2 + half) * kPtAtom) + (uint32_t)r * 128u;
-            const float neg_m = -m;
-            float ls = 0.f;
+                float mx = kNegBig;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(s[8 * c8 + 2 * e]), a.scale_log2, neg_m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(s[8 * c8 + 2 * e + 1]), a.scale_log2, neg_m));
-                    ls += p0 + p1;
-                    const __nv_bfloat162 pv = __floats2bfloat162_rn(p0, p1);
-                    w[e] = *reinterpret_cast<const uint32_t *>(&pv);
-                }
-                st_shared_v4(p_row + ((uint32_t)(c8 ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
-            }
-            l += ls;
-            // the tile's V rows past its keys: zeroed (once they have landed) before P V reads them
-            const int tile_keys = min(n_keys - kbase, kPtKeys);
-            if (tile_keys < kPtKeys) {
-                if (!__all_sync(kFull, mbar_wait_bounded(&bar.v_full[b], (uint32_t)(j >> 1) & 1u, a.err))) {
+                for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+                bool met;
+                mx = fmaxf(mx, exchange(mx, met)) * a.scale_log2;  // (scale > 0)
+                if (!met) {
                     ok = false;
                     break;
                 }
-                if (half < L::kAtoms && r >= tile_keys)
+                float alpha = 1.f;
+                if (j == 0) {
+                    m = mx;
+                } else if (mx > m + kPtRescale) {
+                    alpha = ex2_approx(m - mx);
+                    m = mx;
+                    l *= alpha;
+                }
+                // P buffer b was read by the P V of key tile g - 2
+                if (g >= 2 &&
+                    !__all_sync(kFull, mbar_wait_bounded(&bar.pv_done[b], (uint32_t)((g - 2) >> 1) & 1u, a.err))) {
+                    ok = false;
+                    break;
+                }
+                if (__any_sync(kFull, alpha != 1.f)) {
+                    // O = the item's P V so far: once the last of them (tile g - 1) is done, scale this half
+                    if (!__all_sync(kFull, mbar_wait_bounded(&bar.pv_done[(g - 1) & 1], (uint32_t)((g - 1) >> 1) & 1u,
+                                                             a.err))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                    for (int x = 0; x < 8; ++x)
-                        st_shared_v4(smem_u32(sm + L::kV + (b * L::kAtoms + half) * kPtAtom) + (uint32_t)r * 128u +
-                                         16u * x,
-                                     0u, 0u, 0u, 0u);
+                    for (int c = 0; c < kOc / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(o_t + 32 * c, o);
+                        tmem_wait_ld32(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(o_t + 32 * c, o);
+                    }
+                    tmem_wait_st();
+                }
+                // P_g, this half: row r of 64-key block `half`, 16-byte chunk c at position c ^ (r % 8);
+                // masked keys hold kNegBig, whose exp2 is 0
+                const uint32_t p_row = smem_u32(sm + L::kP + (b * 2 + half) * kPtAtom) + (uint32_t)r * 128u;
+                const float neg_m = -m;
+                float ls = 0.f;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float p0 = ex2_approx(fmaf(__uint_as_float(s[8 * c8 + 2 * e]), a.scale_log2, neg_m));
+                        const float p1 = ex2_approx(fmaf(__uint_as_float(s[8 * c8 + 2 * e + 1]), a.scale_log2, neg_m));
+                        ls += p0 + p1;
+                        const __nv_bfloat162 pv = __floats2bfloat162_rn(p0, p1);
+                        w[e] = *reinterpret_cast<const uint32_t *>(&pv);
+                    }
+                    st_shared_v4(p_row + ((uint32_t)(c8 ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+                }
+                l += ls;
+                // the tile's V rows past its keys: zeroed (once they have landed) before P V reads them
+                const int tile_keys = min(it.n_keys - kbase, kPtKeys);
+                if (tile_keys < kPtKeys) {
+                    if (!__all_sync(kFull, mbar_wait_bounded(&bar.v_full[b], (uint32_t)(g >> 1) & 1u, a.err))) {
+                        ok = false;
+                        break;
+                    }
+                    if (half < L::kAtoms && r >= tile_keys)
+#pragma unroll
+                        for (int x = 0; x < 8; ++x)
+                            st_shared_v4(smem_u32(sm + L::kV + (b * L::kAtoms + half) * kPtAtom) + (uint32_t)r * 128u +
+                                             16u * x,
+                                         0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();  // P (and the zeroed rows) before the tensor core reads them
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.p_full[b]);
             }
-            fence_proxy_async_smem();  // P (and the zeroed rows) before the tensor core reads them
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.p_full[b]);
-        }
-        if (ok)
-            ok = __all_sync(kFull, !*abort && mbar_wait_bounded(&bar.pv_done[(n_kt - 1) & 1],
-                                                                (uint32_t)((n_kt - 1) >> 1) & 1u, a.err));
-        // the row's sum: both halves (in the slots of the parity the last tile did not use)
-        if (ok) {
-            *red_at(n_kt & 1, half) = l;
-            ok = pair_sync();
-            l += *red_at(n_kt & 1, half ^ 1);
-        }
-        if (ok) {
+            if (!ok) break;
+            // the item's output: once its last P V is done, O / l (the row's sum from both halves)
+            bool met;
+            l += exchange(l, met);
+            if (!met || !__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.pv_done[(g - 1) & 1],
+                                                                         (uint32_t)((g - 1) >> 1) & 1u, a.err))) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             const float inv = 1.f / l;
-            bf16 *dst = a.out + (size_t)(off + q0 + r) * a.H + h * D + kOc * half;
+            bf16 *dst = a.out + (size_t)(it.off + it.q0 + r) * a.H + it.h * D + kOc * half;
 #pragma unroll
             for (int c = 0; c < kOc / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld32(lane_t + kPtTmemO + (uint32_t)(kOc * half + 32 * c), o);
+                tmem_ld32(o_t + 32 * c, o);
                 tmem_wait_ld32(o);
-                if (r < rows) {
+                if (r < it.rows) {
                     uint32_t w[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -1079,9 +1149,12 @@ __global__ void __launch_bounds__(kPtThreads, 1)
                     for (int x = 0; x < 4; ++x) d4[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
                 }
             }
-        } else {
-            *abort = 1;
+            // O buffer ob may take item k + 2
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.o_free[ob]);
         }
+        if (!ok) *abort = 1;
     }
     tc_fence_before();
     __syncthreads();
@@ -1508,8 +1581,13 @@ cudaError_t launch_attn(const AttnArgs<T> &a, bool decode, bool prefill, cudaStr
                     return cudaErrorInvalidValue;
                 e = max_smem_once((const void *)attn_prefill_tc_kernel<D>, (int)PtLayout<D>::kBytes);
                 if (e != cudaSuccess) return e;
-                e = launch_pdl(attn_prefill_tc_kernel<D>, dim3(a.p.n_pre_tiles, a.n_heads), dim3(kPtThreads),
-                               PtLayout<D>::kBytes, st, tmq, tmkv, a);
+                // persistent: one CTA per SM walks the (head, tile) items
+                int sms = 0, dev = 0;
+                cudaGetDevice(&dev);
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+                const int grid = std::max(1, std::min(a.p.n_pre_tiles * a.n_heads, sms));
+                e = launch_pdl(attn_prefill_tc_kernel<D>, dim3(grid), dim3(kPtThreads), PtLayout<D>::kBytes, st, tmq,
+                               tmkv, a);
             } else {
                 e = launch_pdl(attn_prefill_mma_kernel<D>, dim3(a.p.n_pre_tiles, a.n_heads, 2), dim3(128),
                                sizeof(PrefillSmem<D>), st, a);
@@ -1542,6 +1620,18 @@ void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_keys, 
     for (int w = 0; w < n_work; ++w) ++start[chunk - keys(w) + 1];
     for (int b = 1; b <= chunk; ++b) start[b] += start[b - 1];
     for (int w = 0; w < n_work; ++w) order[start[chunk - keys(w)]++] = w;
+}
+
+void prefill_order(int32_t *pre_tiles, int n_tiles, const int32_t *req_off, const int32_t *req_ctx) {
+    struct Tile {
+        int32_t i, q0;
+    };
+    static_assert(sizeof(Tile) == 2 * sizeof(int32_t), "tiles are (request, first row) pairs");
+    Tile *t = reinterpret_cast<Tile *>(pre_tiles);
+    auto keys = [&](const Tile &x) {
+        return req_ctx[x.i] + x.q0 + std::min(kPrefillRowsPerTile, req_off[x.i + 1] - req_off[x.i] - x.q0);
+    };
+    std::stable_sort(t, t + n_tiles, [&](const Tile &x, const Tile &y) { return keys(x) > keys(y); });
 }
 
 void decode_items(const int32_t *order, const int32_t *dec_work, int n_work, const int32_t *req_off,

@@ -137,6 +137,10 @@ cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *ou
 // first (stable), for the persistent decode kernel's load balance.
 // req_keys[i]: the keys request i's items cover (AttnPlan::req_keys).
 void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_keys, int chunk, int32_t *order);
+// Order the prefill tiles ((request, first row) pairs, kPrefillRowsPerTile
+// rows each) by the keys their rows see, most first (stable): the persistent
+// prefill kernel walks them in this order, longest first.
+void prefill_order(int32_t *pre_tiles, int n_tiles, const int32_t *req_off, const int32_t *req_ctx);
 // The 8-word records of AttnPlan::dec_items, in the order of `order`.
 void decode_items(const int32_t *order, const int32_t *dec_work, int n_work, const int32_t *req_off,
                   const int32_t *req_keys, const int32_t *req_kvoff, const int32_t *dec_wbegin, const int32_t *dec_nch,
