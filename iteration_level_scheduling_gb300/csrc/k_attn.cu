@@ -53,6 +53,15 @@ int override_prefill_tc() {
     }();
     return v;
 }
+// ORCA_ATTN_DECODE_EARLY=-1: the decode kernel's producer waits for the
+// previous kernel before its first load (read once; comparisons).
+int override_decode_early() {
+    static const int v = [] {
+        const char *e = getenv("ORCA_ATTN_DECODE_EARLY");
+        return e && *e ? atoi(e) : 0;
+    }();
+    return v;
+}
 
 template <typename T>
 struct AttnArgs {
@@ -67,6 +76,7 @@ struct AttnArgs {
     float *part;
     int *counters;
     unsigned *err;
+    int early;  // the decode producer may load keys before the context end ahead of the grid wait
 };
 
 // One warp attends its query (q, already scaled, VEC values of its lane's
@@ -1264,23 +1274,33 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
         prefetch_tmap(&tm16);
     }
     __syncthreads();
-    pdl_wait();  // this iteration's K/V rows are appended by the previous kernel
 
     // Every wait is bounded; a role whose wait gives up raises the abort flag
     // and leaves, and the others leave at their next wait or item.
     if (warp == kMdProducerWarp) {
         // ------------------------------ producer ------------------------------
+        // This iteration's K/V rows (key ctx of every request, ctx its context
+        // before the iteration) are appended by the previous kernel; the keys
+        // before them were written by earlier iterations.  So the ring's first
+        // stages, while they hold only such keys, are loaded before waiting for
+        // the previous kernel: the stream starts during its tail.
         if (elect_one()) {
             const uint64_t pol = l2_policy_evict_first();  // every cached row is read once per iteration
             uint32_t g = 0, issued = 0;
-            bool ok = true;
-            int4 r0, n0, n1;  // the producer reads only the first half of a record
+            bool ok = true, waited = false;
+            int4 r0, r1, n0, n1;
             if (nth(0) < total) rec(nth(0), n0, n1);
             for (int k = 0, q = nth(0); q < total && ok; q = nth(++k)) {
-                r0 = n0;
+                r0 = n0, r1 = n1;
                 if (nth(k + 1) < total) rec(nth(k + 1), n0, n1);  // the next record, in flight meanwhile
                 const int h = q % a.n_heads, y0 = r0.x, nk = r0.y;
+                // keys [0, old) of the item precede the request's context end
+                const int old = waited || !a.early ? 0 : a.p.req_ctx[r0.w] - r1.w;
                 for (int t = 0; t < nk; t += kMdTok, ++g) {
+                    if (!waited && (issued >= (uint32_t)S || t + min(kMdTok, nk - t) > old)) {
+                        pdl_wait();
+                        waited = true;
+                    }
                     const int s = g % S;
                     if (sm.abort || !mbar_wait_bounded(&sm.empty[s], ((g / S) & 1u) ^ 1u, a.err)) {
                         ok = false;
@@ -1320,6 +1340,7 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
         return;
     }
 
+    pdl_wait();  // q and this iteration's K/V rows come from the previous kernel
     if (warp >= kMdMergerWarp) {
         // ---------------- merge: the consumer warps' states of each item ----------------
         const int mw = warp - kMdMergerWarp;  // items k = mw, mw + kMdMergers, ...
@@ -1664,6 +1685,7 @@ cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *ou
     a.part = part;
     a.counters = counters;
     a.err = err;
+    a.early = override_decode_early() >= 0;
     switch (D) {
         case 16: return launch_attn<T, 16>(a, decode, prefill, st);
         case 32: return launch_attn<T, 32>(a, decode, prefill, st);
