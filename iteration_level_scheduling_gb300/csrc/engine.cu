@@ -392,6 +392,7 @@ int run_plan(orca_engine *E, const int32_t *hp, const int32_t *dp, int32_t *dev_
     ap.n_pre_tiles = hp[P_NPRETILES];
     ap.chunk = hp[P_CHUNK];
     ap.n_rows = hp[P_NROWS];
+    ap.claim = decode_claim_enabled() ? E->attn_cnt + (size_t)E->cfg.max_batch * E->cfg.n_heads : nullptr;
     const int32_t *tokens = dp + hp[P_TOKENS], *row_pos = dp + hp[P_ROWPOS], *row_slot = dp + hp[P_ROWSLOT];
     const int32_t *last_row = dp + hp[P_LASTROW];
     const double dec_keys = hp[P_DECKEYS], pre_keys = hp[P_PREKEYS];
@@ -524,8 +525,9 @@ int check_flag(orca_engine *E) {
     if (*E->h_err == 0) return ORCA_OK;
     *E->h_err = 0;
     cudaMemsetAsync(E->d_err, 0, sizeof(unsigned), E->st);
-    // a kernel that gave up may have left split-request arrival counters part-way
-    cudaMemsetAsync(E->attn_cnt, 0, (size_t)E->cfg.max_batch * E->cfg.n_heads * 4, E->st);
+    // a kernel that gave up may have left split-request arrival counters or the
+    // decode work-claim counters part-way
+    cudaMemsetAsync(E->attn_cnt, 0, ((size_t)E->cfg.max_batch * E->cfg.n_heads + 2) * 4, E->st);
     if (E->sk_cnt) cudaMemsetAsync(E->sk_cnt, 0, (size_t)E->gs_op.sk_cnt_n * 4, E->st);
     cudaStreamSynchronize(E->st);
     return ORCA_ERR_DEVICE_FLAG;
@@ -617,7 +619,8 @@ int orca_engine_create(const orca_model_config *cfg, const orca_weights *w, void
     if (rc == ORCA_OK) rc = dev_alloc(&E->d_plan, (size_t)E->plan_cap * 4);
     if (rc == ORCA_OK && E->part_cap) rc = dev_alloc(&E->part, E->part_cap * 4);
     if (rc == ORCA_OK) rc = dev_alloc(&E->attn_part, (size_t)E->attn_part_work * c.n_heads * (d + 2) * 4);
-    if (rc == ORCA_OK) rc = dev_alloc(&E->attn_cnt, B * c.n_heads * 4);
+    // per-(request, head) arrival counters, then the decode kernel's two work-claim counters
+    if (rc == ORCA_OK) rc = dev_alloc(&E->attn_cnt, (B * c.n_heads + 2) * 4);
     if (rc == ORCA_OK && E->bf) {
         // stream-K GEMM workspace (token rows of any linear layer, the LM head's included)
         E->gs_op.sk_part_floats = gemm_sk_part_floats(E->num_sms);
@@ -639,7 +642,7 @@ int orca_engine_create(const orca_model_config *cfg, const orca_weights *w, void
         E->gs.err = E->d_err;
         E->gs_op.err = E->d_err;
         E->gs_op.num_sms = E->num_sms;
-        if (cudaMemset(E->attn_cnt, 0, B * c.n_heads * 4) != cudaSuccess || cudaMemset(E->d_err, 0, 4) != cudaSuccess ||
+        if (cudaMemset(E->attn_cnt, 0, (B * c.n_heads + 2) * 4) != cudaSuccess || cudaMemset(E->d_err, 0, 4) != cudaSuccess ||
             cudaMemset(E->next, 0, B * 4) != cudaSuccess)
             rc = ORCA_ERR_CUDA;
     }
@@ -961,6 +964,7 @@ int orca_op_attention(orca_engine *E, int32_t dtype, const void *qkv, const void
     ap.n_pre_tiles = lay.n_pre_tiles;
     ap.chunk = lay.chunk;
     ap.n_rows = (int)rows;
+    ap.claim = decode_claim_enabled() ? E->attn_cnt + (size_t)E->cfg.max_batch * E->cfg.n_heads : nullptr;
     const int H = n_heads * head_dim;
     cudaError_t ce;
     if (dtype == ORCA_DTYPE_BF16)

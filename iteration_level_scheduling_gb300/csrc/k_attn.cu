@@ -53,6 +53,21 @@ int override_prefill_tc() {
     }();
     return v;
 }
+}  // namespace
+
+// ORCA_ATTN_DECODE_CLAIM=-1: the tensor-core decode kernel deals every CTA a
+// fixed share of the work items instead of claiming them at run time (read
+// once; comparisons).
+bool decode_claim_enabled() {
+    static const bool on = [] {
+        const char *e = getenv("ORCA_ATTN_DECODE_CLAIM");
+        return !(e && *e && atoi(e) < 0);
+    }();
+    return on;
+}
+
+namespace {
+
 // ORCA_ATTN_DECODE_EARLY=-1: the decode kernel's producer waits for the
 // previous kernel before its first load (read once; comparisons).
 int override_decode_early() {
@@ -1199,6 +1214,7 @@ constexpr int kMdProducerWarp = kMdConsumers, kMdMergerWarp = kMdConsumers + 1;
 constexpr int kMdThreads = 32 * (kMdConsumers + 1 + kMdMergers);
 constexpr int kMdCtasPerSm = 2;
 constexpr int kMdMerge = 4;  // item results queued for the merge warp
+constexpr int kMdIds = 8;    // ring of the CTA's item ids, producer -> consumers
 
 template <int D>
 __host__ __device__ constexpr uint32_t md_stage_bytes() {
@@ -1212,6 +1228,9 @@ template <int D>
 struct MdTail {  // after the ring
     uint64_t full[md_stages<D>()], empty[md_stages<D>()];
     uint64_t mfull[kMdMerge], mempty[kMdMerge];
+    uint64_t id_full[kMdIds];
+    int ids[kMdIds];    // the CTA's j-th item (j >= 1) at [(j - 1) % kMdIds] (>= total: no more)
+    int mq[kMdMerge];   // the item of each merge entry (-1: no more)
     float o[kMdMerge][kMdConsumers][D];  // each consumer warp's unnormalised output of an item
     float m[kMdMerge][kMdConsumers], l[kMdMerge][kMdConsumers];
     volatile int abort;
@@ -1268,6 +1287,7 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
             mbar_init(&sm.mfull[e], kMdConsumers);
             mbar_init(&sm.mempty[e], 1);
         }
+        for (int j = 0; j < kMdIds; ++j) mbar_init(&sm.id_full[j], 1);
         sm.abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tm);
@@ -1284,23 +1304,56 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
         // before them were written by earlier iterations.  So the ring's first
         // stages, while they hold only such keys, are loaded before waiting for
         // the previous kernel: the stream starts during its tail.
+        //
+        // The CTA's items: the first is dealt (entry blockIdx.x, so it can
+        // stream before the wait); the others are claimed at run time from the
+        // plan's counter, in list order (longest first), so that SMs that
+        // stream faster take more -- after the wait, so that a following
+        // launch never claims before this one has ended.  Each is claimed two
+        // items ahead (the atomic's round trip overlaps an item) and its id
+        // handed to the consumer warps before the item before it starts.
+        // Without a counter the k-th item is the dealt entry nth(k).
         if (elect_one()) {
             const uint64_t pol = l2_policy_evict_first();  // every cached row is read once per iteration
             uint32_t g = 0, issued = 0;
-            bool ok = true, waited = false;
+            bool ok = true, waited = false, claiming = a.p.claim != nullptr;
+            int nxt = total, nxt2 = total;  // items k + 1 and k + 2, once known
+            auto take = [&](int j) {  // the CTA's j-th item, j >= 1
+                if (!a.p.claim) return nth(j);
+                const int v = G + atomicAdd(a.p.claim, 1);
+                if (v >= total) {  // this CTA's last claim: the last CTA to finish claiming resets the counters
+                    claiming = false;
+                    if (atomicAdd(a.p.claim + 1, 1) == G - 1) a.p.claim[0] = 0, a.p.claim[1] = 0;
+                }
+                return v;
+            };
+            auto publish = [&](int j, int v) {  // item j's id (j >= 1) for the consumers (the arrive releases it)
+                sm.ids[(j - 1) % kMdIds] = v;
+                mbar_arrive(&sm.id_full[(j - 1) % kMdIds]);
+            };
             int4 r0, r1, n0, n1;
-            if (nth(0) < total) rec(nth(0), n0, n1);
-            for (int k = 0, q = nth(0); q < total && ok; q = nth(++k)) {
+            auto grid_wait = [&]() {  // then items 1 and 2 are claimed, item 1 handed over
+                pdl_wait();
+                waited = true;
+                nxt = take(1);
+                publish(1, nxt);
+                nxt2 = nxt < total ? take(2) : total;
+                if (nxt < total) rec(nxt, n0, n1);  // the next record, in flight meanwhile
+            };
+            rec((int)blockIdx.x, n0, n1);  // (the grid has at most `total` CTAs)
+            for (int k = 0, q = (int)blockIdx.x; q < total && ok; ++k, q = nxt) {
                 r0 = n0, r1 = n1;
-                if (nth(k + 1) < total) rec(nth(k + 1), n0, n1);  // the next record, in flight meanwhile
+                if (k >= 1) {
+                    nxt = nxt2;
+                    publish(k + 1, nxt);
+                    nxt2 = nxt < total ? take(k + 2) : total;
+                    if (nxt < total) rec(nxt, n0, n1);
+                }
                 const int h = q % a.n_heads, y0 = r0.x, nk = r0.y;
                 // keys [0, old) of the item precede the request's context end
                 const int old = waited || !a.early ? 0 : a.p.req_ctx[r0.w] - r1.w;
                 for (int t = 0; t < nk; t += kMdTok, ++g) {
-                    if (!waited && (issued >= (uint32_t)S || t + min(kMdTok, nk - t) > old)) {
-                        pdl_wait();
-                        waited = true;
-                    }
+                    if (!waited && (issued >= (uint32_t)S || t + min(kMdTok, nk - t) > old)) grid_wait();
                     const int s = g % S;
                     if (sm.abort || !mbar_wait_bounded(&sm.empty[s], ((g / S) & 1u) ^ 1u, a.err)) {
                         ok = false;
@@ -1330,6 +1383,7 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
                     }
                     ++issued;
                 }
+                if (ok && !waited) grid_wait();  // the first item held only earlier keys, in fewer than S stages
             }
             if (!ok) {  // let the copies in flight land before the CTA exits
                 sm.abort = 1;
@@ -1344,12 +1398,14 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
     if (warp >= kMdMergerWarp) {
         // ---------------- merge: the consumer warps' states of each item ----------------
         const int mw = warp - kMdMergerWarp;  // items k = mw, mw + kMdMergers, ...
-        for (int k = mw, q = nth(mw); q < total; k += kMdMergers, q = nth(k)) {
+        for (int k = mw;; k += kMdMergers) {
             const int e = k % kMdMerge;
             if (!__all_sync(0xffffffffu, !sm.abort && mbar_wait_bounded(&sm.mfull[e], (k / kMdMerge) & 1u, a.err))) {
                 sm.abort = 1;
                 return;
             }
+            const int q = *reinterpret_cast<volatile int *>(&sm.mq[e]);  // the item, or -1: no more
+            if (q < 0) return;
             int4 r0, r1;
             rec(q, r0, r1);
             const int h = q % a.n_heads, i = r0.w, c = r1.x;
@@ -1435,9 +1491,18 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
         for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qp[8 * ks + t4], qb[ks][1] = qp[8 * ks + 4 + t4];
     };
     uint32_t qn[KS][2];
-    if (nth(0) < total) load_q(nth(0), qn);
+    load_q((int)blockIdx.x, qn);  // (the grid has at most `total` CTAs)
     uint32_t g = 0;
-    for (int k = 0, q = nth(0); q < total; q = nth(++k)) {
+    int k = 0;
+    for (int q = (int)blockIdx.x, q_nx; q < total; ++k, q = q_nx) {
+        // the CTA's next item (handed over before this one's first stage, or after the grid wait)
+        // (item j >= 1 at entry (j - 1) % kMdIds, its (j - 1) / kMdIds-th use)
+        if (!__all_sync(0xffffffffu, !sm.abort && mbar_wait_bounded(&sm.id_full[k % kMdIds],
+                                                                    (uint32_t)(k / kMdIds) & 1u, a.err))) {
+            sm.abort = 1;
+            return;
+        }
+        q_nx = *reinterpret_cast<volatile int *>(&sm.ids[k % kMdIds]);
         int4 r0, r1;
         rec(q, r0, r1);
         const int t0 = 0, t1 = r0.y;  // keys of this item, from its first
@@ -1448,7 +1513,7 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
         uint32_t qb[KS][2];
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qn[ks][0], qb[ks][1] = qn[ks][1];
-        if (nth(k + 1) < total) load_q(nth(k + 1), qn);  // the next item's q, in flight during this one
+        if (q_nx < total) load_q(q_nx, qn);  // the next item's q, in flight during this one
         float m = kNegBig, l = 0.f, o[MT][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -1531,6 +1596,19 @@ __global__ void __launch_bounds__(kMdThreads) attn_decode_mma_kernel(const __gri
         for (int mt = 0; mt < MT; ++mt)
             if ((mt & 3) == t4) sm.o[e][warp][16 * mt + g8] = o[mt][0], sm.o[e][warp][16 * mt + g8 + 8] = o[mt][2];
         if (lane == 0) sm.m[e][warp] = m, sm.l[e][warp] = l;
+        if (lane == 0 && warp == 0) sm.mq[e] = q;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.mfull[e]);
+    }
+    // no more items: the merge warps' next entries (k and k + 1, one for each) say so
+    for (int kk = k; kk < k + kMdMergers; ++kk) {
+        const int e = kk % kMdMerge;
+        if (kk >= kMdMerge &&
+            !__all_sync(0xffffffffu, !sm.abort && mbar_wait_bounded(&sm.mempty[e], ((kk / kMdMerge) - 1) & 1u, a.err))) {
+            sm.abort = 1;
+            return;
+        }
+        if (lane == 0 && warp == 0) sm.mq[e] = -1;
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.mfull[e]);
     }
@@ -1818,6 +1896,7 @@ extern "C" int orca_attention_decode_noalloc(int32_t dtype, const void *qkv, con
     ap.n_pre_tiles = 0;
     ap.chunk = chunk;
     ap.n_rows = 0;
+    ap.claim = nullptr;  // a fixed share per CTA: no counter to keep between calls
     const int H = n_heads * head_dim;
     cudaError_t ce =
         dtype == 1 ? attention<bf16>((const bf16 *)qkv, (const bf16 *)kv_layer, kv_slots, (bf16 *)out, ap, H, n_heads,

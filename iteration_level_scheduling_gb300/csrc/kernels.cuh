@@ -124,6 +124,10 @@ struct AttnPlan {
     const int32_t *pre_tiles;                        // prefill (request, first row) tiles
     int n_dec_work, n_pre_tiles, chunk;
     int n_rows;  // rows of the qkv matrix (bounds the tcgen05 prefill's q loads; 0: that kernel is not used)
+    // two ints, zero between launches: the tensor-core decode kernel claims work
+    // items from [0] at run time, counting finished CTAs in [1] (null: every
+    // CTA takes a fixed share)
+    int *claim;
 };
 
 // Attention for one layer.  Decode: requests with one input row, split-K over
@@ -137,6 +141,9 @@ cudaError_t attention(const T *qkv, const T *pool_layer, int64_t kv_slots, T *ou
 // first (stable), for the persistent decode kernel's load balance.
 // req_keys[i]: the keys request i's items cover (AttnPlan::req_keys).
 void decode_order(const int32_t *dec_work, int n_work, const int32_t *req_keys, int chunk, int32_t *order);
+// Whether the engine gives the decode kernel its work-claim counters
+// (AttnPlan::claim); ORCA_ATTN_DECODE_CLAIM=-1 turns that off.
+bool decode_claim_enabled();
 // Order the prefill tiles ((request, first row) pairs, kPrefillRowsPerTile
 // rows each) by the keys their rows see, most first (stable): the persistent
 // prefill kernel walks them in this order, longest first.
