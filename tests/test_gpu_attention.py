@@ -160,18 +160,46 @@ def test_attention_ignores_foreign_slots(eng, d):
     assert rel(got, ref) < 2e-2
 
 
-def test_prefill_mma_sync_kernel_when_chosen(eng):
-    """The mma.sync prefill kernel (kept for comparisons, ORCA_ATTN_PREFILL_TC=-1,
-    read once per process): the 128-row plan tiles as two 64-row halves."""
+def run_child(env_extra):
     import json
     import os
     import subprocess
     import sys
-    child = os.path.join(os.path.dirname(__file__), "prefill_kernel_child.py")
-    env = dict(os.environ, ORCA_ATTN_PREFILL_TC="-1")
+    child = os.path.join(os.path.dirname(__file__), "attention_kernel_child.py")
+    env = dict(os.environ, **env_extra)
     out = subprocess.run([sys.executable, child], env=env, capture_output=True, text=True, timeout=600)
     assert out.returncode == 0, out.stderr[-2000:]
-    rows = [json.loads(line) for line in out.stdout.splitlines() if line.startswith("{")]
-    assert len(rows) == 2
+    return [json.loads(line) for line in out.stdout.splitlines() if line.startswith("{")]
+
+
+def test_prefill_mma_sync_kernel_when_chosen(eng):
+    """The mma.sync prefill kernel (kept for comparisons, ORCA_ATTN_PREFILL_TC=-1,
+    read once per process): the 128-row plan tiles as two 64-row halves."""
+    rows = run_child({"ORCA_ATTN_PREFILL_TC": "-1"})
+    assert len(rows) == 3
     for r in rows:
         assert r["rel"] < 2e-2, r
+
+
+def test_decode_fixed_share_when_chosen(eng):
+    """The tensor-core decode kernel with a fixed share of work items per CTA
+    (ORCA_ATTN_DECODE_CLAIM=-1, as the allocation-free entry point runs it)
+    instead of items claimed at run time: 48 requests x 40 heads, contexts up
+    to 3000 keys (several items per CTA, split requests merged)."""
+    rows = run_child({"ORCA_ATTN_DECODE_CLAIM": "-1"})
+    assert len(rows) == 3
+    for r in rows:
+        assert r["rel"] < 2e-2, r
+
+
+def test_decode_claimed_many_items_per_cta(eng):
+    """The same decode batch with items claimed at run time, three launches in a
+    row: each finds the claim counters back at zero (a counter left behind
+    would skip items and leave rows unwritten)."""
+    g = np.random.default_rng(7)
+    reqs = [(1, int(c)) for c in g.integers(1, 3000, size=48)]
+    offs, kv_slots, pool, qkv = make_case(7, 40, 128, reqs, "bf16")
+    ref = oracle_out(reqs, offs, pool, qkv, 40, 128)
+    for _ in range(3):
+        got = run_op(eng, "bf16", reqs, offs, kv_slots, pool, qkv, 40, 128)
+        assert rel(got, ref) < 2e-2
