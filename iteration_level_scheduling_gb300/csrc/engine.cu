@@ -201,8 +201,19 @@ struct Layout {
 int rows_of(const Layout &lay, const orca_batch *b, int i) { return lay.padded ? lay.lq : b->n_input[i]; }
 int keys_of(const Layout &lay, const orca_batch *b, int i) { return lay.padded ? lay.lk : b->ctx_len[i] + 1; }
 
+// ORCA_DECODE_CHUNK: the largest decode chunk in keys (64 .. 512, a power of
+// two; tuning); unset = 512.
+int max_decode_chunk() {
+    static const int v = [] {
+        const char *e = getenv("ORCA_DECODE_CHUNK");
+        const int c = e && *e ? atoi(e) : 512;
+        return c == 64 || c == 128 || c == 256 ? c : 512;
+    }();
+    return v;
+}
+
 int decode_chunk(const orca_engine *E, const orca_batch *b, const Layout &lay) {
-    int chunk = 512;
+    int chunk = max_decode_chunk();
     // shrink the chunk until the decode grid has a few CTAs per SM
     while (chunk > 64) {
         int64_t items = 0;
