@@ -701,7 +701,7 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const AttnArgs<bf
 // requests or slots never written: those scores are masked by index and
 // those V rows zeroed in shared memory before P V reads them.
 // ---------------------------------------------------------------------------
-constexpr int kPtRows = 128;         // query rows per CTA (== kPrefillRowsPerTile)
+constexpr int kPtRows = 128;         // query rows per item (== kPrefillRowsPerTile)
 constexpr int kPtKeys = 128;         // keys per tile
 constexpr int kPtThreads = 320;      // TMA warp, MMA warp, eight softmax warps (two per TMEM lane quarter)
 constexpr uint32_t kPtAtom = 16384;  // 128 rows x 128 bytes: one 128-byte-swizzled block
