@@ -1035,6 +1035,49 @@ __global__ void __launch_bounds__(kPtThreads, 1)
             return other;
         };
         constexpr int kOc = D / 2;  // O columns of this half
+        // An item's output is read out of O after the next item's first P has
+        // been written (O has two buffers), so the tensor pipe has that
+        // item's P V and S to work on meanwhile.
+        struct Done {  // a finished item whose output is still in O
+            int k, g_last, row, h, rows;
+            float l;
+        };
+        auto write_out = [&](const Done &e) {
+            bool met;
+            const float lt = e.l + exchange(e.l, met);  // the row's sum over both halves
+            if (!met || !__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.pv_done[e.g_last & 1],
+                                                                       (uint32_t)(e.g_last >> 1) & 1u, a.err)))
+                return false;
+            tc_fence_after();
+            const uint32_t ot = lane_t + kPtTmemO + (uint32_t)((e.k & 1) * kPtOCols + kOc * half);
+            const float inv = 1.f / lt;
+            bf16 *dst = a.out + (size_t)(e.row + r) * a.H + e.h * D + kOc * half;
+#pragma unroll
+            for (int c = 0; c < kOc / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(ot + 32 * c, o);
+                tmem_wait_ld32(o);
+                if (r < e.rows) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(o[2 * x]) * inv,
+                                                                       __uint_as_float(o[2 * x + 1]) * inv);
+                        w[x] = *reinterpret_cast<const uint32_t *>(&v);
+                    }
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) d4[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+                }
+            }
+            // O buffer k & 1 may take item k + 2
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.o_free[e.k & 1]);
+            return true;
+        };
+        Done late{};
+        bool has_late = false;
         bool ok = true;
         int g = 0;
         for (int k = 0; k < n_mine && ok; ++k) {
@@ -1143,42 +1186,19 @@ __global__ void __launch_bounds__(kPtThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.p_full[b]);
-            }
-            if (!ok) break;
-            // the item's output: once its last P V is done, O / l (the row's sum from both halves)
-            bool met;
-            l += exchange(l, met);
-            if (!met || !__all_sync(kFull, !*abort && mbar_wait_bounded(&bar.pv_done[(g - 1) & 1],
-                                                                         (uint32_t)((g - 1) >> 1) & 1u, a.err))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const float inv = 1.f / l;
-            bf16 *dst = a.out + (size_t)(it.off + it.q0 + r) * a.H + it.h * D + kOc * half;
-#pragma unroll
-            for (int c = 0; c < kOc / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(o_t + 32 * c, o);
-                tmem_wait_ld32(o);
-                if (r < it.rows) {
-                    uint32_t w[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * inv,
-                                                                       __uint_as_float(o[2 * e + 1]) * inv);
-                        w[e] = *reinterpret_cast<const uint32_t *>(&v);
+                if (j == 0 && has_late) {  // the item before: its output, now that this item's first P is out
+                    if (!write_out(late)) {
+                        ok = false;
+                        break;
                     }
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) d4[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+                    has_late = false;
                 }
             }
-            // O buffer ob may take item k + 2
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.o_free[ob]);
+            if (!ok) break;
+            late = Done{k, g - 1, it.off + it.q0, it.h, it.rows, l};
+            has_late = true;
         }
+        if (ok && has_late) ok = write_out(late);
         if (!ok) *abort = 1;
     }
     tc_fence_before();

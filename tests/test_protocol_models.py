@@ -176,7 +176,18 @@ def prefill_cta(items, rnd):
                 g += 1
 
     def softmax():
+        # an item's output is read out after the next item's first P is written
+        # (O has two buffers), so that P V's of the next item run meanwhile
+        def epilogue(k, g_last):
+            while not waitable(pv[g_last & 1], g_last >> 1):
+                yield
+            assert g_last in pv_done_tiles, ("O read before the item's last P V", k)
+            o_read.add(k)
+            of[k & 1].arrive(8)
+            yield
+
         g = 0
+        late = None  # (item, its last key tile) whose output is still to be read
         for k in range(n):
             for j in range(items[k]):
                 b = g & 1
@@ -197,12 +208,12 @@ def prefill_cta(items, rnd):
                 pf[b].arrive(8)
                 yield
                 g += 1
-            while not waitable(pv[(g - 1) & 1], (g - 1) >> 1):
-                yield
-            assert g - 1 in pv_done_tiles, ("O read before the item's last P V", k)
-            o_read.add(k)
-            of[k & 1].arrive(8)
-            yield
+                if j == 0 and late is not None:
+                    yield from epilogue(*late)
+                    late = None
+            late = (k, g - 1)
+        if late is not None:
+            yield from epilogue(*late)
 
     return [producer(), mma(), softmax()], pending
 
